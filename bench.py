@@ -1,0 +1,389 @@
+"""Benchmark of the heterogeneous-batch paged LoRA delta on one layer.
+
+One step = the whole hot path over one batch: group the batch's tokens by
+adapter (build_segments), then y += s (x A_a) B_a for the layer's q, k, v, o
+projections (one multi-projection apply).  The workload is the Llama-7B-shaped
+decode batch: H = 4096, 256 tokens (one per request), 1000 adapters of ranks
+{8, 16, 32, 64} resident in a pre-fragmented pool, token -> adapter Zipf(1),
+fp16.  L2 is flushed (a 256 MiB device write) before every timed step, so
+adapter pages, x and y come from HBM; only the steps themselves are timed,
+with CUDA events on the compute stream.
+
+Printed: one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+on a bounded sample of the same workload instead (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "lora_delta_tokens_per_s_per_layer"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+
+# ncu DRAM counters of the dominant kernel (dram__bytes_read.sum + write.sum,
+# per launch) on the benchmark workload, with the hash of the kernel source
+# they were taken from; reported as null once the source has changed.
+NCU_TRAFFIC = {}
+
+
+def _kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("kernels.cu", "tc_kernels.cu", "internal.h"):
+        p = os.path.join(ROOT, "lora_adapters_gb300", "csrc", f)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------- workload
+def algorithmic_bytes(wl, elt=2):
+    """Per kernel and per step: x read + distinct adapter rows + y read/write.
+
+    shrink: T_a * H_in (x) + sum over distinct adapters r_a * H_in, per projection;
+    expand: 2 * T_a * H_out (y read + write) + sum over distinct adapters r_a * H_out;
+    T_a = tokens that carry an adapter.  Page tables, segments and the fp32
+    shrink scratch are metadata and not counted.
+    """
+    ta = wl.token_adapter
+    Ta = int((ta >= 0).sum())
+    distinct = sorted(set(int(a) for a in ta if a >= 0))
+    rsum = int(sum(int(wl.ranks[a]) for a in distinct))
+    shrink = sum((Ta * p.h_in + rsum * p.h_in) * elt for p in wl.projections)
+    expand = sum((2 * Ta * p.h_out + rsum * p.h_out) * elt for p in wl.projections)
+    return {"shrink_cc": shrink, "expand_cc": expand, "step": shrink + expand,
+            "distinct_adapters": len(distinct), "tokens": Ta}
+
+
+def setup_device(wl, device):
+    import torch
+
+    from lora_adapters_gb300 import slora
+
+    sp = wl.spec
+    dims = [(p.h_in, p.h_out) for p in sp.projections]
+    pool = slora.Pool(wl.pool_pages, wl.H, sp.dtype, dims, sp.num_adapters, max(sp.rank_set),
+                      max(wl.T, 1), device=device)
+    pool.replay(wl.pool_ops, wl.ranks, wl.adapter)
+    tdt = pool.tdtype
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(tdt).to(device)
+
+    xs = [dev(wl.x(p)) for p in range(len(dims))]
+    y0 = [dev(wl.y_in(p)) for p in range(len(dims))]
+    ys = [y.clone() for y in y0]
+    ta = torch.from_numpy(wl.token_adapter.copy()).to(device)
+    torch.cuda.synchronize()
+    return pool, ta, xs, ys, y0
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"unavailable": "nvidia-smi not runnable"}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        lines = [l.strip() for l in open(self.out.name) if l.strip()]
+        os.unlink(self.out.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"unavailable": "no samples"}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _gpu_id(torch):
+    try:
+        u = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[0] if vis else str(torch.cuda.current_device())
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_sample(wl, n_tokens: int, threads: int, seed: int = 0):
+    """Time the oracle on n_tokens tokens of the batch, all projections."""
+    from oracle import lora as olora
+    from oracle import pool as opool
+
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(wl.T, size=min(n_tokens, wl.T), replace=False)).astype(np.int32)
+    sp = wl.spec
+    pool = opool.OraclePool(wl.pool_pages, wl.H, [(p.h_in, p.h_out) for p in sp.projections],
+                            sp.num_adapters, max(sp.rank_set))
+    pool.replay(wl.pool_ops, wl.ranks)
+    store = opool.OracleStore(wl.pool_pages, wl.H)
+    for a in sorted(set(int(wl.token_adapter[i]) for i in rows if wl.token_adapter[i] >= 0)):
+        store.write_adapter(pool, a, wl.adapter(a))
+    inputs = [(wl.x(p), wl.y_in(p)) for p in range(len(sp.projections))]
+    t0 = time.perf_counter()
+    for p, (x, y) in enumerate(inputs):
+        olora.apply(store, pool, p, wl.token_adapter, x, y, sp.s, sp.dtype, tokens=rows, num_threads=threads)
+    return time.perf_counter() - t0, len(rows)
+
+
+def cpu_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, wl, cfg):
+    """The reference arm: the CPU oracle, as it stands, on host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    threads = cpu_threads()
+    sample = args.ref_tokens
+    for _ in range(args.warmup):
+        oracle_sample(wl, max(1, sample // 4), threads)
+    total_t, total_n = 0.0, 0
+    for k in range(args.steps):
+        t, n = oracle_sample(wl, sample, threads, seed=k)
+        total_t += t
+        total_n += n
+    value = total_n / total_t
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": cfg,
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"{sample} tokens of the batch per step, all 4 projections"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama7b_decode")
+    ap.add_argument("--mode", default="decode", choices=["auto", "decode", "prefill"])
+    ap.add_argument("--ref-tokens", type=int, default=24)
+    ap.add_argument("--cpu-tokens", type=int, default=0, help="oracle sample size (0: sized to ~10 s)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from lora_adapters_gb300 import workloads
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    wl = workloads.make(args.workload, seed=rank)      # each replica draws its own batch
+    sp = wl.spec
+    cfg = {"workload": sp.name, "H": sp.H, "tokens_per_step": wl.T,
+           "projections": [f"{p.name}:{p.h_in}->{p.h_out}" for p in sp.projections],
+           "adapters_resident": sp.num_adapters, "ranks": list(sp.rank_set),
+           "popularity": f"{sp.popularity}{'(alpha=%g)' % sp.zipf_alpha if sp.popularity == 'zipf' else ''}",
+           "pool_pages": wl.pool_pages, "page_bytes": sp.H * 2, "mode": args.mode,
+           "l2": "flushed before every timed step (256 MiB device write)",
+           "parallelism": f"replicas x{args.gpus}"}
+    if args.impl == "reference":
+        run_reference(args, wl, cfg)
+        return
+
+    import torch
+
+    from lora_adapters_gb300 import build, slora
+
+    build.build()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=device)
+    mode = {"auto": slora.MODE_AUTO, "decode": slora.MODE_DECODE, "prefill": slora.MODE_PREFILL}[args.mode]
+
+    pool, ta, xs, ys, y0 = setup_device(wl, device)
+    n = len(sp.projections)
+    projs = list(range(n))
+    stream = pool.compute_stream
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def step():
+        seg = pool.build_segments(ta)
+        pool.apply_multi(seg, projs, xs, ys, sp.s, mode)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # ---- device-timed steps (inputs resident in HBM)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    slora.slora_timing_enable(pool.handle, True)
+    slora.slora_timing_read(pool.handle)                  # reset the per-kernel totals
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(_gpu_id(torch))
+    wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for k in range(args.steps):
+            flush.fill_(k & 0xff)
+            starts[k].record(stream)
+            step()
+            ends[k].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    kern = slora.slora_timing_read(pool.handle)
+    slora.slora_timing_enable(pool.handle, False)
+    ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    ms_step = ms / args.steps
+    if world > 1:
+        t = torch.tensor([ms_step], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+    value = world * wl.T / (ms_step * 1e-3)
+
+    # ---- roofline of the dominant kernel
+    hbm_peak, peak_kind = _peaks()
+    ab = algorithmic_bytes(wl)
+    per_kernel = {}
+    for name in ("shrink_cc", "expand_cc", "build_segments"):
+        tms, cnt = kern.get(name, (0.0, 0))
+        if cnt:
+            per_kernel[name] = {"avg_us": 1e3 * tms / cnt, "launches": int(cnt)}
+            if name in ab:
+                per_kernel[name]["gbs"] = ab[name] / (tms / cnt * 1e-3) / 1e9
+    dom = max(("shrink_cc", "expand_cc"), key=lambda k: per_kernel.get(k, {}).get("avg_us", 0))
+    achieved = per_kernel[dom]["gbs"]
+    src_hash = _kernel_source_hash()
+    tr = NCU_TRAFFIC.get((dom, sp.name))
+    traffic = tr[0] if tr and tr[1] == src_hash else None
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "peak_source": peak_kind, "traffic": traffic,
+                "algorithmic_bytes_per_launch": ab[dom],
+                "step_achieved_gbs": ab["step"] / (ms_step * 1e-3) / 1e9,
+                "step_frac": ab["step"] / (ms_step * 1e-3) / 1e9 / hbm_peak,
+                "kernels": per_kernel, "source_hash": src_hash}
+    launches = int(sum(c for _, c in kern.values()))
+
+    # ---- end to end through the C ABI with host buffers
+    pin_x = [x.cpu().pin_memory() for x in xs]
+    pin_y = [y.cpu().pin_memory() for y in y0]
+    pin_ta = ta.cpu().pin_memory()
+    out_y = [torch.empty_like(y, device="cpu").pin_memory() for y in ys]
+    h2d = sum(t.numel() * t.element_size() for t in pin_x + pin_y) + pin_ta.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in out_y)
+
+    def e2e_step():
+        ta.copy_(pin_ta, non_blocking=True)
+        for d, h in zip(xs, pin_x):
+            d.copy_(h, non_blocking=True)
+        for d, h in zip(ys, pin_y):
+            d.copy_(h, non_blocking=True)
+        step()
+        for h, d in zip(out_y, ys):
+            h.copy_(d, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        e_ms = 0.0
+        for k in range(args.steps):
+            flush.fill_(k & 0xff)
+            s0 = torch.cuda.Event(enable_timing=True)
+            s1 = torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            e2e_step()
+            s1.record(stream)
+            s1.synchronize()
+            e_ms += s0.elapsed_time(s1)
+    e_ms /= args.steps
+    if world > 1:
+        t = torch.tensor([e_ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e_ms = float(t.item())
+    e2e = {"value": world * wl.T / (e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+           "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms}
+
+    # ---- CPU baseline: the oracle on a bounded sample, rank 0 at N = 1 only
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = cpu_threads()
+        n_tok = args.cpu_tokens
+        if n_tok <= 0:
+            t1, n1 = oracle_sample(wl, 4, threads)
+            n_tok = int(max(4, min(wl.T, 10.0 / max(t1 / n1, 1e-6))))
+        t, nn = oracle_sample(wl, n_tok, threads, seed=1)
+        cpu = {"value": nn / t, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{nn} of the {wl.T} tokens, all {n} projections, fp64 C loops ({t:.1f} s)"}
+
+    pool.close()
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": sp.dtype, "data": "synthetic", "config": cfg,
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+                "gpu_launches": launches, "wall_s_timed_region": wall}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

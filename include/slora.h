@@ -1,0 +1,245 @@
+/*
+ * slora.h -- C ABI of the GB300 heterogeneous-batch LoRA library (libslora.so).
+ *
+ * The library implements the data-parallel hot path of S-LoRA ("S-LoRA:
+ * Serving Thousands of Concurrent LoRA Adapters", MLSys 2024): for every
+ * token i of one batch, with its own adapter a = a(i) of its own rank r_a,
+ *
+ *     y_i  +=  s * (x_i A_a) B_a
+ *
+ * where the rows of A_a and B_a are not contiguous tensors but sit on pages
+ * of one unified pool that the adapters share with the KV cache.
+ *   - Unified Paging: one pool of fixed-size pages holds adapter weights of
+ *     different ranks and KV tensors of different lengths (nubint.ai review,
+ *     abstract and method list; dongaigc.com summary, section 1).
+ *   - Adapters live in host memory and are fetched to the GPU on demand,
+ *     asynchronously (nubint.ai review, abstract; cmlonder.com newsletter,
+ *     section "Iddia ve Gerceklik").
+ *   - Heterogeneous batching: one pass computes the LoRA part for tokens of
+ *     many adapters of different ranks directly on non-contiguous memory
+ *     (dongaigc.com summary, section 2; nubint.ai review, method list).
+ *   - The base model's batched GEMM is computed elsewhere; this library only
+ *     adds the adapter part into its output y (nubint.ai review, method list:
+ *     base computation batched, adapter computation separate).
+ *
+ * Conventions for every function below
+ *   - Return value: SLORA_OK (0) or a negative SLORA_ERR_* code.  On error
+ *     nothing observable changed (allocator state, page tables, device data)
+ *     unless the description says otherwise; slora_last_error_string() then
+ *     holds a one-line reason (thread-local, valid until the next call on
+ *     the same thread).
+ *   - "device pointer" = memory of the GPU current when the pool was
+ *     created; "host pointer" = ordinary (preferably pinned) host memory.
+ *   - Streams/events are cudaStream_t / cudaEvent_t passed as void*.  All
+ *     device work of the pool is ordered on its compute stream, except
+ *     adapter copies, which run on its copy stream.  No function blocks the
+ *     host on the GPU unless it says so.
+ *   - A pool is not thread-safe: the caller serialises calls on one pool.
+ *   - 16-bit values are IEEE binary16 (SLORA_F16) or bfloat16 (SLORA_BF16);
+ *     accumulation is fp32; y is rounded once, to nearest even.
+ */
+#ifndef SLORA_H
+#define SLORA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define SLORA_OK 0
+#define SLORA_ERR_INVALID (-1)      /* bad argument, size, alignment or id */
+#define SLORA_ERR_OOM (-2)          /* not enough free pages; state unchanged */
+#define SLORA_ERR_EXISTS (-3)       /* adapter id already resident */
+#define SLORA_ERR_NOT_RESIDENT (-4) /* adapter id not resident */
+#define SLORA_ERR_BUSY (-5)         /* reserved: the pool orders reuse by events instead */
+#define SLORA_ERR_CUDA (-6)         /* a CUDA runtime call failed (see error string) */
+#define SLORA_ERR_DEVICE (-7)       /* a kernel reported bad input (see slora_device_status) */
+
+/* ---- element types and apply modes -------------------------------------- */
+#define SLORA_F16 0
+#define SLORA_BF16 1
+
+#define SLORA_MODE_AUTO 0    /* CUDA-core tiles below the tensor-core threshold, tcgen05 tiles above */
+#define SLORA_MODE_DECODE 1  /* every segment on the CUDA-core gather kernels */
+#define SLORA_MODE_PREFILL 2 /* every segment on the tcgen05 tensor-core kernels */
+
+/* Library limits (also checked at run time). */
+#define SLORA_MAX_PROJ 8           /* projections per pool */
+#define SLORA_MAX_RANK 256         /* largest adapter rank */
+#define SLORA_MAX_ADAPTERS 32768   /* adapter ids 0 .. max_adapters-1 */
+
+typedef struct slora_pool slora_pool; /* opaque, owned by the library */
+
+/*
+ * The token grouping of one batch (the "segments" of segmented gather
+ * matrix-vector products, SGMV: cmlonder.com newsletter, section "Iddia ve
+ * Gerceklik").  Tokens are stably sorted by adapter id, ascending; tokens
+ * with id -1 carry no adapter and are left out, as are tokens that name an
+ * adapter that is not resident (those are counted in counts[2] and raise
+ * the device status SLORA_ERR_NOT_RESIDENT).  All arrays are DEVICE memory
+ * owned by the pool; they stay valid until the next slora_build_segments on
+ * the same pool (or the next evict), which invalidates every earlier handle
+ * (generation check).
+ */
+typedef struct slora_segments {
+  int32_t T;                  /* tokens in the batch */
+  int32_t max_segs;           /* capacity of seg_adapter / seg_start */
+  const int32_t* perm;        /* [T] sorted position j -> token index; [0, counts[1]) valid */
+  const int32_t* seg_start;   /* [max_segs + 1] first sorted position of each segment */
+  const int32_t* seg_adapter; /* [max_segs] adapter id of each segment (ascending) */
+  const int32_t* counts;      /* [16] {num_segs, n_sorted, bad_tokens, internal work totals...} */
+  uint64_t generation;        /* must match the pool's current segment generation */
+} slora_segments;
+
+/*
+ * Create a pool over a caller-owned device buffer.
+ *   d_pool      device buffer of num_pages * page_elems 16-bit elements,
+ *               16-byte aligned; caller-owned, must outlive the pool.  NULL
+ *               creates a PLANNING pool: host allocator and page tables only,
+ *               no CUDA call is ever made (loads only allocate; build/apply
+ *               return SLORA_ERR_INVALID).
+ *   num_pages   pages in the pool (> 0, < 2^31)
+ *   page_elems  H = elements per page = the hidden size = one token's K (or
+ *               V) vector for one layer, so one KV slot of one token and one
+ *               layer is two pages; multiple of 8, <= 65536
+ *   dtype       SLORA_F16 or SLORA_BF16 (pool, x and y share it)
+ *   max_adapters, max_rank   adapter ids are 0..max_adapters-1, ranks 1..max_rank
+ *   max_tokens  largest batch (T) accepted by slora_build_segments
+ *   num_proj, proj_in, proj_out   the projections adapters carry (host
+ *               arrays, copied); every dim a positive multiple of 8
+ *   compute, copy   cudaStream_t for kernels / for adapter copies (may be
+ *               equal; NULL = legacy default stream)
+ * Allocates with cudaMalloc: the device page table (max_adapters * max_rank
+ * * sum_q(ceil(in_q/H)+ceil(out_q/H)) int32), segment arrays, the fp32
+ * shrink scratch (SLORA_MAX_PROJ * max_tokens * max_rank floats) and one
+ * adapter-sized staging buffer; pins an equally sized host page-table mirror.
+ */
+int slora_pool_create(slora_pool** out, void* d_pool, int64_t num_pages, int32_t page_elems,
+                      int32_t dtype, int32_t max_adapters, int32_t max_rank, int32_t max_tokens,
+                      int32_t num_proj, const int32_t* proj_in, const int32_t* proj_out,
+                      void* compute_stream, void* copy_stream);
+
+/* Synchronises both streams and frees everything the pool allocated (not d_pool). */
+int slora_pool_destroy(slora_pool* pool);
+
+/*
+ * KV-slot pages (PagedAttention-style: taken on demand, returned when a
+ * request ends; fatihsoysal.com page, section "vLLM'in PagedAttention
+ * Mekanizmasi").  alloc writes the n lowest-numbered free pages, ascending,
+ * to out_pages (host int32[n]); all or nothing (SLORA_ERR_OOM).  free
+ * returns n KV pages (host int32[n]); every page must be a KV page and
+ * listed once, else SLORA_ERR_INVALID and nothing is freed.  Pages released
+ * by slora_adapter_evict may still be read by kernels already queued on the
+ * compute stream: write reused pages on that stream or after it.
+ */
+int slora_pages_alloc(slora_pool* pool, int64_t n, int32_t* out_pages);
+int slora_pages_free(slora_pool* pool, int64_t n, const int32_t* pages);
+
+/* Free page count and page size; any pointer may be NULL. */
+int slora_pool_info(const slora_pool* pool, int64_t* free_pages, int64_t* num_pages,
+                    int32_t* page_elems, int64_t* pages_per_rank);
+
+/*
+ * Load adapter `adapter_id` of rank `rank` from host memory into pool pages
+ * (the on-demand fetch of the nubint.ai review, abstract).  Allocates
+ * rank * sum_q(ceil(in_q/H) + ceil(out_q/H)) pages, lowest-numbered first,
+ * and lists them in this page-table order: for each projection q, the rank
+ * rows of A (each ceil(in_q/H) page chunks), then the rank rows of B (each
+ * ceil(out_q/H) chunks); the i-th lowest page holds the i-th chunk.  The tail
+ * of a row's last page is zero-filled.
+ *   h_A[q]  host, rank x in_q 16-bit row-major: row k is column k of the
+ *           in_q x rank matrix A (A transposed)
+ *   h_B[q]  host, rank x out_q 16-bit row-major: row k is row k of B
+ *   done    optional out: a cudaEvent_t (owned by the pool, valid until the
+ *           adapter is evicted) that completes when the pages are written
+ * The copies are queued on the copy stream after all work queued so far on
+ * the compute stream (so pages freed earlier are no longer being read) and
+ * the host buffers must stay untouched until `done` completes.  Later
+ * slora_build_segments calls make the compute stream wait for pending loads.
+ * Errors: SLORA_ERR_INVALID (id/rank out of range, NULL buffer),
+ * SLORA_ERR_EXISTS, SLORA_ERR_OOM (state unchanged), SLORA_ERR_CUDA (the
+ * pages are released again, state as before the call).
+ * On a planning pool h_A / h_B may be NULL and nothing is copied.
+ */
+int slora_adapter_load(slora_pool* pool, int32_t adapter_id, int32_t rank,
+                       const void* const* h_A, const void* const* h_B, void** done);
+
+/*
+ * Evict a resident adapter: its pages return to the free list at once and
+ * its device rank is cleared on the compute stream (work queued before the
+ * evict still sees the adapter).  Every segment handle built before the
+ * evict becomes stale (build the segments again).  SLORA_ERR_NOT_RESIDENT if
+ * it is not loaded.
+ */
+int slora_adapter_evict(slora_pool* pool, int32_t adapter_id);
+
+/* Host copy of an adapter's page table (page-table order above); *n = entries. */
+int slora_adapter_pages(const slora_pool* pool, int32_t adapter_id, int32_t* out_pages,
+                        int64_t capacity, int64_t* n);
+
+/*
+ * Group the batch's tokens by adapter on the GPU (one kernel on the compute
+ * stream).  d_token_adapter: device int32[T], ids in [-1, max_adapters);
+ * 0 <= T <= max_tokens.  Fills *out with pool-owned device arrays (see
+ * slora_segments) plus the internal work lists of the apply kernels.
+ */
+int slora_build_segments(slora_pool* pool, const int32_t* d_token_adapter, int32_t T,
+                         slora_segments* out);
+
+/*
+ * y += s * (x A_a) B_a for one projection `proj` over every token of the
+ * batch `seg` was built from (tokens left out of the segments are not
+ * touched).  x: device, T rows of proj_in[proj] elements, row stride ldx
+ * elements; y: device, T rows of proj_out[proj], stride ldy, updated in
+ * place.  Strides multiples of 8, pointers 16-byte aligned, x and y must not
+ * overlap.  mode: SLORA_MODE_*.  Kernels only; nothing is synchronised.
+ */
+int slora_lora_apply(slora_pool* pool, const slora_segments* seg, int32_t proj, const void* d_x,
+                     int64_t ldx, void* d_y, int64_t ldy, float s, int32_t mode);
+
+/* The same for n projections of one layer in one set of launches. */
+int slora_lora_apply_multi(slora_pool* pool, const slora_segments* seg, int32_t n,
+                           const int32_t* projs, const void* const* d_x, const int64_t* ldx,
+                           void* const* d_y, const int64_t* ldy, float s, int32_t mode);
+
+/*
+ * Synchronises the compute stream, returns in *status the first error a
+ * kernel reported since the last call (SLORA_OK, SLORA_ERR_NOT_RESIDENT for a
+ * token naming an adapter that is not loaded, SLORA_ERR_INVALID for an id
+ * out of range) and clears it.
+ */
+int slora_device_status(slora_pool* pool, int32_t* status);
+
+/*
+ * Serialise the host allocator state for bit-exact comparison: int64
+ * num_pages, int64 free_pages, int32 max_adapters, int32 stride, then
+ * int32 owner[num_pages] (-1 free, -2 KV, else adapter id), int32
+ * rank[max_adapters], int32 page_table[max_adapters * stride] (-1 unused).
+ * With buf NULL only *len is set; otherwise *len must be >= the size.
+ */
+int slora_pool_snapshot(const slora_pool* pool, void* buf, size_t* len);
+
+/*
+ * Per-kernel device timing (tracing).  When enabled, every kernel the pool
+ * launches is bracketed by CUDA events on its stream.  slora_timing_read
+ * synchronises, then writes for each kernel kind k < *n (at most capacity):
+ * names[k] (static strings), total milliseconds ms[k] and launches[k], and
+ * resets the totals.
+ */
+int slora_timing_enable(slora_pool* pool, int32_t enable);
+int slora_timing_read(slora_pool* pool, int32_t capacity, const char** names, double* ms,
+                      int64_t* launches, int32_t* n);
+
+/* Tensor-core threshold of SLORA_MODE_AUTO: segments with at least this many
+ * tokens use the tcgen05 kernels (default 64). */
+int slora_set_tc_threshold(slora_pool* pool, int32_t min_tokens);
+
+const char* slora_last_error_string(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SLORA_H */

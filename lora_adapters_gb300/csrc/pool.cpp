@@ -1,0 +1,735 @@
+// Host side of libslora: the unified page pool (allocator + page tables), the
+// asynchronous adapter loader, and the C ABI declared in include/slora.h.
+//
+// Unified Paging ("S-LoRA: Serving Thousands of Concurrent LoRA Adapters",
+// nubint.ai review, abstract; dongaigc.com summary, section 1): one pool of
+// H-element pages holds adapter rows of every rank and KV slots of every
+// length.  The allocator always hands out the lowest-numbered free pages
+// (all or nothing), which makes every page table reproducible call by call.
+// Adapters live in host memory and are fetched on demand (nubint.ai review,
+// abstract): one cudaMemcpyAsync per weight block into a device staging
+// buffer on the copy stream, then a scatter kernel that writes each row chunk
+// to its page; the compute stream waits on the load's event before using it.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/slora.h"
+#include "internal.h"
+
+using namespace slora;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+#define CUDA_TRY(call)                                                                    \
+  do {                                                                                    \
+    cudaError_t e_ = (call);                                                              \
+    if (e_ != cudaSuccess)                                                                \
+      return fail(SLORA_ERR_CUDA, "%s failed: %s", #call, cudaGetErrorString(e_));         \
+  } while (0)
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+constexpr int32_t kOwnerFree = -1;
+constexpr int32_t kOwnerKV = -2;
+constexpr int32_t kOwnerPending = -3;
+
+enum TimerKind { kTBuild = 0, kTShrinkCC, kTExpandCC, kTShrinkTC, kTExpandTC, kTScatter, kTNum };
+const char* kTimerNames[kTNum] = {"build_segments", "shrink_cc", "expand_cc",
+                                  "shrink_tc", "expand_tc", "scatter"};
+
+}  // namespace
+
+struct slora_pool {
+  // configuration
+  int64_t num_pages = 0;
+  int32_t H = 0, dtype = 0, max_adapters = 0, max_rank = 0, max_tokens = 0, num_proj = 0;
+  int32_t max_segs = 0;
+  int32_t proj_in[kMaxProj] = {}, proj_out[kMaxProj] = {};
+  int32_t ppi[kMaxProj] = {}, ppo[kMaxProj] = {}, rows_before[kMaxProj] = {};
+  int64_t chunks_per_rank = 0;   // page-table entries per unit of rank
+  int64_t pt_stride = 0;         // entries reserved per adapter id
+  int64_t staging_elems = 0;
+  bool planning = true;
+  int32_t tc_threshold = 64;
+
+  // allocator
+  std::vector<int32_t> owner;    // per page: -1 free, -2 KV, else adapter id
+  std::vector<uint64_t> free_bits;
+  int64_t free_count = 0;
+  int64_t hint_word = 0;         // no free page below word hint_word
+  std::vector<int32_t> rank_h;
+  std::vector<int64_t> npages_h; // page-table entries per resident adapter
+  int32_t* pt_h = nullptr;       // host page-table mirror (pinned unless planning)
+  int32_t* rank_pin = nullptr;   // pinned rank mirror (source of the rank H2D copies)
+
+  // device
+  uint16_t* d_pool = nullptr;
+  cudaStream_t compute = nullptr, copy = nullptr;
+  int device = 0;
+  int32_t* d_pt = nullptr;
+  int32_t* d_rank = nullptr;
+  int32_t* d_error = nullptr;
+  int32_t* d_seg_mem = nullptr;
+  SegDev seg{};
+  float* d_v = nullptr;
+  uint16_t* d_staging = nullptr;
+  std::vector<cudaEvent_t> load_event;   // per adapter id (created lazily)
+  std::vector<char> load_pending;        // load event recorded, maybe not yet complete
+  std::vector<int32_t> pending;          // ids with load_pending set
+  cudaEvent_t order_event = nullptr;
+  uint64_t seg_generation = 0;
+  int32_t seg_T = 0;
+  int num_sms = 0;
+  int grid_shrink_cc = 0, grid_expand_cc = 0;
+
+  // timing
+  bool timing = false;
+  struct Rec {
+    int kind;
+    cudaEvent_t a, b;
+  };
+  std::vector<Rec> recs;
+  std::vector<cudaEvent_t> spare_events;
+  double t_ms[kTNum] = {};
+  int64_t t_launches[kTNum] = {};
+};
+
+namespace {
+
+// ---- allocator ------------------------------------------------------------------
+void bits_set_free(slora_pool* p, int64_t page, bool is_free) {
+  uint64_t m = 1ull << (page & 63);
+  if (is_free) p->free_bits[page >> 6] |= m;
+  else p->free_bits[page >> 6] &= ~m;
+}
+
+// The n lowest-numbered free pages, ascending; caller checked n <= free_count.
+void take_lowest(slora_pool* p, int64_t n, int32_t owner, int32_t* out) {
+  int64_t got = 0;
+  int64_t w = p->hint_word;
+  const int64_t nw = (int64_t)p->free_bits.size();
+  while (got < n && w < nw) {
+    uint64_t bits = p->free_bits[w];
+    while (bits && got < n) {
+      const int b = __builtin_ctzll(bits);
+      bits &= bits - 1;
+      const int64_t page = (w << 6) + b;
+      out[got++] = (int32_t)page;
+      p->owner[page] = owner;
+      bits_set_free(p, page, false);
+    }
+    if (p->free_bits[w] == 0) ++w;
+    else break;
+  }
+  p->hint_word = w;
+  // skip words that became full
+  while (p->hint_word < nw && p->free_bits[p->hint_word] == 0) ++p->hint_word;
+  p->free_count -= n;
+}
+
+void give_back(slora_pool* p, int64_t n, const int32_t* pages) {
+  for (int64_t i = 0; i < n; ++i) {
+    const int64_t page = pages[i];
+    p->owner[page] = kOwnerFree;
+    bits_set_free(p, page, true);
+    p->hint_word = std::min<int64_t>(p->hint_word, page >> 6);
+  }
+  p->free_count += n;
+}
+
+int check_pool(const slora_pool* p) {
+  if (!p) return fail(SLORA_ERR_INVALID, "pool is NULL");
+  return SLORA_OK;
+}
+
+int check_device_pool(const slora_pool* p) {
+  if (!p) return fail(SLORA_ERR_INVALID, "pool is NULL");
+  if (p->planning) return fail(SLORA_ERR_INVALID, "planning pool (no device buffer): no GPU work");
+  return SLORA_OK;
+}
+
+// ---- timing ---------------------------------------------------------------------
+cudaEvent_t get_event(slora_pool* p) {
+  if (!p->spare_events.empty()) {
+    cudaEvent_t e = p->spare_events.back();
+    p->spare_events.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+struct Timed {
+  slora_pool* p;
+  int kind;
+  cudaStream_t st;
+  cudaEvent_t a = nullptr;
+  Timed(slora_pool* p_, int kind_, cudaStream_t st_) : p(p_), kind(kind_), st(st_) {
+    if (p->timing) {
+      a = get_event(p);
+      if (a) cudaEventRecord(a, st);
+    }
+  }
+  void done() {
+    if (!a) return;
+    cudaEvent_t b = get_event(p);
+    if (!b) return;
+    cudaEventRecord(b, st);
+    p->recs.push_back({kind, a, b});
+    a = nullptr;
+  }
+};
+
+// Make the compute stream wait for adapter loads that may still be running.
+int wait_pending_loads(slora_pool* p) {
+  std::vector<int32_t> still;
+  for (int32_t a : p->pending) {
+    if (!p->load_pending[a]) continue;
+    cudaError_t q = cudaEventQuery(p->load_event[a]);
+    if (q == cudaSuccess) {
+      p->load_pending[a] = 0;
+      continue;
+    }
+    if (q != cudaErrorNotReady) return fail(SLORA_ERR_CUDA, "cudaEventQuery: %s", cudaGetErrorString(q));
+    (void)cudaGetLastError();  // clear the sticky-free not-ready status
+    CUDA_TRY(cudaStreamWaitEvent(p->compute, p->load_event[a], 0));
+    still.push_back(a);
+  }
+  p->pending.swap(still);
+  return SLORA_OK;
+}
+
+void free_device(slora_pool* p) {
+  if (p->planning) {
+    std::free(p->pt_h);
+    std::free(p->rank_pin);
+    return;
+  }
+  for (auto& r : p->recs) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  for (auto e : p->spare_events) cudaEventDestroy(e);
+  for (auto e : p->load_event)
+    if (e) cudaEventDestroy(e);
+  if (p->order_event) cudaEventDestroy(p->order_event);
+  cudaFree(p->d_pt);
+  cudaFree(p->d_rank);
+  cudaFree(p->d_error);
+  cudaFree(p->d_seg_mem);
+  cudaFree(p->d_v);
+  cudaFree(p->d_staging);
+  if (p->pt_h) cudaFreeHost(p->pt_h);
+  if (p->rank_pin) cudaFreeHost(p->rank_pin);
+}
+
+}  // namespace
+
+// =================================================================================
+extern "C" {
+
+const char* slora_last_error_string(void) { return g_err.c_str(); }
+
+int slora_pool_create(slora_pool** out, void* d_pool, int64_t num_pages, int32_t page_elems,
+                      int32_t dtype, int32_t max_adapters, int32_t max_rank, int32_t max_tokens,
+                      int32_t num_proj, const int32_t* proj_in, const int32_t* proj_out,
+                      void* compute_stream, void* copy_stream) {
+  if (!out) return fail(SLORA_ERR_INVALID, "out is NULL");
+  *out = nullptr;
+  if (num_pages <= 0 || num_pages >= (1ll << 31))
+    return fail(SLORA_ERR_INVALID, "num_pages %lld out of range", (long long)num_pages);
+  if (page_elems <= 0 || page_elems % 8 != 0 || page_elems > 65536)
+    return fail(SLORA_ERR_INVALID, "page_elems %d must be a positive multiple of 8, <= 65536", page_elems);
+  if (dtype != SLORA_F16 && dtype != SLORA_BF16) return fail(SLORA_ERR_INVALID, "dtype %d", dtype);
+  if (max_adapters <= 0 || max_adapters > kMaxAdapters)
+    return fail(SLORA_ERR_INVALID, "max_adapters %d not in [1, %d]", max_adapters, kMaxAdapters);
+  if (max_rank <= 0 || max_rank > kMaxRank)
+    return fail(SLORA_ERR_INVALID, "max_rank %d not in [1, %d]", max_rank, kMaxRank);
+  if (max_tokens < 0 || max_tokens > (1 << 24)) return fail(SLORA_ERR_INVALID, "max_tokens %d", max_tokens);
+  if (num_proj <= 0 || num_proj > kMaxProj || !proj_in || !proj_out)
+    return fail(SLORA_ERR_INVALID, "num_proj %d not in [1, %d]", num_proj, kMaxProj);
+  if (d_pool && (reinterpret_cast<uintptr_t>(d_pool) & 15))
+    return fail(SLORA_ERR_INVALID, "d_pool must be 16-byte aligned");
+
+  slora_pool* p = new (std::nothrow) slora_pool();
+  if (!p) return fail(SLORA_ERR_OOM, "host allocation failed");
+  p->num_pages = num_pages;
+  p->H = page_elems;
+  p->dtype = dtype;
+  p->max_adapters = max_adapters;
+  p->max_rank = max_rank;
+  p->max_tokens = max_tokens;
+  p->num_proj = num_proj;
+  p->max_segs = std::max(1, std::min(max_tokens, max_adapters));
+  int64_t before = 0;
+  for (int q = 0; q < num_proj; ++q) {
+    if (proj_in[q] <= 0 || proj_out[q] <= 0 || proj_in[q] % 8 || proj_out[q] % 8) {
+      delete p;
+      return fail(SLORA_ERR_INVALID, "projection %d dims %d x %d must be positive multiples of 8", q,
+                  proj_in[q], proj_out[q]);
+    }
+    p->proj_in[q] = proj_in[q];
+    p->proj_out[q] = proj_out[q];
+    p->ppi[q] = (int32_t)ceil_div(proj_in[q], page_elems);
+    p->ppo[q] = (int32_t)ceil_div(proj_out[q], page_elems);
+    p->rows_before[q] = (int32_t)before;
+    before += p->ppi[q] + p->ppo[q];
+    p->staging_elems += (int64_t)max_rank * (proj_in[q] + proj_out[q]);
+  }
+  p->chunks_per_rank = before;
+  p->pt_stride = (int64_t)max_rank * before;
+  const int64_t pt_entries = (int64_t)max_adapters * p->pt_stride;
+
+  p->owner.assign((size_t)num_pages, kOwnerFree);
+  p->free_bits.assign((size_t)ceil_div(num_pages, 64), ~0ull);
+  if (num_pages % 64) p->free_bits.back() = (1ull << (num_pages % 64)) - 1;
+  p->free_count = num_pages;
+  p->rank_h.assign((size_t)max_adapters, 0);
+  p->npages_h.assign((size_t)max_adapters, 0);
+  p->planning = (d_pool == nullptr);
+
+  if (p->planning) {
+    p->pt_h = static_cast<int32_t*>(std::malloc(sizeof(int32_t) * (size_t)pt_entries));
+    p->rank_pin = static_cast<int32_t*>(std::calloc((size_t)max_adapters, sizeof(int32_t)));
+    if (!p->pt_h || !p->rank_pin) {
+      free_device(p);
+      delete p;
+      return fail(SLORA_ERR_OOM, "host allocation failed");
+    }
+    std::fill(p->pt_h, p->pt_h + pt_entries, -1);
+    *out = p;
+    return SLORA_OK;
+  }
+
+  p->d_pool = static_cast<uint16_t*>(d_pool);
+  p->compute = static_cast<cudaStream_t>(compute_stream);
+  p->copy = static_cast<cudaStream_t>(copy_stream);
+  int rc = SLORA_OK;
+  auto setup = [&]() -> int {
+    CUDA_TRY(cudaGetDevice(&p->device));
+    CUDA_TRY(cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device));
+    CUDA_TRY(prepare_kernels(p->device));
+    CUDA_TRY(cudaMallocHost(&p->pt_h, sizeof(int32_t) * (size_t)pt_entries));
+    CUDA_TRY(cudaMallocHost(&p->rank_pin, sizeof(int32_t) * (size_t)max_adapters));
+    std::fill(p->pt_h, p->pt_h + pt_entries, -1);
+    std::fill(p->rank_pin, p->rank_pin + max_adapters, 0);
+    CUDA_TRY(cudaMalloc(&p->d_pt, sizeof(int32_t) * (size_t)pt_entries));
+    CUDA_TRY(cudaMalloc(&p->d_rank, sizeof(int32_t) * (size_t)max_adapters));
+    CUDA_TRY(cudaMalloc(&p->d_error, sizeof(int32_t)));
+    // segment arrays: perm, seg_start, seg_adapter, seg_rank, counts, 6 prefix arrays
+    const int64_t S1 = p->max_segs + 1;
+    const int64_t seg_ints = std::max<int64_t>(max_tokens, 1) + S1 * 9 + kNumCounts;
+    CUDA_TRY(cudaMalloc(&p->d_seg_mem, sizeof(int32_t) * (size_t)seg_ints));
+    int32_t* q = p->d_seg_mem;
+    p->seg.counts = q; q += kNumCounts;
+    p->seg.perm = q; q += std::max<int64_t>(max_tokens, 1);
+    p->seg.seg_start = q; q += S1;
+    p->seg.seg_adapter = q; q += S1;
+    p->seg.seg_rank = q; q += S1;
+    p->seg.cc_shrink_all = q; q += S1;
+    p->seg.cc_tile_all = q; q += S1;
+    p->seg.cc_shrink_short = q; q += S1;
+    p->seg.cc_tile_short = q; q += S1;
+    p->seg.tc_tile_all = q; q += S1;
+    p->seg.tc_tile_long = q; q += S1;
+    CUDA_TRY(cudaMalloc(&p->d_v, sizeof(float) * (size_t)kMaxProj * std::max(max_tokens, 1) * max_rank));
+    CUDA_TRY(cudaMalloc(&p->d_staging, sizeof(uint16_t) * (size_t)p->staging_elems));
+    CUDA_TRY(cudaMemsetAsync(p->d_pt, 0xff, sizeof(int32_t) * (size_t)pt_entries, p->compute));
+    CUDA_TRY(cudaMemsetAsync(p->d_rank, 0, sizeof(int32_t) * (size_t)max_adapters, p->compute));
+    CUDA_TRY(cudaMemsetAsync(p->d_error, 0, sizeof(int32_t), p->compute));
+    CUDA_TRY(cudaMemsetAsync(p->d_seg_mem, 0, sizeof(int32_t) * (size_t)seg_ints, p->compute));
+    CUDA_TRY(cudaEventCreateWithFlags(&p->order_event, cudaEventDisableTiming));
+    CUDA_TRY(cudaStreamSynchronize(p->compute));
+    p->load_event.assign((size_t)max_adapters, nullptr);
+    p->load_pending.assign((size_t)max_adapters, 0);
+    p->grid_shrink_cc = p->num_sms * occupancy_shrink_cc(dtype);
+    p->grid_expand_cc = p->num_sms * occupancy_expand_cc(dtype);
+    return SLORA_OK;
+  };
+  rc = setup();
+  if (rc != SLORA_OK) {
+    std::string why = g_err;
+    free_device(p);
+    delete p;
+    g_err = why;
+    return rc;
+  }
+  *out = p;
+  return SLORA_OK;
+}
+
+int slora_pool_destroy(slora_pool* p) {
+  if (!p) return fail(SLORA_ERR_INVALID, "pool is NULL");
+  int rc = SLORA_OK;
+  if (!p->planning) {
+    cudaError_t e1 = cudaStreamSynchronize(p->copy);
+    cudaError_t e2 = cudaStreamSynchronize(p->compute);
+    if (e1 != cudaSuccess || e2 != cudaSuccess)
+      rc = fail(SLORA_ERR_CUDA, "stream synchronize at destroy: %s",
+                cudaGetErrorString(e1 != cudaSuccess ? e1 : e2));
+  }
+  free_device(p);
+  delete p;
+  return rc;
+}
+
+int slora_pages_alloc(slora_pool* p, int64_t n, int32_t* out_pages) {
+  if (int rc = check_pool(p)) return rc;
+  if (n < 0 || (n > 0 && !out_pages)) return fail(SLORA_ERR_INVALID, "bad count or NULL output");
+  if (n > p->free_count)
+    return fail(SLORA_ERR_OOM, "need %lld pages, %lld free", (long long)n, (long long)p->free_count);
+  take_lowest(p, n, kOwnerKV, out_pages);
+  return SLORA_OK;
+}
+
+int slora_pages_free(slora_pool* p, int64_t n, const int32_t* pages) {
+  if (int rc = check_pool(p)) return rc;
+  if (n < 0 || (n > 0 && !pages)) return fail(SLORA_ERR_INVALID, "bad count or NULL pages");
+  int64_t i = 0;
+  int rc = SLORA_OK;
+  for (; i < n; ++i) {  // validate, marking pages pending to catch duplicates
+    const int64_t pg = pages[i];
+    if (pg < 0 || pg >= p->num_pages) { rc = fail(SLORA_ERR_INVALID, "page %lld out of range", (long long)pg); break; }
+    if (p->owner[pg] != kOwnerKV) {
+      rc = fail(SLORA_ERR_INVALID, "page %lld is not a KV page (owner %d)", (long long)pg, p->owner[pg]);
+      break;
+    }
+    p->owner[pg] = kOwnerPending;
+  }
+  if (rc != SLORA_OK) {
+    for (int64_t j = 0; j < i; ++j) p->owner[pages[j]] = kOwnerKV;
+    return rc;
+  }
+  give_back(p, n, pages);
+  return SLORA_OK;
+}
+
+int slora_pool_info(const slora_pool* p, int64_t* free_pages, int64_t* num_pages, int32_t* page_elems,
+                    int64_t* pages_per_rank) {
+  if (int rc = check_pool(p)) return rc;
+  if (free_pages) *free_pages = p->free_count;
+  if (num_pages) *num_pages = p->num_pages;
+  if (page_elems) *page_elems = p->H;
+  if (pages_per_rank) *pages_per_rank = p->chunks_per_rank;
+  return SLORA_OK;
+}
+
+int slora_adapter_load(slora_pool* p, int32_t a, int32_t rank, const void* const* h_A,
+                       const void* const* h_B, void** done) {
+  if (int rc = check_pool(p)) return rc;
+  if (done) *done = nullptr;
+  if (a < 0 || a >= p->max_adapters) return fail(SLORA_ERR_INVALID, "adapter id %d out of range", a);
+  if (rank < 1 || rank > p->max_rank) return fail(SLORA_ERR_INVALID, "rank %d not in [1, %d]", rank, p->max_rank);
+  if (p->rank_h[a] != 0) return fail(SLORA_ERR_EXISTS, "adapter %d already resident", a);
+  if (!p->planning) {
+    if (!h_A || !h_B) return fail(SLORA_ERR_INVALID, "NULL weight arrays");
+    for (int q = 0; q < p->num_proj; ++q)
+      if (!h_A[q] || !h_B[q]) return fail(SLORA_ERR_INVALID, "NULL weights of projection %d", q);
+  }
+  const int64_t n = (int64_t)rank * p->chunks_per_rank;
+  if (n > p->free_count)
+    return fail(SLORA_ERR_OOM, "adapter %d needs %lld pages, %lld free", a, (long long)n, (long long)p->free_count);
+
+  if (!p->planning && p->load_pending[a]) {
+    // The previous load of this id may still read its page-table mirror.
+    CUDA_TRY(cudaEventSynchronize(p->load_event[a]));
+    p->load_pending[a] = 0;
+  }
+  int32_t* tab = p->pt_h + (int64_t)a * p->pt_stride;
+  take_lowest(p, n, a, tab);
+  p->rank_h[a] = rank;
+  p->npages_h[a] = n;
+  if (p->planning) return SLORA_OK;
+
+  auto rollback = [&](int code) {
+    const std::string why = g_err;
+    give_back(p, n, tab);
+    std::fill(tab, tab + n, -1);
+    p->rank_h[a] = 0;
+    p->npages_h[a] = 0;
+    g_err = why;
+    return code;
+  };
+  auto enqueue = [&]() -> int {
+    if (!p->load_event[a]) CUDA_TRY(cudaEventCreateWithFlags(&p->load_event[a], cudaEventDisableTiming));
+    // Order the copies after everything queued on the compute stream so far:
+    // pages released by earlier evicts / KV frees are no longer being read,
+    // and an evict's rank clear of this id lands before the new rank.
+    CUDA_TRY(cudaEventRecord(p->order_event, p->compute));
+    CUDA_TRY(cudaStreamWaitEvent(p->copy, p->order_event, 0));
+    p->rank_pin[a] = rank;
+    CUDA_TRY(cudaMemcpyAsync(p->d_pt + (int64_t)a * p->pt_stride, tab, sizeof(int32_t) * (size_t)n,
+                             cudaMemcpyHostToDevice, p->copy));
+    int64_t off = 0;
+    ScatterDev sd{};
+    sd.staging = p->d_staging;
+    sd.pool = p->d_pool;
+    sd.H = p->H;
+    sd.pages = p->d_pt + (int64_t)a * p->pt_stride;
+    sd.n_entries = (int32_t)n;
+    sd.rank = rank;
+    sd.nproj = p->num_proj;
+    for (int q = 0; q < p->num_proj; ++q) {
+      const size_t bytesA = sizeof(uint16_t) * (size_t)rank * p->proj_in[q];
+      const size_t bytesB = sizeof(uint16_t) * (size_t)rank * p->proj_out[q];
+      sd.h_in[q] = p->proj_in[q];
+      sd.h_out[q] = p->proj_out[q];
+      sd.ppi[q] = p->ppi[q];
+      sd.ppo[q] = p->ppo[q];
+      sd.src_base[q] = off;
+      sd.entry_base[q] = (int32_t)((int64_t)rank * p->rows_before[q]);
+      CUDA_TRY(cudaMemcpyAsync(p->d_staging + off, h_A[q], bytesA, cudaMemcpyHostToDevice, p->copy));
+      off += (int64_t)rank * p->proj_in[q];
+      CUDA_TRY(cudaMemcpyAsync(p->d_staging + off, h_B[q], bytesB, cudaMemcpyHostToDevice, p->copy));
+      off += (int64_t)rank * p->proj_out[q];
+    }
+    {
+      Timed tm(p, kTScatter, p->copy);
+      CUDA_TRY(launch_scatter(sd, p->copy));
+      tm.done();
+    }
+    CUDA_TRY(cudaMemcpyAsync(p->d_rank + a, p->rank_pin + a, sizeof(int32_t), cudaMemcpyHostToDevice,
+                             p->copy));
+    CUDA_TRY(cudaEventRecord(p->load_event[a], p->copy));
+    return SLORA_OK;
+  };
+  int rc = enqueue();
+  if (rc != SLORA_OK) return rollback(rc);
+  p->load_pending[a] = 1;
+  p->pending.push_back(a);
+  if (done) *done = p->load_event[a];
+  return SLORA_OK;
+}
+
+int slora_adapter_evict(slora_pool* p, int32_t a) {
+  if (int rc = check_pool(p)) return rc;
+  if (a < 0 || a >= p->max_adapters || p->rank_h[a] == 0)
+    return fail(SLORA_ERR_NOT_RESIDENT, "adapter %d is not resident", a);
+  if (!p->planning) {
+    // Work queued before this call still sees the adapter; later work does not.
+    CUDA_TRY(cudaMemsetAsync(p->d_rank + a, 0, sizeof(int32_t), p->compute));
+  }
+  int32_t* tab = p->pt_h + (int64_t)a * p->pt_stride;
+  give_back(p, p->npages_h[a], tab);
+  std::fill(tab, tab + p->npages_h[a], -1);
+  p->rank_h[a] = 0;
+  p->npages_h[a] = 0;
+  // Segment handles carry the ranks seen when they were built; a reload of
+  // this id with another rank would make them index the wrong entries.
+  p->seg_generation++;
+  return SLORA_OK;
+}
+
+int slora_adapter_pages(const slora_pool* p, int32_t a, int32_t* out_pages, int64_t capacity, int64_t* n) {
+  if (int rc = check_pool(p)) return rc;
+  if (a < 0 || a >= p->max_adapters || p->rank_h[a] == 0)
+    return fail(SLORA_ERR_NOT_RESIDENT, "adapter %d is not resident", a);
+  const int64_t cnt = p->npages_h[a];
+  if (n) *n = cnt;
+  if (out_pages) {
+    if (capacity < cnt) return fail(SLORA_ERR_INVALID, "capacity %lld < %lld", (long long)capacity, (long long)cnt);
+    std::memcpy(out_pages, p->pt_h + (int64_t)a * p->pt_stride, sizeof(int32_t) * (size_t)cnt);
+  }
+  return SLORA_OK;
+}
+
+int slora_build_segments(slora_pool* p, const int32_t* d_ta, int32_t T, slora_segments* out) {
+  if (int rc = check_device_pool(p)) return rc;
+  if (!out) return fail(SLORA_ERR_INVALID, "out is NULL");
+  if (T < 0 || T > p->max_tokens) return fail(SLORA_ERR_INVALID, "T=%d not in [0, %d]", T, p->max_tokens);
+  if (T > 0 && !d_ta) return fail(SLORA_ERR_INVALID, "token_adapter is NULL");
+  if (int rc = wait_pending_loads(p)) return rc;
+  SegBuildArgs args{};
+  args.token_adapter = d_ta;
+  args.T = T;
+  args.rank = p->d_rank;
+  args.max_adapters = p->max_adapters;
+  args.tc_threshold = p->tc_threshold;
+  args.seg = p->seg;
+  args.error = p->d_error;
+  {
+    Timed tm(p, kTBuild, p->compute);
+    CUDA_TRY(launch_build_segments(args, p->compute));
+    tm.done();
+  }
+  p->seg_generation++;
+  p->seg_T = T;
+  out->T = T;
+  out->max_segs = p->max_segs;
+  out->perm = p->seg.perm;
+  out->seg_start = p->seg.seg_start;
+  out->seg_adapter = p->seg.seg_adapter;
+  out->counts = p->seg.counts;
+  out->generation = p->seg_generation;
+  return SLORA_OK;
+}
+
+int slora_lora_apply_multi(slora_pool* p, const slora_segments* seg, int32_t n, const int32_t* projs,
+                           const void* const* d_x, const int64_t* ldx, void* const* d_y,
+                           const int64_t* ldy, float s, int32_t mode) {
+  if (int rc = check_device_pool(p)) return rc;
+  if (!seg || seg->generation != p->seg_generation || seg->generation == 0)
+    return fail(SLORA_ERR_INVALID, "segments are missing or stale (rebuild them after every build call)");
+  if (n < 1 || n > kMaxProj || !projs || !d_x || !ldx || !d_y || !ldy)
+    return fail(SLORA_ERR_INVALID, "n=%d projections (1..%d) and non-NULL arrays required", n, kMaxProj);
+  if (mode < SLORA_MODE_AUTO || mode > SLORA_MODE_PREFILL) return fail(SLORA_ERR_INVALID, "mode %d", mode);
+  ApplyDev d{};
+  d.nproj = n;
+  d.H = p->H;
+  d.pool = p->d_pool;
+  d.page_table = p->d_pt;
+  d.pt_stride = p->pt_stride;
+  d.perm = p->seg.perm;
+  d.seg_start = p->seg.seg_start;
+  d.seg_adapter = p->seg.seg_adapter;
+  d.seg_rank = p->seg.seg_rank;
+  d.counts = p->seg.counts;
+  d.v_ld = p->max_rank;
+  d.s = s;
+  for (int i = 0; i < n; ++i) {
+    const int q = projs[i];
+    if (q < 0 || q >= p->num_proj) return fail(SLORA_ERR_INVALID, "projection %d out of range", q);
+    if (p->seg_T > 0 && (!d_x[i] || !d_y[i])) return fail(SLORA_ERR_INVALID, "NULL x or y");
+    if ((reinterpret_cast<uintptr_t>(d_x[i]) | reinterpret_cast<uintptr_t>(d_y[i])) & 15)
+      return fail(SLORA_ERR_INVALID, "x and y must be 16-byte aligned");
+    if (ldx[i] < p->proj_in[q] || ldx[i] % 8 || ldy[i] < p->proj_out[q] || ldy[i] % 8)
+      return fail(SLORA_ERR_INVALID, "row strides must be multiples of 8 and cover the row");
+    ProjDev& P = d.proj[i];
+    P.x = d_x[i];
+    P.ldx = ldx[i];
+    P.y = d_y[i];
+    P.ldy = ldy[i];
+    P.h_in = p->proj_in[q];
+    P.h_out = p->proj_out[q];
+    P.ppi = p->ppi[q];
+    P.ppo = p->ppo[q];
+    P.rows_before = p->rows_before[q];
+    P.ncol_tiles = (int32_t)ceil_div(P.h_out, kExpandCols);
+    P.v = p->d_v + (int64_t)i * std::max(p->max_tokens, 1) * p->max_rank;
+  }
+  if (p->seg_T == 0) return SLORA_OK;
+  // Until the tensor-core tiles are enabled every segment runs on the
+  // CUDA-core kernels, whatever the mode.
+  d.shrink_off = p->seg.cc_shrink_all;
+  d.tile_off = p->seg.cc_tile_all;
+  d.shrink_total_idx = kCcShrinkAll;
+  d.tile_total_idx = kCcTileAll;
+  {
+    Timed tm(p, kTShrinkCC, p->compute);
+    CUDA_TRY(launch_shrink_cc(d, p->dtype, p->grid_shrink_cc, p->compute));
+    tm.done();
+  }
+  {
+    Timed tm(p, kTExpandCC, p->compute);
+    CUDA_TRY(launch_expand_cc(d, p->dtype, p->grid_expand_cc, p->compute));
+    tm.done();
+  }
+  return SLORA_OK;
+}
+
+int slora_lora_apply(slora_pool* p, const slora_segments* seg, int32_t proj, const void* d_x, int64_t ldx,
+                     void* d_y, int64_t ldy, float s, int32_t mode) {
+  const void* xs[1] = {d_x};
+  void* ys[1] = {d_y};
+  return slora_lora_apply_multi(p, seg, 1, &proj, xs, &ldx, ys, &ldy, s, mode);
+}
+
+int slora_device_status(slora_pool* p, int32_t* status) {
+  if (int rc = check_device_pool(p)) return rc;
+  if (!status) return fail(SLORA_ERR_INVALID, "status is NULL");
+  int32_t v = 0;
+  CUDA_TRY(cudaMemcpyAsync(&v, p->d_error, sizeof v, cudaMemcpyDeviceToHost, p->compute));
+  CUDA_TRY(cudaMemsetAsync(p->d_error, 0, sizeof(int32_t), p->compute));
+  CUDA_TRY(cudaStreamSynchronize(p->compute));
+  *status = v;
+  return SLORA_OK;
+}
+
+int slora_pool_snapshot(const slora_pool* p, void* buf, size_t* len) {
+  if (int rc = check_pool(p)) return rc;
+  if (!len) return fail(SLORA_ERR_INVALID, "len is NULL");
+  const size_t need = 2 * sizeof(int64_t) + 2 * sizeof(int32_t) +
+                      sizeof(int32_t) * ((size_t)p->num_pages + (size_t)p->max_adapters +
+                                         (size_t)p->max_adapters * (size_t)p->pt_stride);
+  if (!buf) {
+    *len = need;
+    return SLORA_OK;
+  }
+  if (*len < need) return fail(SLORA_ERR_INVALID, "buffer of %zu bytes < %zu", *len, need);
+  char* c = static_cast<char*>(buf);
+  const int64_t hdr64[2] = {p->num_pages, p->free_count};
+  const int32_t hdr32[2] = {p->max_adapters, (int32_t)p->pt_stride};
+  std::memcpy(c, hdr64, sizeof hdr64);
+  c += sizeof hdr64;
+  std::memcpy(c, hdr32, sizeof hdr32);
+  c += sizeof hdr32;
+  std::memcpy(c, p->owner.data(), sizeof(int32_t) * (size_t)p->num_pages);
+  c += sizeof(int32_t) * (size_t)p->num_pages;
+  std::memcpy(c, p->rank_h.data(), sizeof(int32_t) * (size_t)p->max_adapters);
+  c += sizeof(int32_t) * (size_t)p->max_adapters;
+  std::memcpy(c, p->pt_h, sizeof(int32_t) * (size_t)p->max_adapters * (size_t)p->pt_stride);
+  *len = need;
+  return SLORA_OK;
+}
+
+int slora_timing_enable(slora_pool* p, int32_t enable) {
+  if (int rc = check_device_pool(p)) return rc;
+  p->timing = enable != 0;
+  return SLORA_OK;
+}
+
+int slora_timing_read(slora_pool* p, int32_t capacity, const char** names, double* ms, int64_t* launches,
+                      int32_t* n) {
+  if (int rc = check_device_pool(p)) return rc;
+  for (auto& r : p->recs) {
+    CUDA_TRY(cudaEventSynchronize(r.b));
+    float t = 0.f;
+    CUDA_TRY(cudaEventElapsedTime(&t, r.a, r.b));
+    p->t_ms[r.kind] += t;
+    p->t_launches[r.kind] += 1;
+    p->spare_events.push_back(r.a);
+    p->spare_events.push_back(r.b);
+  }
+  p->recs.clear();
+  const int k = std::min<int>(capacity, kTNum);
+  for (int i = 0; i < k; ++i) {
+    if (names) names[i] = kTimerNames[i];
+    if (ms) ms[i] = p->t_ms[i];
+    if (launches) launches[i] = p->t_launches[i];
+  }
+  for (int i = 0; i < kTNum; ++i) {
+    p->t_ms[i] = 0;
+    p->t_launches[i] = 0;
+  }
+  if (n) *n = k;
+  return SLORA_OK;
+}
+
+int slora_set_tc_threshold(slora_pool* p, int32_t min_tokens) {
+  if (int rc = check_pool(p)) return rc;
+  if (min_tokens < 0) return fail(SLORA_ERR_INVALID, "threshold %d", min_tokens);
+  p->tc_threshold = min_tokens;
+  return SLORA_OK;
+}
+
+}  // extern "C"

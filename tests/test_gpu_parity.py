@@ -1,0 +1,215 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the CPU oracle.
+
+Integer / index work (device page contents, perm, seg_start, seg_adapter,
+counts) must be bit-exact; y must satisfy |gpu - oracle| <= 5e-3 + 1e-2 |oracle|
+elementwise (fp16/bf16 storage, fp32 accumulation, one rounding).
+"""
+import numpy as np
+import pytest
+import torch
+
+from lora_adapters_gb300 import slora, workloads
+from oracle import pool as opool
+from tests import gpu_setup as G
+from tests import helpers as H
+
+pytestmark = pytest.mark.gpu
+
+MODES = [slora.MODE_DECODE, slora.MODE_AUTO, slora.MODE_PREFILL]
+
+# Small cases that still span several token tiles, rank chunks, column tiles
+# and page chunks, with ragged tails everywhere.
+SMALL = {
+    "tiny": workloads.spec("tiny"),
+    "tiny_bf16": workloads.spec("tiny", dtype="bf16", seed=3),
+    "mlp_ragged_bf16": workloads.WorkloadSpec(
+        name="mlp_ragged", H=256, dtype="bf16",
+        projections=(workloads.Projection("gate", 256, 1384), workloads.Projection("up", 256, 1384),
+                     workloads.Projection("down", 1384, 256)),
+        num_adapters=37, rank_set=(1, 7, 16, 33, 64), kind="decode", tokens=203, popularity="zipf",
+        zipf_alpha=1.2, pool_factor=1.4, s=0.5, seed=21),
+    "prefill_ragged_f16": workloads.WorkloadSpec(
+        name="prefill_ragged", H=512, dtype="f16", projections=workloads._qkvo(512),
+        num_adapters=11, rank_set=(8, 16, 128), kind="prefill", requests=9, prompt_len=(1, 300),
+        pool_factor=1.3, s=-1.25, seed=5),
+    "many_tokens_f16": workloads.WorkloadSpec(
+        name="many_tokens", H=128, dtype="f16", projections=(workloads.Projection("q", 128, 136),),
+        num_adapters=300, rank_set=(2, 8, 24), kind="decode", tokens=3001, popularity="uniform",
+        pool_factor=1.2, s=1.0, seed=8),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from lora_adapters_gb300 import build
+
+    build.build()
+    slora.lib()
+
+
+def _run_and_check(case: G.GpuCase, mode: int, want=None, rows=None, multi=True):
+    wl = case.wl
+    case.fresh_y()
+    seg = case.pool.build_segments(case.ta_dev)
+    n = len(wl.projections)
+    if multi:
+        case.pool.apply_multi(seg, list(range(n)), case.xs, case.ys, wl.spec.s, mode)
+    else:
+        for p in range(n):
+            case.pool.apply(seg, p, case.xs[p], case.ys[p], wl.spec.s, mode)
+    torch.cuda.synchronize()
+    assert case.pool.status() == slora.OK
+    want = want if want is not None else G.oracle_outputs(case, tokens=rows)
+    for p in range(n):
+        got = G.to_bits(case.ys[p])
+        ok, err, bad = G.compare(got, want[p], wl.spec.dtype, rows=rows)
+        assert ok, f"projection {p} mode {mode}: {bad} elements out of tolerance, max |err| {err}"
+    return seg, want
+
+
+def _check_segments(case: G.GpuCase, seg):
+    want = opool.build_segments(case.wl.token_adapter, case.oracle_pool.rank)
+    perm, start, adapter, counts = G.seg_arrays(seg)
+    assert counts[0] == want.num_segs and counts[1] == want.perm.shape[0] and counts[2] == want.bad_tokens
+    assert np.array_equal(perm, want.perm)
+    assert np.array_equal(start, want.seg_start)
+    assert np.array_equal(adapter, want.seg_adapter)
+
+
+def _check_pages(case: G.GpuCase, adapters):
+    """Device page contents of the given adapters equal the oracle's own load, bit for bit."""
+    store = H.oracle_store_for(case.wl, case.oracle_pool, adapters)
+    buf = case.pool.buffer
+    for a in adapters:
+        tab = case.oracle_pool.tables[a].astype(np.int64)
+        got = G.to_bits(buf[torch.from_numpy(tab).to(buf.device)])
+        want = store.data[store.page_slot[tab]]
+        assert np.array_equal(got, want), f"adapter {a} pages differ"
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_cases_all_modes(name):
+    wl = workloads.make(SMALL[name])
+    case = G.build_case(wl)
+    snap = case.pool.snapshot()
+    assert np.array_equal(snap["owner"], case.oracle_pool.owner)
+    _check_pages(case, case.touched)
+    want = None
+    for mode in MODES:
+        seg, want = _run_and_check(case, mode, want)
+        _check_segments(case, seg)
+    _run_and_check(case, slora.MODE_AUTO, want, multi=False)
+    case.pool.close()
+
+
+def test_full_size_llama7b_decode():
+    """The benchmark workload: H=4096, q/k/v/o, 256 tokens, 1000 adapters, Zipf 1."""
+    wl = workloads.make("llama7b_decode")
+    case = G.build_case(wl, weights="all")
+    seg, want = _run_and_check(case, slora.MODE_DECODE)
+    _check_segments(case, seg)
+    _check_pages(case, case.touched[:8])
+    _run_and_check(case, slora.MODE_AUTO, want)
+    case.pool.close()
+
+
+def _sample_rows(wl, n, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = set(rng.choice(wl.T, size=min(n, wl.T), replace=False).tolist())
+    rows |= {0, wl.T - 1}
+    return np.asarray(sorted(rows), dtype=np.int32)
+
+
+def test_full_size_llama7b_prefill_sampled():
+    wl = workloads.make("llama7b_prefill")
+    case = G.build_case(wl, weights="touched")
+    rows = _sample_rows(wl, 384)
+    want = G.oracle_outputs(case, tokens=rows)
+    for mode in (slora.MODE_AUTO, slora.MODE_PREFILL):
+        seg, _ = _run_and_check(case, mode, want, rows=rows)
+    _check_segments(case, seg)
+    case.pool.close()
+
+
+def test_full_size_llama13b_mlp_decode():
+    """120 GB pool filled by 2000 adapters and KV slots, bf16, gate/up/down."""
+    wl = workloads.make("llama13b_mlp_decode")
+    case = G.build_case(wl, weights="touched")
+    assert case.pool.snapshot()["free_pages"] == 0
+    seg, _ = _run_and_check(case, slora.MODE_DECODE)
+    _check_segments(case, seg)
+    case.pool.close()
+
+
+def test_edge_cases():
+    wl = workloads.make("tiny")
+    case = G.build_case(wl)
+    pool = case.pool
+    # empty batch
+    empty = torch.zeros(0, dtype=torch.int32, device="cuda")
+    seg = pool.build_segments(empty)
+    pool.apply(seg, 0, case.xs[0], case.ys[0], 1.0)
+    torch.cuda.synchronize()
+    assert G.seg_arrays(seg)[3][0] == 0
+    # every token base-only: y unchanged, no segments
+    case.fresh_y()
+    ta = torch.full((wl.T,), -1, dtype=torch.int32, device="cuda")
+    seg = pool.build_segments(ta)
+    pool.apply(seg, 0, case.xs[0], case.ys[0], 1.0)
+    torch.cuda.synchronize()
+    assert np.array_equal(G.to_bits(case.ys[0]), wl.y_in(0))
+    # s = 0 and a stale segment handle
+    case.fresh_y()
+    seg = pool.build_segments(case.ta_dev)
+    pool.apply(seg, 0, case.xs[0], case.ys[0], 0.0)
+    torch.cuda.synchronize()
+    assert np.array_equal(G.to_bits(case.ys[0]), wl.y_in(0))
+    pool.build_segments(case.ta_dev)
+    with pytest.raises(slora.SloraError):
+        pool.apply(seg, 0, case.xs[0], case.ys[0], 1.0)
+    # a token naming an adapter that is not resident is left out and reported
+    case.fresh_y()
+    ta = case.ta_dev.clone()
+    ta[0] = 3
+    slora.slora_adapter_evict(pool.handle, 3)
+    seg = pool.build_segments(ta)
+    pool.apply(seg, 0, case.xs[0], case.ys[0], 1.0)
+    torch.cuda.synchronize()
+    assert pool.status() == slora.ERR_NOT_RESIDENT
+    assert np.array_equal(G.to_bits(case.ys[0])[0], wl.y_in(0)[0])
+    assert pool.status() == slora.OK                  # reading clears it
+    pool.close()
+
+
+def test_evict_and_reload_into_other_pages_gives_identical_y():
+    wl = workloads.make("tiny")
+    case = G.build_case(wl)
+    seg, want = _run_and_check(case, slora.MODE_DECODE)
+    first = [G.to_bits(y) for y in case.ys]
+    old = {a: slora.slora_adapter_pages(case.pool.handle, a) for a in range(4)}
+    hold = slora.slora_pages_alloc(case.pool.handle, 5)
+    for a in range(4):
+        slora.slora_adapter_evict(case.pool.handle, a)
+    for a in (3, 1, 0, 2):
+        case.pool.load(a, int(wl.ranks[a]), wl.adapter(a))
+    case.pool.sync_loads()
+    assert any(not np.array_equal(old[a], slora.slora_adapter_pages(case.pool.handle, a)) for a in range(4))
+    case.fresh_y()
+    seg = case.pool.build_segments(case.ta_dev)
+    case.pool.apply(seg, 0, case.xs[0], case.ys[0], wl.spec.s, slora.MODE_DECODE)
+    torch.cuda.synchronize()
+    assert np.array_equal(G.to_bits(case.ys[0]), first[0])
+    del hold
+    case.pool.close()
+
+
+def test_timing_hooks_count_launches():
+    wl = workloads.make("tiny")
+    case = G.build_case(wl)
+    slora.slora_timing_enable(case.pool.handle, True)
+    seg = case.pool.build_segments(case.ta_dev)
+    case.pool.apply(seg, 0, case.xs[0], case.ys[0], 1.0, slora.MODE_DECODE)
+    t = slora.slora_timing_read(case.pool.handle)
+    assert t["build_segments"][1] == 1 and t["shrink_cc"][1] == 1 and t["expand_cc"][1] == 1
+    assert all(ms >= 0 for ms, _ in t.values())
+    case.pool.close()
