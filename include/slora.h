@@ -239,6 +239,49 @@ int slora_set_tc_threshold(slora_pool* pool, int32_t min_tokens);
 
 const char* slora_last_error_string(void);
 
+/*
+ * slora_lora_apply_noalloc -- y += s * (x A_a) B_a for one projection,
+ * allocating nothing.  The paper has no counterpart of this entry point.
+ *
+ * For callers that cannot call cudaMalloc where they compute the delta: a
+ * serving runtime that has handed all GPU memory to its own arena (page pool,
+ * KV cache, activations) and may not grow its footprint, or code that must
+ * not allocate at all while it serves.  Such a caller owns every buffer
+ * already; this call needs no slora_pool and makes no cudaMalloc, cudaFree or
+ * other allocating call.  Its scratch (token grouping and the fp32 shrink
+ * result) is one static device array of SLORA_NOALLOC_SCRATCH_BYTES that
+ * every GPU loading the library holds until the process exits.
+ *   d_pool, page_elems, dtype   the page pool (device, 16-byte aligned)
+ *   d_page_table, pt_stride     device int32; adapter a's entries start at
+ *                               a * pt_stride, in the page-table order of
+ *                               slora_adapter_load (the layout a pool uses);
+ *                               every entry read must name a page of d_pool
+ *   d_rank, max_adapters        device int32[max_adapters]; 0 = not resident;
+ *                               ranks outside [1, SLORA_MAX_RANK] count as 0
+ *   num_proj, proj_in, proj_out host arrays: every projection adapters carry
+ *   proj                        the projection to apply
+ *   d_token_adapter, T          device int32[T], ids in [-1, max_adapters);
+ *                               T <= SLORA_NOALLOC_MAX_TOKENS (else
+ *                               SLORA_ERR_INVALID); tokens with id -1 or a
+ *                               non-resident adapter are left unchanged
+ *   d_x, ldx, d_y, ldy, s       as in slora_lora_apply
+ *   stream                      cudaStream_t (NULL = legacy default stream)
+ * The first call on a device sets that device up (it looks up the device
+ * address of the scratch array and sizes the kernels' grids); make that first
+ * call before any stream capture.  Every call shares the one scratch array
+ * and leaves the last call's contents in it: calls that may overlap on the
+ * GPU (other streams, other threads) race and must be serialised by the
+ * caller.
+ */
+#define SLORA_NOALLOC_MAX_TOKENS 2048
+#define SLORA_NOALLOC_SCRATCH_BYTES 2310400u /* 2.2 MiB: grouping of 2048 tokens, 32768 ranks, v */
+int slora_lora_apply_noalloc(const void* d_pool, int32_t page_elems, int32_t dtype,
+                             const int32_t* d_page_table, int64_t pt_stride, const int32_t* d_rank,
+                             int32_t max_adapters, int32_t num_proj, const int32_t* proj_in,
+                             const int32_t* proj_out, int32_t proj, const int32_t* d_token_adapter,
+                             int32_t T, const void* d_x, int64_t ldx, void* d_y, int64_t ldy, float s,
+                             void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJ_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libslora.so")
-SOURCES = ["pool.cpp", "kernels.cu", "tc_kernels.cu"]
+SOURCES = ["pool.cpp", "kernels.cu", "tc_kernels.cu", "noalloc.cu"]
 HEADERS = [os.path.join(CSRC, "internal.h"), os.path.join(ROOT, "include", "slora.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]

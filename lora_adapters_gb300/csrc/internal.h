@@ -116,6 +116,8 @@ cudaError_t launch_shrink_cc(const ApplyDev& a, int dtype, int grid, cudaStream_
 cudaError_t launch_expand_cc(const ApplyDev& a, int dtype, int grid, cudaStream_t st);
 cudaError_t launch_scatter(const ScatterDev& a, cudaStream_t st);
 cudaError_t prepare_kernels(int device);   // opt-in shared memory sizes
+// Sets the message slora_last_error_string() returns on this thread (pool.cpp).
+void set_last_error(const char* msg);
 // Resident CTAs per SM of each persistent kernel (for grid sizing).
 int occupancy_shrink_cc(int dtype);
 int occupancy_expand_cc(int dtype);

@@ -245,6 +245,8 @@ void free_device(slora_pool* p) {
 
 }  // namespace
 
+void slora::set_last_error(const char* msg) { g_err = msg ? msg : ""; }
+
 // =================================================================================
 extern "C" {
 

@@ -35,7 +35,7 @@ EXPORTED = (
     "slora_pool_info", "slora_adapter_load", "slora_adapter_evict", "slora_adapter_pages",
     "slora_build_segments", "slora_lora_apply", "slora_lora_apply_multi", "slora_device_status",
     "slora_pool_snapshot", "slora_timing_enable", "slora_timing_read", "slora_set_tc_threshold",
-    "slora_last_error_string",
+    "slora_last_error_string", "slora_lora_apply_noalloc",
 )
 
 
@@ -72,6 +72,8 @@ _SIGS = {
     "slora_timing_enable": [P, I32],
     "slora_timing_read": [P, I32, P, P, P, P],
     "slora_set_tc_threshold": [P, I32],
+    "slora_lora_apply_noalloc": [P, I32, I32, P, I64, P, I32, I32, P, P, I32, P, I32, P, I64, P, I64,
+                                 ctypes.c_float, P],
 }
 
 
@@ -225,6 +227,20 @@ def slora_timing_read(pool: int) -> dict:
 
 def slora_set_tc_threshold(pool: int, min_tokens: int) -> None:
     _check(lib().slora_set_tc_threshold(pool, min_tokens), "slora_set_tc_threshold")
+
+
+NOALLOC_MAX_TOKENS = 2048
+
+
+def slora_lora_apply_noalloc(d_pool: int, page_elems: int, dtype: int, d_page_table: int, pt_stride: int,
+                             d_rank: int, max_adapters: int, proj_in: Sequence[int], proj_out: Sequence[int],
+                             proj: int, d_token_adapter: int, T: int, d_x: int, ldx: int, d_y: int, ldy: int,
+                             s: float, stream: int = 0) -> None:
+    """The allocation-free apply (every buffer caller-owned; see slora.h)."""
+    _check(lib().slora_lora_apply_noalloc(d_pool, page_elems, dtype, d_page_table, pt_stride, d_rank,
+                                          max_adapters, len(proj_in), _arr(proj_in, I32), _arr(proj_out, I32),
+                                          proj, d_token_adapter or None, T, d_x, ldx, d_y, ldy, s,
+                                          stream or None), "slora_lora_apply_noalloc")
 
 
 # ---- convenience wrapper for torch tensors -----------------------------------------
