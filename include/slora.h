@@ -57,6 +57,7 @@ extern "C" {
 #define SLORA_ERR_BUSY (-5)         /* reserved: the pool orders reuse by events instead */
 #define SLORA_ERR_CUDA (-6)         /* a CUDA runtime call failed (see error string) */
 #define SLORA_ERR_DEVICE (-7)       /* a kernel reported bad input (see slora_device_status) */
+#define SLORA_ERR_TIMEOUT (-8)      /* a kernel's bounded wait gave up (device status only) */
 
 /* ---- element types and apply modes -------------------------------------- */
 #define SLORA_F16 0
@@ -209,7 +210,7 @@ int slora_lora_apply_multi(slora_pool* pool, const slora_segments* seg, int32_t 
  * Synchronises the compute stream, returns in *status the first error a
  * kernel reported since the last call (SLORA_OK, SLORA_ERR_NOT_RESIDENT for a
  * token naming an adapter that is not loaded, SLORA_ERR_INVALID for an id
- * out of range) and clears it.
+ * out of range, SLORA_ERR_TIMEOUT when a pipeline wait gave up) and clears it.
  */
 int slora_device_status(slora_pool* pool, int32_t* status);
 
@@ -274,7 +275,7 @@ const char* slora_last_error_string(void);
  * caller.
  */
 #define SLORA_NOALLOC_MAX_TOKENS 2048
-#define SLORA_NOALLOC_SCRATCH_BYTES 2310400u /* 2.2 MiB: grouping of 2048 tokens, 32768 ranks, v */
+#define SLORA_NOALLOC_SCRATCH_BYTES 2482432u /* 2.2 MiB: grouping of 2048 tokens, 32768 ranks, v */
 int slora_lora_apply_noalloc(const void* d_pool, int32_t page_elems, int32_t dtype,
                              const int32_t* d_page_table, int64_t pt_stride, const int32_t* d_rank,
                              int32_t max_adapters, int32_t num_proj, const int32_t* proj_in,

@@ -11,12 +11,14 @@ constexpr int kMaxProj = 8;            // == SLORA_MAX_PROJ
 constexpr int kMaxRank = 256;          // == SLORA_MAX_RANK
 constexpr int kMaxAdapters = 32768;    // == SLORA_MAX_ADAPTERS (segment kernel keeps a histogram in smem)
 
-// CUDA-core (gather) kernels: token tile and shrink row chunk.
-constexpr int kTT = 8;                 // tokens per tile
-constexpr int kShrinkThreads = 256;    // 8 warps, one rank row per warp
-constexpr int kShrinkRows = kShrinkThreads / 32;
-constexpr int kExpandThreads = 128;    // 8 output columns (16 bytes) per thread
-constexpr int kExpandCols = kExpandThreads * 8;
+// CUDA-core (gather) kernels: persistent, one CTA per SM, 8 consumer warps
+// and one producer warp that feeds a shared-memory ring with bulk copies.
+constexpr int kTT = 4;                 // tokens per tile
+constexpr int kShrinkRows = 8;         // rank rows per shrink work unit (one per consumer warp)
+constexpr int kCcConsumerWarps = 8;
+constexpr int kCcThreads = (kCcConsumerWarps + 1) * 32;
+constexpr int kExpandCols = kCcConsumerWarps * 32 * 8;  // 8 output columns (16 bytes) per thread
+constexpr int kSegSmem = 1536;         // work-list prefix entries searched in shared memory
 constexpr int kSegThreads = 1024;
 
 // Tensor-core (tcgen05) kernels: M tile of tokens.
@@ -37,12 +39,14 @@ enum CountIdx {
 };
 
 // Device arrays written by the segment kernel.  Prefix arrays have
-// max_segs + 1 entries: prefix[s] = work units of segments < s.
+// max_segs + 1 entries over work-order positions: prefix[q] = work units of
+// the segments seg_order[0..q-1].
 struct SegDev {
   int32_t* perm;            // [max_tokens]
   int32_t* seg_start;       // [max_segs + 1]
   int32_t* seg_adapter;     // [max_segs]
   int32_t* seg_rank;        // [max_segs]
+  int32_t* seg_order;       // [max_segs] work order: segments by rank, largest first
   int32_t* counts;          // [kNumCounts]
   int32_t* cc_shrink_all;   // shrink items (token tile x rank-row chunk), every segment
   int32_t* cc_tile_all;     // token tiles, every segment
@@ -86,14 +90,44 @@ struct ApplyDev {
   const int32_t* seg_start;
   const int32_t* seg_adapter;
   const int32_t* seg_rank;
+  const int32_t* seg_order;
   const int32_t* counts;
   const int32_t* shrink_off;     // prefix array of the chosen work list
   const int32_t* tile_off;
   int32_t shrink_total_idx;      // counts[] index of the list's totals
   int32_t tile_total_idx;
-  int32_t v_ld;
+  int32_t v_ld;                  // multiple of 4 (v rows are bulk-copied)
   float s;
+  int32_t* error;                // first device error (0 = none)
+  // Per (projection, token tile) counters of the fused apply kernel: ready =
+  // rank rows of v published, passed = expand units past their wait.  Zero
+  // between calls (each call leaves them zero again).
+  int32_t* ready;                // [kMaxProj][max_tiles]
+  int32_t* passed;               // [kMaxProj][max_tiles]
+  int32_t max_tiles;
+  // Which units this launch runs: kPhaseShrink | kPhaseExpand in one launch
+  // (expand units wait on the tile counters), or one phase per launch (the
+  // kernel boundary orders them; no counters are touched).
+  int32_t phases;
 };
+constexpr int32_t kPhaseShrink = 1, kPhaseExpand = 2;
+
+// Token tiles of a batch of at most max_tokens tokens in at most max_segs
+// segments (each segment's last tile may be partial).
+inline int32_t max_token_tiles(int32_t max_tokens, int32_t max_segs) {
+  return (max_tokens + kTT - 1) / kTT + max_segs;
+}
+
+// Column tiles of a row of h_out elements over pages of H: tiles of at most
+// kExpandCols columns that never cross a page boundary.
+inline int32_t expand_col_tiles(int32_t h_out, int32_t H) {
+  int32_t n = 0;
+  for (int32_t c = 0; c * H < h_out; ++c) {
+    const int32_t len = (h_out - c * H) < H ? (h_out - c * H) : H;
+    n += (len + kExpandCols - 1) / kExpandCols;
+  }
+  return n;
+}
 
 // Adapter load: staging -> pages.
 struct ScatterDev {
@@ -112,14 +146,11 @@ struct ScatterDev {
 
 // Launchers (kernels.cu).  dtype: 0 = fp16, 1 = bf16.
 cudaError_t launch_build_segments(const SegBuildArgs& a, cudaStream_t st);
-cudaError_t launch_shrink_cc(const ApplyDev& a, int dtype, int grid, cudaStream_t st);
-cudaError_t launch_expand_cc(const ApplyDev& a, int dtype, int grid, cudaStream_t st);
+// The fused CUDA-core apply (shrink units, then expand units); grid = SMs.
+cudaError_t launch_apply_cc(const ApplyDev& a, int dtype, int grid, cudaStream_t st);
 cudaError_t launch_scatter(const ScatterDev& a, cudaStream_t st);
 cudaError_t prepare_kernels(int device);   // opt-in shared memory sizes
 // Sets the message slora_last_error_string() returns on this thread (pool.cpp).
 void set_last_error(const char* msg);
-// Resident CTAs per SM of each persistent kernel (for grid sizing).
-int occupancy_shrink_cc(int dtype);
-int occupancy_expand_cc(int dtype);
 
 }  // namespace slora

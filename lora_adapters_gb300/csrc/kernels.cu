@@ -1,6 +1,7 @@
 // CUDA-core kernels of the heterogeneous-batch LoRA path (sm_103a):
-//   build_segments  -- stable grouping of the batch's tokens by adapter
-//   shrink_cc       -- v[j, k] = x[perm[j], :] . A_a[:, k]   (gather, HBM-bound)
+//   build_segments  -- stable grouping of the batch's tokens by adapter, and
+//                      the work lists of the apply kernels
+//   shrink_cc       -- v[j, k] = x[perm[j], :] . A_a[:, k]
 //   expand_cc       -- y[perm[j], n] += s * sum_k v[j, k] B_a[k, n]
 //   scatter         -- adapter load: staged rows -> their pool pages
 //
@@ -9,10 +10,11 @@
 // method list) batches the LoRA part of tokens that use different adapters of
 // different ranks in one pass, reading adapter weights directly from
 // non-contiguous pool pages.  At decode shapes the arithmetic intensity is
-// below 2 flop/byte, so these kernels are organised around HBM traffic: each
-// distinct adapter's page rows are streamed once per token tile with 128-bit
-// loads, x and y rows are touched once per rank chunk / column tile, and
-// persistent grids walk flattened work lists built by build_segments.
+// below 2 flop/byte, so shrink and expand are organised around HBM traffic:
+// persistent CTAs (one per SM) in which one producer warp streams whole page
+// rows into a shared-memory ring with 1-D bulk copies (TMA engine, mbarrier
+// completion) while eight consumer warps compute from shared memory.  Every
+// distinct adapter row leaves HBM once per token tile.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <string.h>
@@ -22,7 +24,7 @@
 namespace slora {
 namespace {
 
-// ---- 16-bit element helpers ------------------------------------------------
+// ---- 16-bit element helpers ----------------------------------------------------
 struct F16 {
   static __device__ __forceinline__ float2 unpack(uint32_t u) {
     __half2 h;
@@ -50,37 +52,11 @@ struct BF16 {
   }
 };
 
-__device__ __forceinline__ uint4 ldg16(const uint16_t* p) {
-  return __ldg(reinterpret_cast<const uint4*>(p));
-}
-
 template <class D>
 __device__ __forceinline__ void unpack8(uint4 v, float (&f)[8]) {
   float2 a = D::unpack(v.x), b = D::unpack(v.y), c = D::unpack(v.z), e = D::unpack(v.w);
   f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
   f[4] = c.x; f[5] = c.y; f[6] = e.x; f[7] = e.y;
-}
-
-template <class D>
-__device__ __forceinline__ float dot8(uint4 a, uint4 b, float acc) {
-  float fa[8], fb[8];
-  unpack8<D>(a, fa);
-  unpack8<D>(b, fb);
-#pragma unroll
-  for (int e = 0; e < 8; ++e) acc = fmaf(fa[e], fb[e], acc);
-  return acc;
-}
-
-// Largest s in [0, S) with off[s] <= item; off is a non-decreasing prefix
-// array with off[S] > item, so segment s holds work unit `item`.
-__device__ __forceinline__ int find_seg(const int32_t* off, int S, int item) {
-  int lo = 0, hi = S - 1;
-  while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
-    if (__ldg(off + mid) <= item) lo = mid;
-    else hi = mid - 1;
-  }
-  return lo;
 }
 
 // Block-wide exclusive scan of K ints per thread; sh holds 33*K ints.
@@ -126,48 +102,156 @@ __device__ __forceinline__ void block_scan_excl(int (&v)[K], int (&total)[K], in
   __syncthreads();
 }
 
-// ---- build_segments ----------------------------------------------------------
-// One CTA of 1024 threads.  (1) histogram of adapter ids in shared memory,
-// (2) exclusive scan -> segment starts in ascending adapter id, (3) stable
-// scatter of token indices: tokens are visited in order, 1024 at a time; a
-// token's position is its adapter's running start + the number of earlier
-// tokens of the same adapter in this tile (same warp: match_any + popc;
-// earlier warps: their per-warp (adapter, count) groups), (4) per-segment
-// work-unit counts and their prefix sums for the apply kernels.
+// ---- bulk copies, mbarriers and programmatic dependent launch ------------------
+// A wait gives up after kWaitLimit polls (each poll may itself block briefly);
+// the kernel then records SLORA_ERR_TIMEOUT in the error word and leaves its
+// loop instead of spinning forever.
+constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr int kErrTimeout = -8;  // SLORA_ERR_TIMEOUT
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n\tfence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase of the given parity to complete.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+// 1-D bulk copy global -> shared through the TMA engine; completion is
+// counted in bytes on the mbarrier.  Both addresses 16-byte aligned, bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+// Programmatic dependent launch: wait for the preceding kernel's results /
+// let the next kernel's CTAs start their prologue.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ void report(int32_t* err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+// Position q (in work order) of work unit `item`: the largest q with
+// off[q] <= item, searched in shared memory when the prefix array fits there.
+__device__ __forceinline__ int find_pos(const int32_t* s_off, const int32_t* g_off, bool in_smem, int S,
+                                        int item) {
+  int lo = 0, hi = S - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    const int v = in_smem ? s_off[mid] : __ldg(g_off + mid);
+    if (v <= item) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Selects a[i] for a warp-uniform runtime index i without local memory.
+template <int N>
+__device__ __forceinline__ int pick(const int (&a)[N], int i) {
+  int v = a[0];
+#pragma unroll
+  for (int m = 1; m < N; ++m)
+    if (i == m) v = a[m];
+  return v;
+}
+
+// ---- build_segments ----------------------------------------------------------------
+// One CTA of 1024 threads.
+//  (1) histogram of adapter ids in shared memory (ids out of range or not
+//      resident are left out and reported);
+//  (2) exclusive scan -> one segment per adapter present, in ascending id;
+//  (3) stable scatter of token indices: tokens are visited in order, 1024 at
+//      a time; a token's position is its adapter's running start + the number
+//      of earlier tokens of that adapter in the tile (same warp: match_any +
+//      popc; earlier warps: their per-warp (adapter, count) groups);
+//  (4) work order: segments by rank, largest first (so that the persistent
+//      apply kernels hand out the longest work units first), then the
+//      per-position work-unit counts and their prefix sums.  Ties between
+//      equal ranks are broken by shared-memory atomics: the order of equal-
+//      rank segments, and so which CTA computes which unit, may differ from
+//      run to run; every output element is still computed by exactly one unit
+//      in a fixed order, so results do not change.
+constexpr int kCachedTiles = 4;  // token keys of the first 4096 tokens stay in registers
+
 __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBuildArgs args) {
   extern __shared__ int32_t hist[];  // [max_adapters]
   __shared__ int32_t grp_key[32][32];
   __shared__ int32_t grp_cnt[32][32];
   __shared__ int32_t ngrp[32];
   __shared__ int32_t scan_sh[33 * 6];
+  __shared__ int32_t rcount[kMaxRank + 1];
   __shared__ int32_t s_bad, s_err;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int A = args.max_adapters, T = args.T;
   const SegDev& sd = args.seg;
+  // The apply kernels may start their prologue now; they wait for this
+  // kernel's results (griddepcontrol.wait) before reading any of them.
+  pdl_trigger();
 
   for (int a = tid; a < A; a += blockDim.x) hist[a] = 0;
+  for (int r = tid; r <= kMaxRank; r += blockDim.x) rcount[r] = 0;
   if (tid == 0) {
     s_bad = 0;
     s_err = 0;
   }
   __syncthreads();
 
-  // (1) histogram; ids that are out of range or not resident are left out
-  for (int i = tid; i < T; i += blockDim.x) {
+  // (1) histogram; keys of the first tiles are kept for (3)
+  int keys[kCachedTiles];
+#pragma unroll
+  for (int c = 0; c < kCachedTiles; ++c) {
+    const int i = c * kSegThreads + tid;
+    int key = -1;
+    if (i < T) {
+      const int a = args.token_adapter[i];
+      if (a >= 0 && a < A && args.rank[a] > 0) {
+        key = a;
+        atomicAdd(&hist[a], 1);
+      } else if (a != -1) {
+        atomicAdd(&s_bad, 1);
+        atomicCAS(&s_err, 0, (a < -1 || a >= A) ? -1 /* SLORA_ERR_INVALID */ : -4 /* NOT_RESIDENT */);
+      }
+    }
+    keys[c] = key;
+  }
+  for (int i = kCachedTiles * kSegThreads + tid; i < T; i += blockDim.x) {
     const int a = args.token_adapter[i];
-    if (a == -1) continue;
-    if (a < -1 || a >= A) {
+    if (a >= 0 && a < A && args.rank[a] > 0) {
+      atomicAdd(&hist[a], 1);
+    } else if (a != -1) {
       atomicAdd(&s_bad, 1);
-      atomicCAS(&s_err, 0, -1 /* SLORA_ERR_INVALID */);
-      continue;
+      atomicCAS(&s_err, 0, (a < -1 || a >= A) ? -1 : -4);
     }
-    if (args.rank[a] <= 0) {
-      atomicAdd(&s_bad, 1);
-      atomicCAS(&s_err, 0, -4 /* SLORA_ERR_NOT_RESIDENT */);
-      continue;
-    }
-    atomicAdd(&hist[a], 1);
   }
   __syncthreads();
 
@@ -197,16 +281,17 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
 
   // (3) stable scatter, one tile of 1024 tokens at a time, in token order
   const unsigned lt = (1u << lane) - 1u;
-  for (int base = 0; base < T; base += blockDim.x) {
+  for (int c = 0, base = 0; base < T; ++c, base += blockDim.x) {
     const int i = base + tid;
     int key = -1;
-    bool valid = false;
-    if (i < T) {
-      key = args.token_adapter[i];
-      valid = key >= 0 && key < A && args.rank[key] > 0;
+    if (c < kCachedTiles) {
+      key = pick(keys, c);
+    } else if (i < T) {
+      const int a = args.token_adapter[i];
+      if (a >= 0 && a < A && args.rank[a] > 0) key = a;
     }
-    const int k2 = valid ? key : -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, k2);
+    const bool valid = key >= 0;
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
     const int rank_w = __popc(peers & lt);
     const bool leader = (peers & lt) == 0u;
     const unsigned lead_mask = __ballot_sync(0xffffffffu, valid && leader);
@@ -228,38 +313,57 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
     }
     __syncthreads();
     if (valid && leader) atomicAdd(&hist[key], __popc(peers));
-    __syncthreads();
   }
 
-  // (4) work units per segment and their prefix sums
+  // (4a) segment ranks and their histogram
+  for (int s = tid; s < segs; s += blockDim.x) {
+    const int r = args.rank[sd.seg_adapter[s]];
+    sd.seg_rank[s] = r;
+    atomicAdd(&rcount[r], 1);
+  }
+  __syncthreads();
+  // (4b) start of each rank's run, largest rank first
+  {
+    int v[1] = {tid <= kMaxRank ? rcount[kMaxRank - tid] : 0}, tot[1];
+    block_scan_excl<1>(v, tot, scan_sh);
+    if (tid <= kMaxRank) rcount[kMaxRank - tid] = v[0];
+  }
+  __syncthreads();
+  // (4c) place every segment in work order
+  for (int s = tid; s < segs; s += blockDim.x) {
+    const int r = sd.seg_rank[s];
+    sd.seg_order[atomicAdd(&rcount[r], 1)] = s;
+  }
+  __syncthreads();
+  // (4d) work units per position and their prefix sums
   int carry[6] = {0, 0, 0, 0, 0, 0};
   for (int base = 0; base < segs; base += blockDim.x) {
-    const int s = base + tid;
-    int q[6] = {0, 0, 0, 0, 0, 0};
-    if (s < segs) {
+    const int q = base + tid;
+    int u[6] = {0, 0, 0, 0, 0, 0};
+    if (q < segs) {
+      const int s = sd.seg_order[q];
       const int len = sd.seg_start[s + 1] - sd.seg_start[s];
-      const int r = args.rank[sd.seg_adapter[s]];
-      sd.seg_rank[s] = r;
+      const int r = sd.seg_rank[s];
       const int ntt = (len + kTT - 1) / kTT;
       const int nrc = (r + kShrinkRows - 1) / kShrinkRows;
       const int nmt = (len + kTcM - 1) / kTcM;
       const bool is_short = len < args.tc_threshold;
-      q[0] = ntt * nrc;
-      q[1] = ntt;
-      q[2] = is_short ? ntt * nrc : 0;
-      q[3] = is_short ? ntt : 0;
-      q[4] = nmt;
-      q[5] = is_short ? 0 : nmt;
+      u[0] = ntt * nrc;
+      u[1] = ntt;
+      u[2] = is_short ? ntt * nrc : 0;
+      u[3] = is_short ? ntt : 0;
+      u[4] = nmt;
+      u[5] = is_short ? 0 : nmt;
     }
     int tot[6];
-    block_scan_excl<6>(q, tot, scan_sh);
-    if (s < segs) {
-      sd.cc_shrink_all[s] = carry[0] + q[0];
-      sd.cc_tile_all[s] = carry[1] + q[1];
-      sd.cc_shrink_short[s] = carry[2] + q[2];
-      sd.cc_tile_short[s] = carry[3] + q[3];
-      sd.tc_tile_all[s] = carry[4] + q[4];
-      sd.tc_tile_long[s] = carry[5] + q[5];
+    block_scan_excl<6>(u, tot, scan_sh);
+    if (q < segs) {
+      sd.cc_shrink_all[q] = carry[0] + u[0];
+      sd.cc_tile_all[q] = carry[1] + u[1];
+      sd.cc_shrink_short[q] = carry[2] + u[2];
+      sd.cc_tile_short[q] = carry[3] + u[3];
+      sd.tc_tile_all[q] = carry[4] + u[4];
+      sd.tc_tile_long[q] = carry[5] + u[5];
     }
 #pragma unroll
     for (int k = 0; k < 6; ++k) carry[k] += tot[k];
@@ -280,175 +384,537 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
   }
 }
 
-// ---- shrink: v = x A (CUDA cores) -----------------------------------------------
-// Work unit = (projection, segment, token tile of <= kTT tokens, chunk of 8
-// rank rows).  Warp w owns rank row k = chunk*8 + w: it streams that A row
-// (one page per H elements) once with 16-byte loads and dots it against the
-// tile's x rows (which the CTA's 8 warps share through L1), then reduces the
-// per-lane partial sums with shuffles.
-template <class D>
-__global__ void __launch_bounds__(kShrinkThreads) shrink_cc_kernel(const __grid_constant__ ApplyDev d) {
-  const int total = d.counts[d.shrink_total_idx];
-  const int S = d.counts[kNumSegs];
-  const int64_t G = (int64_t)total * d.nproj;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int64_t g = blockIdx.x; g < G; g += gridDim.x) {
-    const int p = (int)(g / total);
-    const int item = (int)(g - (int64_t)p * total);
-    const ProjDev& P = d.proj[p];
-    const int s = find_seg(d.shrink_off, S, item);
-    const int local = item - __ldg(d.shrink_off + s);
-    const int r = __ldg(d.seg_rank + s);
-    const int nrc = (r + kShrinkRows - 1) / kShrinkRows;
-    const int tt = local / nrc, rc = local - tt * nrc;
-    const int j0 = __ldg(d.seg_start + s) + tt * kTT;
-    const int ntok = min(kTT, __ldg(d.seg_start + s + 1) - j0);
-    const int k = rc * kShrinkRows + warp;
-    if (k >= r) continue;
-    const int a = __ldg(d.seg_adapter + s);
-    const int32_t* pt = d.page_table + (int64_t)a * d.pt_stride +
-                        (int64_t)r * P.rows_before + (int64_t)k * P.ppi;
-    const uint16_t* xr[kTT];
-#pragma unroll
-    for (int t = 0; t < kTT; ++t)
-      xr[t] = static_cast<const uint16_t*>(P.x) +
-              (int64_t)__ldg(d.perm + j0 + min(t, ntok - 1)) * P.ldx;
-    float acc[kTT];
-#pragma unroll
-    for (int t = 0; t < kTT; ++t) acc[t] = 0.f;
+// ---- the fused apply kernel: shrink then expand (CUDA cores, bulk-copy pipeline) ----
+// Persistent CTA per SM (grid = number of SMs): warp 8 is the producer, warps
+// 0-7 consume.  Every CTA first runs its shrink units, then its expand units;
+// both kinds stream through the same 4-deep ring of 48 KB stages.
+//
+// Shrink unit = (segment position q, token tile of <= kTT tokens, chunk of 8
+// rank rows, projection); projection varies fastest.  Per K chunk of <=
+// kShrinkK elements (never crossing a page) producer lane i bulk-copies A row
+// k0+i straight from its pool page and lanes 8..11 the tile's x rows; consumer
+// warp w dots A row w against the x rows, keeping per-lane partial sums across
+// the unit's chunks, reduces them with shuffles and writes v; lane 0 then
+// publishes the row (release add on the tile's ready counter).
+//
+// Expand unit = (segment position q, token tile, projection, column tile of
+// <= kExpandCols columns inside one page); projection and column tile vary
+// fastest.  Before its first stage the producer waits (acquire, bounded) until
+// the tile's ready counter shows all r rows of v, then bulk-copies the tile's
+// v rows into an item ring; stages carry kExpandRK B rows each, and the last
+// stage also carries the tile's y rows.  Each consumer thread owns 8 adjacent
+// columns: fp32 accumulation over the unit's rank rows for every token of the
+// tile, then y + s * acc, one rounding, a 16-byte store.  The last of a tile's
+// expand units to pass the wait resets the tile's counters for the next call.
+//
+// The producer resolves units 32 at a time (one per lane), so page-table and
+// segment lookups of a whole batch of units cost one round of loads, and it
+// fetches the next expand unit's page indices while it streams the current one.
+#ifndef SLORA_STAGES
+#define SLORA_STAGES 4
+#endif
+constexpr int kStages = SLORA_STAGES;                  // ring depth (also the v item-ring depth)
+constexpr int kShrinkK = 2048;                         // K chunk (elements) of a shrink stage
+constexpr int kExpandRK = 8;                           // B rows per expand stage
+constexpr int kStageElems = kShrinkRows * kShrinkK + kTT * kShrinkK;   // 48 KB of 16-bit elements
+constexpr int kRowsOff = kShrinkRows * kShrinkK;       // x (shrink) / y (expand) rows start here
+constexpr int kPagesPerLane = kMaxRank / 32;           // B-row page indices one lane prefetches
+static_assert(kExpandRK * kExpandCols <= kRowsOff, "B rows of a stage must fit before the x/y rows");
+static_assert(kTT * kExpandCols <= kStageElems - kRowsOff, "y rows of a stage must fit");
+static_assert(32 % kExpandRK == 0, "a stage's B rows come from one 32-row block of page indices");
 
-    for (int chunk = 0; chunk < P.ppi; ++chunk) {
-      const uint16_t* page = d.pool + (int64_t)__ldg(pt + chunk) * d.H;
-      const int c0 = chunk * d.H;
-      const int n8 = min(d.H, P.h_in - c0) >> 3;  // 16-byte vectors in this chunk
-      for (int v0 = lane; v0 < n8; v0 += 32 * 4) {
-        uint4 av[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int vv = v0 + u * 32;
-          av[u] = vv < n8 ? ldg16(page + vv * 8) : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int t = 0; t < kTT; ++t) {
-          if (t < ntok) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int vv = v0 + u * 32;
-              if (vv < n8) acc[t] = dot8<D>(av[u], ldg16(xr[t] + c0 + vv * 8), acc[t]);
-            }
-          }
-        }
-      }
+enum : int { kKindShrink = 0, kKindExpand = 1 };
+struct __align__(16) StageMeta {
+  int kind, ntok, p, len, last;
+  int j0, k0, nrows, tile;          // shrink
+  int col0, nk, buf;                // expand (k0 = first B row of the stage)
+  int rows[kTT];
+};
+struct ApplySmem {
+  uint16_t st[kStages][kStageElems];
+  float V[kStages][kTT][kMaxRank];
+  StageMeta meta[kStages];
+  uint64_t full[kStages], empty[kStages];
+  int32_t off_s[kSegSmem], off_e[kSegSmem];
+};
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  unsigned long long ua, ub, uc, r;
+  memcpy(&ua, &a, 8);
+  memcpy(&ub, &b, 8);
+  memcpy(&uc, &c, 8);
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(ua), "l"(ub), "l"(uc));
+  float2 o;
+  memcpy(&o, &r, 8);
+  return o;
+}
+template <class D>
+__device__ __forceinline__ void unpack4x2(uint4 v, float2 (&f)[4]) {
+  f[0] = D::unpack(v.x);
+  f[1] = D::unpack(v.y);
+  f[2] = D::unpack(v.z);
+  f[3] = D::unpack(v.w);
+}
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Column tile ct of a row of h_out elements stored in pages of H: tiles never
+// cross a page; returns the page chunk c, the offset o inside it and the length.
+__device__ __forceinline__ void col_tile(int ct, int h_out, int H, int& c, int& o, int& len) {
+  for (c = 0;; ++c) {
+    const int lenc = min(H, h_out - c * H);
+    const int nt = (lenc + kExpandCols - 1) / kExpandCols;
+    if (ct < nt) {
+      o = ct * kExpandCols;
+      len = min(kExpandCols, lenc - o);
+      return;
     }
-#pragma unroll
-    for (int t = 0; t < kTT; ++t) {
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], off);
-    }
-    float mine = acc[0];
-#pragma unroll
-    for (int t = 1; t < kTT; ++t)
-      if (lane == t) mine = acc[t];
-    if (lane < ntok) P.v[(int64_t)(j0 + lane) * d.v_ld + k] = mine;
+    ct -= nt;
   }
 }
 
-// ---- expand: y += s v B (CUDA cores) ------------------------------------------
-// Work unit = (projection, segment, token tile, column tile of 1024).  The
-// tile's v rows go to shared memory; each thread owns 8 adjacent output
-// columns (one 16-byte vector), streams the adapter's B rows for them
-// (8 rows in flight), accumulates in fp32 for every token of the tile, then
-// reads y once, adds s * acc, rounds once and writes y back.
+// Page indices of B rows lane, lane+32, ... of (adapter a, rank r, projection
+// p, page chunk c).
+__device__ __forceinline__ void load_b_pages(const ApplyDev& d, int a, int r, int p, int c,
+                                             int (&pg)[kPagesPerLane], int lane) {
+  const ProjDev& P = d.proj[p];
+  const int32_t* ptB = d.page_table + (int64_t)a * d.pt_stride + (int64_t)r * (P.rows_before + P.ppi) + c;
+#pragma unroll
+  for (int m = 0; m < kPagesPerLane; ++m) {
+    const int row = lane + 32 * m;
+    pg[m] = row < r ? __ldg(ptB + (int64_t)row * P.ppo) : 0;
+  }
+}
+
+// Producer: acquire the next stage slot (lane 0 waits, the warp learns the outcome).
+__device__ __forceinline__ bool acquire_slot(ApplySmem& sm, uint32_t stage, uint32_t phase, int lane) {
+  bool got = true;
+  if (lane == 0) got = mbar_wait(&sm.empty[stage], phase ^ 1);
+  return __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+}
+
+// Stage compute of the consumer warps, specialised on the tile's token count
+// so that no issue slot goes to absent tokens.
+template <class D, int NT>
+__device__ __forceinline__ void shrink_stage(const uint16_t* arow, const uint16_t* xrows, int n8, int lane,
+                                             float (&acc)[kTT]) {
+  float s0[NT], s1[NT];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) s0[t] = s1[t] = 0.f;
+  for (int v = lane; v < n8; v += 64) {   // two vectors per lane, independent chains
+    const bool two = v + 32 < n8;
+    float fa0[8], fa1[8];
+    unpack8<D>(*reinterpret_cast<const uint4*>(arow + v * 8), fa0);
+    unpack8<D>(two ? *reinterpret_cast<const uint4*>(arow + (v + 32) * 8) : make_uint4(0u, 0u, 0u, 0u), fa1);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      float fx0[8], fx1[8];
+      unpack8<D>(*reinterpret_cast<const uint4*>(xrows + t * kShrinkK + v * 8), fx0);
+      unpack8<D>(two ? *reinterpret_cast<const uint4*>(xrows + t * kShrinkK + (v + 32) * 8)
+                     : make_uint4(0u, 0u, 0u, 0u),
+                 fx1);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        s0[t] = fmaf(fa0[e], fx0[e], s0[t]);
+        s1[t] = fmaf(fa1[e], fx1[e], s1[t]);
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < NT; ++t) acc[t] += s0[t] + s1[t];
+}
+
+template <class D, int NT>
+__device__ __forceinline__ void expand_stage(const uint16_t* brows, const float (*V)[kMaxRank], int k0, int nk,
+                                             int col, float2 (&acc)[kTT][4]) {
+#pragma unroll 2
+  for (int k = 0; k < nk; ++k) {
+    float2 fb[4];
+    unpack4x2<D>(*reinterpret_cast<const uint4*>(brows + k * kExpandCols + col), fb);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const float vv = V[t][k0 + k];
+      const float2 v2 = make_float2(vv, vv);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[t][e] = ffma2(v2, fb[e], acc[t][e]);
+    }
+  }
+}
+
 template <class D>
-__global__ void __launch_bounds__(kExpandThreads) expand_cc_kernel(const __grid_constant__ ApplyDev d) {
-  __shared__ float vt[kTT][kMaxRank];
+__global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_constant__ ApplyDev d) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  ApplySmem& sm = *reinterpret_cast<ApplySmem*>(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], kCcConsumerWarps);
+    }
+    mbar_fence_init();
+  }
+  pdl_wait();  // the work lists come from the segment kernel
+  const int units_s = d.counts[d.shrink_total_idx];
   const int tiles = d.counts[d.tile_total_idx];
   const int S = d.counts[kNumSegs];
-  int64_t G = 0;
-  for (int p = 0; p < d.nproj; ++p) G += (int64_t)tiles * d.proj[p].ncol_tiles;
-  for (int64_t g = blockIdx.x; g < G; g += gridDim.x) {
-    int p = 0;
-    int64_t gg = g;
-    while (gg >= (int64_t)tiles * d.proj[p].ncol_tiles) {
-      gg -= (int64_t)tiles * d.proj[p].ncol_tiles;
-      ++p;
+  const bool off_smem = S + 1 <= kSegSmem;
+  if (off_smem)
+    for (int i = threadIdx.x; i <= S; i += blockDim.x) {
+      sm.off_s[i] = d.shrink_off[i];
+      sm.off_e[i] = d.tile_off[i];
     }
-    const ProjDev& P = d.proj[p];
-    const int tile = (int)(gg / P.ncol_tiles);
-    const int ct = (int)(gg - (int64_t)tile * P.ncol_tiles);
-    const int s = find_seg(d.tile_off, S, tile);
-    const int tt = tile - __ldg(d.tile_off + s);
-    const int j0 = __ldg(d.seg_start + s) + tt * kTT;
-    const int ntok = min(kTT, __ldg(d.seg_start + s + 1) - j0);
-    const int r = __ldg(d.seg_rank + s);
-    const int a = __ldg(d.seg_adapter + s);
-    __syncthreads();  // vt of the previous unit is no longer read
-    for (int e = threadIdx.x; e < ntok * r; e += blockDim.x) {
-      const int t = e / r, k = e - t * r;
-      vt[t][k] = P.v[(int64_t)(j0 + t) * d.v_ld + k];
-    }
-    __syncthreads();
-    const int col = ct * kExpandCols + threadIdx.x * 8;
-    if (col >= P.h_out) continue;
-    const int chunk = col / d.H, off = col - chunk * d.H;
-    const int32_t* ptB = d.page_table + (int64_t)a * d.pt_stride +
-                         (int64_t)r * (P.rows_before + P.ppi) + chunk;
-    float acc[kTT][8];
-#pragma unroll
-    for (int t = 0; t < kTT; ++t)
-#pragma unroll
-      for (int e = 0; e < 8; ++e) acc[t][e] = 0.f;
+  __syncthreads();
+  pdl_trigger();
+  int per_tile = 0;  // expand units of one token tile: (projection, column tile)
+  for (int p = 0; p < d.nproj; ++p) per_tile += d.proj[p].ncol_tiles;
+  const int64_t Gs = (d.phases & kPhaseShrink) ? (int64_t)units_s * d.nproj : 0;
+  const int64_t Ge = (d.phases & kPhaseExpand) ? (int64_t)tiles * per_tile : 0;
+  const bool fused = d.phases == (kPhaseShrink | kPhaseExpand);  // expand waits on tile counters
+  const int64_t stride = gridDim.x;
 
-    constexpr int U = 8;
-    int k = 0;
-    for (; k + U <= r; k += U) {
-      uint4 b[U];
+  if (warp == kCcConsumerWarps) {  // ============================ producer warp
+    uint32_t stage = 0, phase = 0, nitem = 0;
+    bool ok = true;
+    // ---- shrink units
+    for (int64_t gb = blockIdx.x; gb < Gs && ok; gb += 32 * stride) {
+      const int64_t gl = gb + (int64_t)lane * stride;   // lane l resolves unit gb + l * stride
+      int m_p = 0, m_j0 = 0, m_ntok = 0, m_k0 = 0, m_nrows = 0, m_r = 0, m_a = 0, m_tile = 0;
+      int pg[kShrinkRows], xt[kTT];
 #pragma unroll
-      for (int u = 0; u < U; ++u)
-        b[u] = ldg16(d.pool + (int64_t)__ldg(ptB + (int64_t)(k + u) * P.ppo) * d.H + off);
+      for (int i = 0; i < kShrinkRows; ++i) pg[i] = 0;
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        float bf[8];
-        unpack8<D>(b[u], bf);
+      for (int t = 0; t < kTT; ++t) xt[t] = 0;
+      if (gl < Gs) {
+        const int unit = (int)(gl / d.nproj);
+        m_p = (int)(gl - (int64_t)unit * d.nproj);
+        const int q = find_pos(sm.off_s, d.shrink_off, off_smem, S, unit);
+        const int local = unit - (off_smem ? sm.off_s[q] : __ldg(d.shrink_off + q));
+        const int s = __ldg(d.seg_order + q);
+        m_r = __ldg(d.seg_rank + s);
+        m_a = __ldg(d.seg_adapter + s);
+        const int nrc = (m_r + kShrinkRows - 1) / kShrinkRows;
+        const int tt = local / nrc, rc = local - tt * nrc;
+        m_tile = (off_smem ? sm.off_e[q] : __ldg(d.tile_off + q)) + tt;
+        m_j0 = __ldg(d.seg_start + s) + tt * kTT;
+        m_ntok = min(kTT, __ldg(d.seg_start + s + 1) - m_j0);
+        m_k0 = rc * kShrinkRows;
+        m_nrows = min(kShrinkRows, m_r - m_k0);
+        const ProjDev& P = d.proj[m_p];
+        const int32_t* pt = d.page_table + (int64_t)m_a * d.pt_stride + (int64_t)m_r * P.rows_before +
+                            (int64_t)m_k0 * P.ppi;
+#pragma unroll
+        for (int i = 0; i < kShrinkRows; ++i)
+          if (i < m_nrows) pg[i] = __ldg(pt + (int64_t)i * P.ppi);
+#pragma unroll
+        for (int t = 0; t < kTT; ++t)
+          if (t < m_ntok) xt[t] = __ldg(d.perm + m_j0 + t);
+      }
+      const int nb = (int)min((int64_t)32, (Gs - gb + stride - 1) / stride);
+      for (int l = 0; l < nb && ok; ++l) {
+        const int p = __shfl_sync(0xffffffffu, m_p, l);
+        const int j0 = __shfl_sync(0xffffffffu, m_j0, l);
+        const int ntok = __shfl_sync(0xffffffffu, m_ntok, l);
+        const int k0 = __shfl_sync(0xffffffffu, m_k0, l);
+        const int nrows = __shfl_sync(0xffffffffu, m_nrows, l);
+        const int r = __shfl_sync(0xffffffffu, m_r, l);
+        const int a = __shfl_sync(0xffffffffu, m_a, l);
+        const int tile = __shfl_sync(0xffffffffu, m_tile, l);
+        int my_page = 0, my_tok = 0;
+#pragma unroll
+        for (int i = 0; i < kShrinkRows; ++i) {
+          const int v = __shfl_sync(0xffffffffu, pg[i], l);
+          if (lane == i) my_page = v;
+        }
 #pragma unroll
         for (int t = 0; t < kTT; ++t) {
-          if (t < ntok) {
-            const float vv = vt[t][k + u];
+          const int v = __shfl_sync(0xffffffffu, xt[t], l);
+          if (lane == kShrinkRows + t) my_tok = v;
+        }
+        const ProjDev& P = d.proj[p];
+        const bool has_row = lane < nrows;
+        const bool has_x = lane >= kShrinkRows && lane < kShrinkRows + ntok;
+        const int32_t* pt_row = d.page_table + (int64_t)a * d.pt_stride + (int64_t)r * P.rows_before +
+                                (int64_t)(k0 + lane) * P.ppi;
+        const uint16_t* xrow = static_cast<const uint16_t*>(P.x) + (int64_t)my_tok * P.ldx;
+        int64_t page = my_page;
+        for (int c = 0; c < P.ppi && ok; ++c) {
+          const int lenc = min(d.H, P.h_in - c * d.H);
+          // the next page of this row, fetched while this one streams
+          const int64_t next_page = (has_row && c + 1 < P.ppi) ? (int64_t)__ldg(pt_row + c + 1) : 0;
+          for (int o = 0; o < lenc; o += kShrinkK) {
+            const int len = min(kShrinkK, lenc - o);
+            const int last = (c == P.ppi - 1) && (o + len >= lenc);
+            if (!acquire_slot(sm, stage, phase, lane)) {
+              ok = false;
+              break;
+            }
+            if (lane == 0) {
+              StageMeta& m = sm.meta[stage];
+              m.kind = kKindShrink;
+              m.ntok = ntok;
+              m.p = p;
+              m.len = len;
+              m.last = last;
+              m.j0 = j0;
+              m.k0 = k0;
+              m.nrows = nrows;
+              m.tile = tile;
+              mbar_expect_tx(&sm.full[stage], (uint32_t)(nrows + ntok) * (uint32_t)len * 2u);
+            }
+            __syncwarp();
+            if (has_row)
+              bulk_load(&sm.st[stage][lane * kShrinkK], d.pool + page * d.H + o, (uint32_t)len * 2u,
+                        &sm.full[stage]);
+            if (has_x)
+              bulk_load(&sm.st[stage][kRowsOff + (lane - kShrinkRows) * kShrinkK], xrow + (int64_t)c * d.H + o,
+                        (uint32_t)len * 2u, &sm.full[stage]);
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          page = next_page;
+        }
+      }
+    }
+    // ---- expand units
+    for (int64_t gb = blockIdx.x; gb < Ge && ok; gb += 32 * stride) {
+      const int64_t gl = gb + (int64_t)lane * stride;   // lane l resolves unit gb + l * stride
+      int m_p = 0, m_j0 = 0, m_ntok = 0, m_r = 0, m_a = 0, m_c = 0, m_o = 0, m_len = 0, m_tile = 0;
+      int rws[kTT];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[t][e] = fmaf(vv, bf[e], acc[t][e]);
+      for (int t = 0; t < kTT; ++t) rws[t] = 0;
+      if (gl < Ge) {
+        m_tile = (int)(gl / per_tile);
+        int ct = (int)(gl - (int64_t)m_tile * per_tile);
+        while (ct >= d.proj[m_p].ncol_tiles) ct -= d.proj[m_p++].ncol_tiles;
+        const int q = find_pos(sm.off_e, d.tile_off, off_smem, S, m_tile);
+        const int tt = m_tile - (off_smem ? sm.off_e[q] : __ldg(d.tile_off + q));
+        const int s = __ldg(d.seg_order + q);
+        m_j0 = __ldg(d.seg_start + s) + tt * kTT;
+        m_ntok = min(kTT, __ldg(d.seg_start + s + 1) - m_j0);
+        m_r = __ldg(d.seg_rank + s);
+        m_a = __ldg(d.seg_adapter + s);
+        col_tile(ct, d.proj[m_p].h_out, d.H, m_c, m_o, m_len);
+#pragma unroll
+        for (int t = 0; t < kTT; ++t)
+          if (t < m_ntok) rws[t] = __ldg(d.perm + m_j0 + t);
+      }
+      const int nb = (int)min((int64_t)32, (Ge - gb + stride - 1) / stride);
+      int pg[kPagesPerLane];
+      load_b_pages(d, __shfl_sync(0xffffffffu, m_a, 0), __shfl_sync(0xffffffffu, m_r, 0),
+                   __shfl_sync(0xffffffffu, m_p, 0), __shfl_sync(0xffffffffu, m_c, 0), pg, lane);
+      for (int l = 0; l < nb && ok; ++l, ++nitem) {
+        const int p = __shfl_sync(0xffffffffu, m_p, l);
+        const int j0 = __shfl_sync(0xffffffffu, m_j0, l);
+        const int ntok = __shfl_sync(0xffffffffu, m_ntok, l);
+        const int r = __shfl_sync(0xffffffffu, m_r, l);
+        const int o = __shfl_sync(0xffffffffu, m_o, l);
+        const int c = __shfl_sync(0xffffffffu, m_c, l);
+        const int len = __shfl_sync(0xffffffffu, m_len, l);
+        const int tile = __shfl_sync(0xffffffffu, m_tile, l);
+        int rows[kTT];
+#pragma unroll
+        for (int t = 0; t < kTT; ++t) rows[t] = __shfl_sync(0xffffffffu, rws[t], l);
+        // prefetch the next unit's page indices
+        int pgn[kPagesPerLane];
+        const int ln = l + 1 < nb ? l + 1 : l;
+        load_b_pages(d, __shfl_sync(0xffffffffu, m_a, ln), __shfl_sync(0xffffffffu, m_r, ln),
+                     __shfl_sync(0xffffffffu, m_p, ln), __shfl_sync(0xffffffffu, m_c, ln), pgn, lane);
+        const ProjDev& P = d.proj[p];
+        // wait until every rank row of this tile's v has been published
+        if (fused && lane == 0) {
+          const int32_t* rp = d.ready + (int64_t)p * d.max_tiles + tile;
+          uint32_t it = 0;
+          while (ld_acquire(rp) < r && it < kWaitLimit) {
+            __nanosleep(32);
+            ++it;
+          }
+          if (it == kWaitLimit) ok = false;
+          asm volatile("fence.proxy.async.global;" ::: "memory");  // v is read by bulk copies below
+          if (ok && atomicAdd(d.passed + (int64_t)p * d.max_tiles + tile, 1) == P.ncol_tiles - 1) {
+            d.ready[(int64_t)p * d.max_tiles + tile] = 0;    // every unit of the tile has passed:
+            d.passed[(int64_t)p * d.max_tiles + tile] = 0;   // reset for the next call
           }
         }
+        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+          ok = false;
+          break;
+        }
+        const int col0 = c * d.H + o;
+        const int buf = (int)(nitem % kStages);
+        const uint32_t vbytes = (uint32_t)((r + 3) & ~3) * 4u;
+        for (int k0 = 0; k0 < r; k0 += kExpandRK) {
+          const int nk = min(kExpandRK, r - k0);
+          const bool first = k0 == 0;
+          const int last = k0 + nk >= r;
+          // page of B row k0 + lane: held by lane (k0 % 32) + lane, slot k0 / 32
+          const int page_i = __shfl_sync(0xffffffffu, pick(pg, k0 >> 5), (k0 & 31) + (lane % kExpandRK));
+          if (!acquire_slot(sm, stage, phase, lane)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            StageMeta& m = sm.meta[stage];
+            m.kind = kKindExpand;
+            m.ntok = ntok;
+            m.p = p;
+            m.len = len;
+            m.last = last;
+            m.k0 = k0;
+            m.col0 = col0;
+            m.nk = nk;
+            m.buf = buf;
+#pragma unroll
+            for (int t = 0; t < kTT; ++t) m.rows[t] = rows[t];
+            uint32_t bytes = (uint32_t)nk * (uint32_t)len * 2u;
+            if (first) bytes += (uint32_t)ntok * vbytes;
+            if (last) bytes += (uint32_t)ntok * (uint32_t)len * 2u;
+            mbar_expect_tx(&sm.full[stage], bytes);
+          }
+          __syncwarp();
+          if (lane < nk)
+            bulk_load(&sm.st[stage][lane * kExpandCols], d.pool + (int64_t)page_i * d.H + o, (uint32_t)len * 2u,
+                      &sm.full[stage]);
+          if (last && lane >= 8 && lane < 8 + ntok) {
+            const int t = lane - 8;
+            bulk_load(&sm.st[stage][kRowsOff + t * kExpandCols],
+                      static_cast<const uint16_t*>(P.y) + (int64_t)pick(rows, t) * P.ldy + col0,
+                      (uint32_t)len * 2u, &sm.full[stage]);
+          }
+          if (first && lane == 0) {
+            // issued by the lane that acquired the tile's ready counter and
+            // fenced the async proxy, so the copies see the published v rows
+            for (int t = 0; t < ntok; ++t)
+              bulk_load(&sm.V[buf][t][0], P.v + (int64_t)(j0 + t) * d.v_ld, vbytes, &sm.full[stage]);
+          }
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < kPagesPerLane; ++m) pg[m] = pgn[m];
       }
     }
-    for (; k < r; ++k) {
-      float bf[8];
-      unpack8<D>(ldg16(d.pool + (int64_t)__ldg(ptB + (int64_t)k * P.ppo) * d.H + off), bf);
+    if (!ok && lane == 0) report(d.error, kErrTimeout);
+  } else {  // ====================================================== consumer warps
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    // ---- shrink units: warp w owns rank row k0 + w of the unit
+    for (int64_t g = blockIdx.x; g < Gs && ok; g += stride) {
+      float acc[kTT];
 #pragma unroll
-      for (int t = 0; t < kTT; ++t) {
-        if (t < ntok) {
-          const float vv = vt[t][k];
+      for (int t = 0; t < kTT; ++t) acc[t] = 0.f;
+      while (true) {
+        if (!mbar_wait(&sm.full[stage], phase)) {
+          ok = false;
+          break;
+        }
+        const StageMeta& ms = sm.meta[stage];
+        const int ntok = ms.ntok, len = ms.len, nrows = ms.nrows, last = ms.last;
+        const int p = ms.p, j0 = ms.j0, k0 = ms.k0, tile = ms.tile;
+        if (warp < nrows) {
+          float accs[kTT];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) acc[t][e] = fmaf(vv, bf[e], acc[t][e]);
+          for (int t = 0; t < kTT; ++t) accs[t] = 0.f;
+          const uint16_t* arow = &sm.st[stage][warp * kShrinkK];
+          const uint16_t* xrows = &sm.st[stage][kRowsOff];
+          const int n8 = len >> 3;
+          switch (ntok) {
+            case 1: shrink_stage<D, 1>(arow, xrows, n8, lane, accs); break;
+            case 2: shrink_stage<D, 2>(arow, xrows, n8, lane, accs); break;
+            case 3: shrink_stage<D, 3>(arow, xrows, n8, lane, accs); break;
+            default: shrink_stage<D, 4>(arow, xrows, n8, lane, accs); break;
+          }
+#pragma unroll
+          for (int t = 0; t < kTT; ++t) acc[t] += accs[t];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[stage]);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+        if (last) {
+          if (warp < nrows) {
+            float tot[kTT];
+#pragma unroll
+            for (int t = 0; t < kTT; ++t) {
+              tot[t] = acc[t];
+#pragma unroll
+              for (int off = 16; off > 0; off >>= 1) tot[t] += __shfl_xor_sync(0xffffffffu, tot[t], off);
+            }
+            if (lane == 0) {
+              float* vrow = d.proj[p].v + (int64_t)j0 * d.v_ld + k0 + warp;
+#pragma unroll
+              for (int t = 0; t < kTT; ++t)
+                if (t < ntok) vrow[(int64_t)t * d.v_ld] = tot[t];
+              if (fused) {
+                __threadfence();  // v row visible before it is published
+                atomicAdd(d.ready + (int64_t)p * d.max_tiles + tile, 1);
+              }
+            }
+          }
+          break;
         }
       }
     }
+    // ---- expand units: thread owns 8 adjacent columns of the unit's tile
+    const int col = threadIdx.x * 8;  // threads 0..255
+    for (int64_t g = blockIdx.x; g < Ge && ok; g += stride) {
+      float2 acc[kTT][4];
 #pragma unroll
-    for (int t = 0; t < kTT; ++t) {
-      if (t < ntok) {
-        const int row = __ldg(d.perm + j0 + t);
-        uint4* yp = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.y) + (int64_t)row * P.ldy + col);
-        uint4 yv = *yp;
-        float yf[8];
-        unpack8<D>(yv, yf);
+      for (int t = 0; t < kTT; ++t)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) yf[e] = yf[e] + d.s * acc[t][e];
-        yv.x = D::pack(yf[0], yf[1]);
-        yv.y = D::pack(yf[2], yf[3]);
-        yv.z = D::pack(yf[4], yf[5]);
-        yv.w = D::pack(yf[6], yf[7]);
-        *yp = yv;
+        for (int e = 0; e < 4; ++e) acc[t][e] = make_float2(0.f, 0.f);
+      while (true) {
+        if (!mbar_wait(&sm.full[stage], phase)) {
+          ok = false;
+          break;
+        }
+        const StageMeta& me = sm.meta[stage];
+        const int ntok = me.ntok, len = me.len, nk = me.nk, k0 = me.k0, buf = me.buf, last = me.last;
+        if (col < len) {
+          const uint16_t* brows = &sm.st[stage][0];
+          switch (ntok) {
+            case 1: expand_stage<D, 1>(brows, sm.V[buf], k0, nk, col, acc); break;
+            case 2: expand_stage<D, 2>(brows, sm.V[buf], k0, nk, col, acc); break;
+            case 3: expand_stage<D, 3>(brows, sm.V[buf], k0, nk, col, acc); break;
+            default: expand_stage<D, 4>(brows, sm.V[buf], k0, nk, col, acc); break;
+          }
+          if (last) {
+            // the tile's y rows arrived with this stage; finish before releasing it
+            const ProjDev& P = d.proj[me.p];
+#pragma unroll
+            for (int t = 0; t < kTT; ++t) {
+              if (t < ntok) {
+                float2 fy[4];
+                unpack4x2<D>(*reinterpret_cast<const uint4*>(&sm.st[stage][kRowsOff + t * kExpandCols + col]), fy);
+                uint4 out;
+                out.x = D::pack(fy[0].x + d.s * acc[t][0].x, fy[0].y + d.s * acc[t][0].y);
+                out.y = D::pack(fy[1].x + d.s * acc[t][1].x, fy[1].y + d.s * acc[t][1].y);
+                out.z = D::pack(fy[2].x + d.s * acc[t][2].x, fy[2].y + d.s * acc[t][2].y);
+                out.w = D::pack(fy[3].x + d.s * acc[t][3].x, fy[3].y + d.s * acc[t][3].y);
+                *reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.y) + (int64_t)me.rows[t] * P.ldy + me.col0 + col) =
+                    out;
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[stage]);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+        if (last) break;
       }
     }
+    if (!ok && lane == 0) report(d.error, kErrTimeout);
   }
 }
 
@@ -485,9 +951,28 @@ __global__ void __launch_bounds__(128) scatter_kernel(const __grid_constant__ Sc
 
 }  // namespace
 
+template <typename Kern>
+cudaError_t launch_pdl(Kern kernel, int grid, int block, size_t smem, cudaStream_t st, const ApplyDev& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
 cudaError_t prepare_kernels(int /*device*/) {
-  return cudaFuncSetAttribute(build_segments_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)(sizeof(int32_t) * kMaxAdapters));
+  cudaError_t e = cudaFuncSetAttribute(build_segments_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)(sizeof(int32_t) * kMaxAdapters));
+  if (e != cudaSuccess) return e;
+  const int as = (int)sizeof(ApplySmem);
+  if ((e = cudaFuncSetAttribute(apply_cc_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, as))) return e;
+  return cudaFuncSetAttribute(apply_cc_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, as);
 }
 
 cudaError_t launch_build_segments(const SegBuildArgs& a, cudaStream_t st) {
@@ -496,16 +981,9 @@ cudaError_t launch_build_segments(const SegBuildArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_shrink_cc(const ApplyDev& a, int dtype, int grid, cudaStream_t st) {
-  if (dtype == 0) shrink_cc_kernel<F16><<<grid, kShrinkThreads, 0, st>>>(a);
-  else shrink_cc_kernel<BF16><<<grid, kShrinkThreads, 0, st>>>(a);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_expand_cc(const ApplyDev& a, int dtype, int grid, cudaStream_t st) {
-  if (dtype == 0) expand_cc_kernel<F16><<<grid, kExpandThreads, 0, st>>>(a);
-  else expand_cc_kernel<BF16><<<grid, kExpandThreads, 0, st>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_apply_cc(const ApplyDev& a, int dtype, int grid, cudaStream_t st) {
+  if (dtype == 0) return launch_pdl(apply_cc_kernel<F16>, grid, kCcThreads, sizeof(ApplySmem), st, a);
+  return launch_pdl(apply_cc_kernel<BF16>, grid, kCcThreads, sizeof(ApplySmem), st, a);
 }
 
 cudaError_t launch_scatter(const ScatterDev& a, cudaStream_t st) {
@@ -513,20 +991,6 @@ cudaError_t launch_scatter(const ScatterDev& a, cudaStream_t st) {
   int grid = a.n_entries < 1216 ? a.n_entries : 1216;
   scatter_kernel<<<grid, 128, 0, st>>>(a);
   return cudaGetLastError();
-}
-
-int occupancy_shrink_cc(int dtype) {
-  int n = 0;
-  if (dtype == 0) cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, shrink_cc_kernel<F16>, kShrinkThreads, 0);
-  else cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, shrink_cc_kernel<BF16>, kShrinkThreads, 0);
-  return n > 0 ? n : 1;
-}
-
-int occupancy_expand_cc(int dtype) {
-  int n = 0;
-  if (dtype == 0) cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, expand_cc_kernel<F16>, kExpandThreads, 0);
-  else cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, expand_cc_kernel<BF16>, kExpandThreads, 0);
-  return n > 0 ? n : 1;
 }
 
 }  // namespace slora

@@ -31,7 +31,9 @@ namespace {
 constexpr int kNaMaxTokens = 2048;
 constexpr int kNaMaxSegs = kNaMaxTokens;
 constexpr int kNaMaxAdapters = kMaxAdapters;
-constexpr size_t kNaIntsSeg = kNumCounts + kNaMaxTokens + 9 * (size_t)(kNaMaxSegs + 1) + 1;
+constexpr int kNaMaxTiles = (kNaMaxTokens + kTT - 1) / kTT + kNaMaxSegs;
+constexpr size_t kNaIntsSeg =
+    kNumCounts + kNaMaxTokens + 10 * (size_t)(kNaMaxSegs + 1) + 1 + 2 * (size_t)kMaxProj * kNaMaxTiles;
 constexpr size_t kNaIntsRank = kNaMaxAdapters;
 constexpr size_t kNaIntBytes = ((kNaIntsSeg + kNaIntsRank) * sizeof(int32_t) + 255) / 256 * 256;
 constexpr size_t kNaVFloats = (size_t)kNaMaxTokens * kMaxRank;
@@ -42,7 +44,7 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNaBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 unsigned char* g_scratch_dev[kMaxDevices] = {};   // device address of g_noalloc_scratch per device
-int g_grid_shrink[kMaxDevices][2] = {}, g_grid_expand[kMaxDevices][2] = {};
+int g_grid[kMaxDevices] = {};
 
 // Failures are reported through slora_last_error_string(), like every call.
 int na_fail(int code, const char* msg, cudaError_t e = cudaSuccess) {
@@ -80,10 +82,7 @@ int setup_device(int dev, unsigned char** base) {
   int sms = 0;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return na_fail(SLORA_ERR_CUDA, "cudaDeviceGetAttribute", e);
-  for (int dt = 0; dt < 2; ++dt) {
-    g_grid_shrink[dev][dt] = sms * occupancy_shrink_cc(dt);
-    g_grid_expand[dev][dt] = sms * occupancy_expand_cc(dt);
-  }
+  g_grid[dev] = sms;   // one persistent CTA per SM
   g_scratch_dev[dev] = static_cast<unsigned char*>(ptr);
   *base = g_scratch_dev[dev];
   return SLORA_OK;
@@ -145,6 +144,7 @@ extern "C" int slora_lora_apply_noalloc(const void* d_pool, int32_t page_elems, 
   sd.seg_start = q; q += S1;
   sd.seg_adapter = q; q += S1;
   sd.seg_rank = q; q += S1;
+  sd.seg_order = q; q += S1;
   sd.cc_shrink_all = q; q += S1;
   sd.cc_tile_all = q; q += S1;
   sd.cc_shrink_short = q; q += S1;
@@ -152,6 +152,9 @@ extern "C" int slora_lora_apply_noalloc(const void* d_pool, int32_t page_elems, 
   sd.tc_tile_all = q; q += S1;
   sd.tc_tile_long = q; q += S1;
   int32_t* err = q; q += 1;
+  // ready / passed counters: zero when the module loads, and every call
+  // leaves them zero again
+  int32_t* counters = q; q += 2 * kMaxProj * kNaMaxTiles;
   int32_t* rank_c = ints + kNaIntsSeg;
   float* v = reinterpret_cast<float*>(base + kNaIntBytes);
 
@@ -182,6 +185,7 @@ extern "C" int slora_lora_apply_noalloc(const void* d_pool, int32_t page_elems, 
   d.seg_start = sd.seg_start;
   d.seg_adapter = sd.seg_adapter;
   d.seg_rank = sd.seg_rank;
+  d.seg_order = sd.seg_order;
   d.counts = sd.counts;
   d.shrink_off = sd.cc_shrink_all;
   d.tile_off = sd.cc_tile_all;
@@ -189,6 +193,7 @@ extern "C" int slora_lora_apply_noalloc(const void* d_pool, int32_t page_elems, 
   d.tile_total_idx = kCcTileAll;
   d.v_ld = kMaxRank;
   d.s = s;
+  d.error = err;
   ProjDev& P = d.proj[0];
   P.x = d_x;
   P.ldx = ldx;
@@ -199,12 +204,15 @@ extern "C" int slora_lora_apply_noalloc(const void* d_pool, int32_t page_elems, 
   P.ppi = (int32_t)ceil_div64(proj_in[proj], page_elems);
   P.ppo = (int32_t)ceil_div64(proj_out[proj], page_elems);
   P.rows_before = (int32_t)before;
-  P.ncol_tiles = (int32_t)ceil_div64(P.h_out, kExpandCols);
+  P.ncol_tiles = expand_col_tiles(P.h_out, page_elems);
   P.v = v;
-  if ((e = launch_shrink_cc(d, dtype, g_grid_shrink[dev][dtype], st)) != cudaSuccess)
-    return na_fail(SLORA_ERR_CUDA, "shrink launch", e);
-  if ((e = launch_expand_cc(d, dtype, g_grid_expand[dev][dtype], st)) != cudaSuccess)
-    return na_fail(SLORA_ERR_CUDA, "expand launch", e);
+  d.ready = counters;
+  d.passed = counters + kMaxProj * kNaMaxTiles;
+  d.max_tiles = kNaMaxTiles;
+  d.phases = kPhaseShrink;
+  if ((e = launch_apply_cc(d, dtype, g_grid[dev], st)) != cudaSuccess) return na_fail(SLORA_ERR_CUDA, "shrink launch", e);
+  d.phases = kPhaseExpand;
+  if ((e = launch_apply_cc(d, dtype, g_grid[dev], st)) != cudaSuccess) return na_fail(SLORA_ERR_CUDA, "expand launch", e);
   return SLORA_OK;
 }
 

@@ -15,6 +15,7 @@
 #include <algorithm>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <string>
@@ -52,9 +53,8 @@ constexpr int32_t kOwnerFree = -1;
 constexpr int32_t kOwnerKV = -2;
 constexpr int32_t kOwnerPending = -3;
 
-enum TimerKind { kTBuild = 0, kTShrinkCC, kTExpandCC, kTShrinkTC, kTExpandTC, kTScatter, kTNum };
-const char* kTimerNames[kTNum] = {"build_segments", "shrink_cc", "expand_cc",
-                                  "shrink_tc", "expand_tc", "scatter"};
+enum TimerKind { kTBuild = 0, kTApplyCC, kTApplyTC, kTScatter, kTNum };
+const char* kTimerNames[kTNum] = {"build_segments", "apply_cc", "apply_tc", "scatter"};
 
 }  // namespace
 
@@ -91,6 +91,8 @@ struct slora_pool {
   int32_t* d_seg_mem = nullptr;
   SegDev seg{};
   float* d_v = nullptr;
+  int32_t* d_counters = nullptr;         // ready + passed counters of the fused apply
+  int32_t max_tiles = 0;
   uint16_t* d_staging = nullptr;
   std::vector<cudaEvent_t> load_event;   // per adapter id (created lazily)
   std::vector<char> load_pending;        // load event recorded, maybe not yet complete
@@ -99,7 +101,8 @@ struct slora_pool {
   uint64_t seg_generation = 0;
   int32_t seg_T = 0;
   int num_sms = 0;
-  int grid_shrink_cc = 0, grid_expand_cc = 0;
+  int grid_cc = 0;
+  bool fused_apply = false;      // one launch for shrink + expand (SLORA_FUSED_APPLY=1)
 
   // timing
   bool timing = false;
@@ -155,6 +158,10 @@ void give_back(slora_pool* p, int64_t n, const int32_t* pages) {
   }
   p->free_count += n;
 }
+
+// Row stride of the fp32 shrink scratch: a multiple of 4 floats, so that
+// every row starts on a 16-byte boundary for the bulk copies that read it.
+int32_t v_ld(const slora_pool* p) { return (p->max_rank + 3) & ~3; }
 
 int check_pool(const slora_pool* p) {
   if (!p) return fail(SLORA_ERR_INVALID, "pool is NULL");
@@ -238,6 +245,7 @@ void free_device(slora_pool* p) {
   cudaFree(p->d_error);
   cudaFree(p->d_seg_mem);
   cudaFree(p->d_v);
+  cudaFree(p->d_counters);
   cudaFree(p->d_staging);
   if (p->pt_h) cudaFreeHost(p->pt_h);
   if (p->rank_pin) cudaFreeHost(p->rank_pin);
@@ -340,7 +348,7 @@ int slora_pool_create(slora_pool** out, void* d_pool, int64_t num_pages, int32_t
     CUDA_TRY(cudaMalloc(&p->d_error, sizeof(int32_t)));
     // segment arrays: perm, seg_start, seg_adapter, seg_rank, counts, 6 prefix arrays
     const int64_t S1 = p->max_segs + 1;
-    const int64_t seg_ints = std::max<int64_t>(max_tokens, 1) + S1 * 9 + kNumCounts;
+    const int64_t seg_ints = std::max<int64_t>(max_tokens, 1) + S1 * 10 + kNumCounts;
     CUDA_TRY(cudaMalloc(&p->d_seg_mem, sizeof(int32_t) * (size_t)seg_ints));
     int32_t* q = p->d_seg_mem;
     p->seg.counts = q; q += kNumCounts;
@@ -348,14 +356,19 @@ int slora_pool_create(slora_pool** out, void* d_pool, int64_t num_pages, int32_t
     p->seg.seg_start = q; q += S1;
     p->seg.seg_adapter = q; q += S1;
     p->seg.seg_rank = q; q += S1;
+    p->seg.seg_order = q; q += S1;
     p->seg.cc_shrink_all = q; q += S1;
     p->seg.cc_tile_all = q; q += S1;
     p->seg.cc_shrink_short = q; q += S1;
     p->seg.cc_tile_short = q; q += S1;
     p->seg.tc_tile_all = q; q += S1;
     p->seg.tc_tile_long = q; q += S1;
-    CUDA_TRY(cudaMalloc(&p->d_v, sizeof(float) * (size_t)kMaxProj * std::max(max_tokens, 1) * max_rank));
+    CUDA_TRY(cudaMalloc(&p->d_v, sizeof(float) * (size_t)kMaxProj * std::max(max_tokens, 1) * v_ld(p)));
     CUDA_TRY(cudaMalloc(&p->d_staging, sizeof(uint16_t) * (size_t)p->staging_elems));
+    p->max_tiles = max_token_tiles(std::max(max_tokens, 1), p->max_segs);
+    const size_t counter_bytes = sizeof(int32_t) * 2 * kMaxProj * (size_t)p->max_tiles;
+    CUDA_TRY(cudaMalloc(&p->d_counters, counter_bytes));
+    CUDA_TRY(cudaMemsetAsync(p->d_counters, 0, counter_bytes, p->compute));
     CUDA_TRY(cudaMemsetAsync(p->d_pt, 0xff, sizeof(int32_t) * (size_t)pt_entries, p->compute));
     CUDA_TRY(cudaMemsetAsync(p->d_rank, 0, sizeof(int32_t) * (size_t)max_adapters, p->compute));
     CUDA_TRY(cudaMemsetAsync(p->d_error, 0, sizeof(int32_t), p->compute));
@@ -364,8 +377,8 @@ int slora_pool_create(slora_pool** out, void* d_pool, int64_t num_pages, int32_t
     CUDA_TRY(cudaStreamSynchronize(p->compute));
     p->load_event.assign((size_t)max_adapters, nullptr);
     p->load_pending.assign((size_t)max_adapters, 0);
-    p->grid_shrink_cc = p->num_sms * occupancy_shrink_cc(dtype);
-    p->grid_expand_cc = p->num_sms * occupancy_expand_cc(dtype);
+    p->grid_cc = p->num_sms;   // one persistent CTA per SM
+    if (const char* f = std::getenv("SLORA_FUSED_APPLY")) p->fused_apply = f[0] == '1';
     return SLORA_OK;
   };
   rc = setup();
@@ -605,8 +618,10 @@ int slora_lora_apply_multi(slora_pool* p, const slora_segments* seg, int32_t n, 
   d.seg_start = p->seg.seg_start;
   d.seg_adapter = p->seg.seg_adapter;
   d.seg_rank = p->seg.seg_rank;
+  d.seg_order = p->seg.seg_order;
   d.counts = p->seg.counts;
-  d.v_ld = p->max_rank;
+  d.v_ld = v_ld(p);
+  d.error = p->d_error;
   d.s = s;
   for (int i = 0; i < n; ++i) {
     const int q = projs[i];
@@ -626,8 +641,8 @@ int slora_lora_apply_multi(slora_pool* p, const slora_segments* seg, int32_t n, 
     P.ppi = p->ppi[q];
     P.ppo = p->ppo[q];
     P.rows_before = p->rows_before[q];
-    P.ncol_tiles = (int32_t)ceil_div(P.h_out, kExpandCols);
-    P.v = p->d_v + (int64_t)i * std::max(p->max_tokens, 1) * p->max_rank;
+    P.ncol_tiles = expand_col_tiles(P.h_out, p->H);
+    P.v = p->d_v + (int64_t)i * std::max(p->max_tokens, 1) * v_ld(p);
   }
   if (p->seg_T == 0) return SLORA_OK;
   // Until the tensor-core tiles are enabled every segment runs on the
@@ -636,14 +651,20 @@ int slora_lora_apply_multi(slora_pool* p, const slora_segments* seg, int32_t n, 
   d.tile_off = p->seg.cc_tile_all;
   d.shrink_total_idx = kCcShrinkAll;
   d.tile_total_idx = kCcTileAll;
-  {
-    Timed tm(p, kTShrinkCC, p->compute);
-    CUDA_TRY(launch_shrink_cc(d, p->dtype, p->grid_shrink_cc, p->compute));
+  d.ready = p->d_counters;
+  d.passed = p->d_counters + kMaxProj * (int64_t)p->max_tiles;
+  d.max_tiles = p->max_tiles;
+  if (p->fused_apply) {
+    d.phases = kPhaseShrink | kPhaseExpand;
+    Timed tm(p, kTApplyCC, p->compute);
+    CUDA_TRY(launch_apply_cc(d, p->dtype, p->grid_cc, p->compute));
     tm.done();
-  }
-  {
-    Timed tm(p, kTExpandCC, p->compute);
-    CUDA_TRY(launch_expand_cc(d, p->dtype, p->grid_expand_cc, p->compute));
+  } else {
+    Timed tm(p, kTApplyCC, p->compute);
+    d.phases = kPhaseShrink;
+    CUDA_TRY(launch_apply_cc(d, p->dtype, p->grid_cc, p->compute));
+    d.phases = kPhaseExpand;
+    CUDA_TRY(launch_apply_cc(d, p->dtype, p->grid_cc, p->compute));
     tm.done();
   }
   return SLORA_OK;
@@ -663,6 +684,12 @@ int slora_device_status(slora_pool* p, int32_t* status) {
   CUDA_TRY(cudaMemcpyAsync(&v, p->d_error, sizeof v, cudaMemcpyDeviceToHost, p->compute));
   CUDA_TRY(cudaMemsetAsync(p->d_error, 0, sizeof(int32_t), p->compute));
   CUDA_TRY(cudaStreamSynchronize(p->compute));
+  if (v == SLORA_ERR_TIMEOUT) {
+    // A call that gave up may have left the fused kernel's tile counters
+    // non-zero; clear them so that the next call starts clean.
+    CUDA_TRY(cudaMemsetAsync(p->d_counters, 0, sizeof(int32_t) * 2 * kMaxProj * (size_t)p->max_tiles, p->compute));
+    CUDA_TRY(cudaStreamSynchronize(p->compute));
+  }
   *status = v;
   return SLORA_OK;
 }

@@ -27,6 +27,7 @@ ERR_NOT_RESIDENT = -4
 ERR_BUSY = -5
 ERR_CUDA = -6
 ERR_DEVICE = -7
+ERR_TIMEOUT = -8
 F16, BF16 = 0, 1
 MODE_AUTO, MODE_DECODE, MODE_PREFILL = 0, 1, 2
 
