@@ -56,9 +56,15 @@ struct SegDev {
   int32_t* tc_tile_long;    // 128-token M tiles, only segments at/above the threshold
 };
 
+// Shared memory of the segment kernel (its own static arrays take ~10 KB).
+constexpr int kSegSmemMax = 200 * 1024;
+constexpr int32_t kRankInSmem = 1, kSegInSmem = 2;
+
 struct SegBuildArgs {
   const int32_t* token_adapter;  // [T]
   int32_t T;
+  int32_t seg_cap;               // segments this batch can have: min(T, max_adapters)
+  int32_t smem_flags;            // set by the launcher
   const int32_t* rank;           // [max_adapters], 0 = not resident
   int32_t max_adapters;
   int32_t tc_threshold;

@@ -187,8 +187,9 @@ __device__ __forceinline__ int pick(const int (&a)[N], int i) {
 // ---- build_segments ----------------------------------------------------------------
 // One CTA of 1024 threads.
 //  (1) histogram of adapter ids in shared memory (ids out of range or not
-//      resident are left out and reported);
-//  (2) exclusive scan -> one segment per adapter present, in ascending id;
+//      resident are left out and reported), caching each adapter's rank;
+//  (2) one block scan over the histogram (each thread owns a run of adapter
+//      ids) -> one segment per adapter present, in ascending id;
 //  (3) stable scatter of token indices: tokens are visited in order, 1024 at
 //      a time; a token's position is its adapter's running start + the number
 //      of earlier tokens of that adapter in the tile (same warp: match_any +
@@ -200,10 +201,12 @@ __device__ __forceinline__ int pick(const int (&a)[N], int i) {
 //      rank segments, and so which CTA computes which unit, may differ from
 //      run to run; every output element is still computed by exactly one unit
 //      in a fixed order, so results do not change.
+// Only step (1) reads global memory; the segment arrays are built in shared
+// memory when they fit (flag kSegInSmem) and written out at the end.
 constexpr int kCachedTiles = 4;  // token keys of the first 4096 tokens stay in registers
 
 __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBuildArgs args) {
-  extern __shared__ int32_t hist[];  // [max_adapters]
+  extern __shared__ int32_t smem_i[];
   __shared__ int32_t grp_key[32][32];
   __shared__ int32_t grp_cnt[32][32];
   __shared__ int32_t ngrp[32];
@@ -211,69 +214,95 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
   __shared__ int32_t rcount[kMaxRank + 1];
   __shared__ int32_t s_bad, s_err;
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x;
   const int A = args.max_adapters, T = args.T;
   const SegDev& sd = args.seg;
+  const bool rank_smem = (args.smem_flags & kRankInSmem) != 0;
+  const bool seg_smem = (args.smem_flags & kSegInSmem) != 0;
+  int32_t* hist = smem_i;                                        // [A]
+  int32_t* rank_s = rank_smem ? smem_i + A : nullptr;            // [A]
+  int32_t* sbase = smem_i + (rank_smem ? 2 * A : A);
+  const int cap = args.seg_cap;
+  int32_t* s_adapter = seg_smem ? sbase : sd.seg_adapter;        // [cap]
+  int32_t* s_start = seg_smem ? sbase + cap : sd.seg_start;      // [cap + 1]
+  int32_t* s_rank = seg_smem ? sbase + 2 * cap + 1 : sd.seg_rank;
+  int32_t* s_order = seg_smem ? sbase + 3 * cap + 1 : sd.seg_order;
   // The apply kernels may start their prologue now; they wait for this
   // kernel's results (griddepcontrol.wait) before reading any of them.
   pdl_trigger();
 
-  for (int a = tid; a < A; a += blockDim.x) hist[a] = 0;
-  for (int r = tid; r <= kMaxRank; r += blockDim.x) rcount[r] = 0;
+  for (int a = tid; a < A; a += nthr) hist[a] = 0;
+  for (int r = tid; r <= kMaxRank; r += nthr) rcount[r] = 0;
   if (tid == 0) {
     s_bad = 0;
     s_err = 0;
   }
   __syncthreads();
 
-  // (1) histogram; keys of the first tiles are kept for (3)
-  int keys[kCachedTiles];
-#pragma unroll
-  for (int c = 0; c < kCachedTiles; ++c) {
-    const int i = c * kSegThreads + tid;
+  // (1) histogram and rank cache; keys of the first tiles are kept for (3)
+  // Whole warps call this (inactive lanes pass i >= T); equal keys within a
+  // warp are counted with one shared-memory atomic (prefill batches hold long
+  // runs of one adapter, which would otherwise serialise on one address).
+  auto classify = [&](int i) -> int {
     int key = -1;
     if (i < T) {
       const int a = args.token_adapter[i];
-      if (a >= 0 && a < A && args.rank[a] > 0) {
-        key = a;
-        atomicAdd(&hist[a], 1);
+      if (a >= 0 && a < A) {
+        const int r = args.rank[a];
+        if (r > 0) {
+          key = a;
+          if (rank_smem) rank_s[a] = r;
+        } else {
+          atomicAdd(&s_bad, 1);
+          atomicCAS(&s_err, 0, -4 /* SLORA_ERR_NOT_RESIDENT */);
+        }
       } else if (a != -1) {
         atomicAdd(&s_bad, 1);
-        atomicCAS(&s_err, 0, (a < -1 || a >= A) ? -1 /* SLORA_ERR_INVALID */ : -4 /* NOT_RESIDENT */);
+        atomicCAS(&s_err, 0, -1 /* SLORA_ERR_INVALID */);
       }
     }
-    keys[c] = key;
-  }
-  for (int i = kCachedTiles * kSegThreads + tid; i < T; i += blockDim.x) {
-    const int a = args.token_adapter[i];
-    if (a >= 0 && a < A && args.rank[a] > 0) {
-      atomicAdd(&hist[a], 1);
-    } else if (a != -1) {
-      atomicAdd(&s_bad, 1);
-      atomicCAS(&s_err, 0, (a < -1 || a >= A) ? -1 : -4);
-    }
-  }
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    if (key >= 0 && (peers & ((1u << lane) - 1u)) == 0u) atomicAdd(&hist[key], __popc(peers));
+    return key;
+  };
+  int keys[kCachedTiles];
+#pragma unroll
+  for (int c = 0; c < kCachedTiles; ++c) keys[c] = classify(c * kSegThreads + tid);
+  for (int base = kCachedTiles * kSegThreads; base < T; base += nthr) classify(base + tid);
   __syncthreads();
 
   // (2) segments in ascending adapter id; hist[a] becomes a's running start
-  int segs = 0, pos = 0;
-  for (int base = 0; base < A; base += blockDim.x) {
-    const int a = base + tid;
-    const int c = a < A ? hist[a] : 0;
-    int v[2] = {c, c > 0 ? 1 : 0}, tot[2];
-    block_scan_excl<2>(v, tot, scan_sh);
-    if (c > 0) {
-      sd.seg_adapter[segs + v[1]] = a;
-      sd.seg_start[segs + v[1]] = pos + v[0];
-      hist[a] = pos + v[0];
+  int segs, total_pos;
+  {
+    const int m = (A + nthr - 1) / nthr;
+    const int lo = min(A, tid * m), hi = min(A, lo + m);
+    int cnt = 0, ns = 0;
+    for (int a = lo; a < hi; ++a) {
+      const int c = hist[a];
+      cnt += c;
+      ns += c > 0;
     }
-    pos += tot[0];
-    segs += tot[1];
+    int v[2] = {cnt, ns}, tot[2];
+    block_scan_excl<2>(v, tot, scan_sh);
+    int pos = v[0], s = v[1];
+    for (int a = lo; a < hi; ++a) {
+      const int c = hist[a];
+      if (c > 0) {
+        s_adapter[s] = a;
+        s_start[s] = pos;
+        s_rank[s] = rank_smem ? rank_s[a] : args.rank[a];
+        hist[a] = pos;
+        pos += c;
+        ++s;
+      }
+    }
+    total_pos = tot[0];
+    segs = tot[1];
   }
   if (tid == 0) {
-    sd.seg_start[segs] = pos;
+    s_start[segs] = total_pos;
     sd.counts[kNumSegs] = segs;
-    sd.counts[kNSorted] = pos;
+    sd.counts[kNSorted] = total_pos;
     sd.counts[kBadTokens] = s_bad;
     if (s_err != 0) atomicCAS(args.error, 0, s_err);
   }
@@ -281,7 +310,7 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
 
   // (3) stable scatter, one tile of 1024 tokens at a time, in token order
   const unsigned lt = (1u << lane) - 1u;
-  for (int c = 0, base = 0; base < T; ++c, base += blockDim.x) {
+  for (int c = 0, base = 0; base < T; ++c, base += nthr) {
     const int i = base + tid;
     int key = -1;
     if (c < kCachedTiles) {
@@ -303,11 +332,25 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
     if (lane == 0) ngrp[warp] = __popc(lead_mask);
     __syncthreads();
     if (valid) {
+      // same-key tokens of earlier warps in this tile: scan their groups,
+      // eight entries per step so the shared-memory loads overlap
       int p = hist[key] + rank_w;
       for (int w = 0; w < warp; ++w) {
         const int ng = ngrp[w];
-        for (int g = 0; g < ng; ++g)
-          if (grp_key[w][g] == key) p += grp_cnt[w][g];
+        const int* gk = grp_key[w];
+        const int* gc = grp_cnt[w];
+        int g = 0;
+        for (; g + 8 <= ng; g += 8) {
+          int kk[8], cc[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            kk[u] = gk[g + u];
+            cc[u] = gc[g + u];
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) p += kk[u] == key ? cc[u] : 0;
+        }
+        for (; g < ng; ++g) p += gk[g] == key ? gc[g] : 0;
       }
       sd.perm[p] = i;
     }
@@ -315,35 +358,44 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
     if (valid && leader) atomicAdd(&hist[key], __popc(peers));
   }
 
-  // (4a) segment ranks and their histogram
-  for (int s = tid; s < segs; s += blockDim.x) {
-    const int r = args.rank[sd.seg_adapter[s]];
-    sd.seg_rank[s] = r;
-    atomicAdd(&rcount[r], 1);
-  }
+  // (4a) histogram of segment ranks
+  for (int s = tid; s < segs; s += nthr) atomicAdd(&rcount[s_rank[s]], 1);
   __syncthreads();
-  // (4b) start of each rank's run, largest rank first
-  {
-    int v[1] = {tid <= kMaxRank ? rcount[kMaxRank - tid] : 0}, tot[1];
-    block_scan_excl<1>(v, tot, scan_sh);
-    if (tid <= kMaxRank) rcount[kMaxRank - tid] = v[0];
+  // (4b) start of each rank's run, largest rank first (warp 0; 9 ranks per lane)
+  if (warp == 0) {
+    int run = 0;
+    for (int j = 0; j < 9; ++j) {
+      const int d = lane * 9 + j;
+      if (d <= kMaxRank) run += rcount[kMaxRank - d];
+    }
+    int inc = run;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, inc, off);
+      if (lane >= off) inc += n;
+    }
+    int base = inc - run;
+    for (int j = 0; j < 9; ++j) {
+      const int d = lane * 9 + j;
+      if (d <= kMaxRank) {
+        const int c = rcount[kMaxRank - d];
+        rcount[kMaxRank - d] = base;
+        base += c;
+      }
+    }
   }
   __syncthreads();
   // (4c) place every segment in work order
-  for (int s = tid; s < segs; s += blockDim.x) {
-    const int r = sd.seg_rank[s];
-    sd.seg_order[atomicAdd(&rcount[r], 1)] = s;
-  }
+  for (int s = tid; s < segs; s += nthr) s_order[atomicAdd(&rcount[s_rank[s]], 1)] = s;
   __syncthreads();
-  // (4d) work units per position and their prefix sums
-  int carry[6] = {0, 0, 0, 0, 0, 0};
-  for (int base = 0; base < segs; base += blockDim.x) {
-    const int q = base + tid;
-    int u[6] = {0, 0, 0, 0, 0, 0};
-    if (q < segs) {
-      const int s = sd.seg_order[q];
-      const int len = sd.seg_start[s + 1] - sd.seg_start[s];
-      const int r = sd.seg_rank[s];
+  // (4d) work units per position and their prefix sums (each thread owns a run of positions)
+  {
+    const int m = (segs + nthr - 1) / nthr;
+    const int lo = min(segs, tid * m), hi = min(segs, lo + m);
+    auto units = [&](int q, int (&u)[6]) {
+      const int s = s_order[q];
+      const int len = s_start[s + 1] - s_start[s];
+      const int r = s_rank[s];
       const int ntt = (len + kTT - 1) / kTT;
       const int nrc = (r + kShrinkRows - 1) / kShrinkRows;
       const int nmt = (len + kTcM - 1) / kTcM;
@@ -354,33 +406,51 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
       u[3] = is_short ? ntt : 0;
       u[4] = nmt;
       u[5] = is_short ? 0 : nmt;
+    };
+    int sum[6] = {0, 0, 0, 0, 0, 0};
+    for (int q = lo; q < hi; ++q) {
+      int u[6];
+      units(q, u);
+#pragma unroll
+      for (int k = 0; k < 6; ++k) sum[k] += u[k];
     }
     int tot[6];
-    block_scan_excl<6>(u, tot, scan_sh);
-    if (q < segs) {
-      sd.cc_shrink_all[q] = carry[0] + u[0];
-      sd.cc_tile_all[q] = carry[1] + u[1];
-      sd.cc_shrink_short[q] = carry[2] + u[2];
-      sd.cc_tile_short[q] = carry[3] + u[3];
-      sd.tc_tile_all[q] = carry[4] + u[4];
-      sd.tc_tile_long[q] = carry[5] + u[5];
-    }
+    block_scan_excl<6>(sum, tot, scan_sh);
+    for (int q = lo; q < hi; ++q) {
+      sd.cc_shrink_all[q] = sum[0];
+      sd.cc_tile_all[q] = sum[1];
+      sd.cc_shrink_short[q] = sum[2];
+      sd.cc_tile_short[q] = sum[3];
+      sd.tc_tile_all[q] = sum[4];
+      sd.tc_tile_long[q] = sum[5];
+      int u[6];
+      units(q, u);
 #pragma unroll
-    for (int k = 0; k < 6; ++k) carry[k] += tot[k];
+      for (int k = 0; k < 6; ++k) sum[k] += u[k];
+    }
+    if (tid == 0) {
+      sd.cc_shrink_all[segs] = tot[0];
+      sd.cc_tile_all[segs] = tot[1];
+      sd.cc_shrink_short[segs] = tot[2];
+      sd.cc_tile_short[segs] = tot[3];
+      sd.tc_tile_all[segs] = tot[4];
+      sd.tc_tile_long[segs] = tot[5];
+      sd.counts[kCcShrinkAll] = tot[0];
+      sd.counts[kCcTileAll] = tot[1];
+      sd.counts[kCcShrinkShort] = tot[2];
+      sd.counts[kCcTileShort] = tot[3];
+      sd.counts[kTcTileAll] = tot[4];
+      sd.counts[kTcTileLong] = tot[5];
+    }
   }
-  if (tid == 0) {
-    sd.cc_shrink_all[segs] = carry[0];
-    sd.cc_tile_all[segs] = carry[1];
-    sd.cc_shrink_short[segs] = carry[2];
-    sd.cc_tile_short[segs] = carry[3];
-    sd.tc_tile_all[segs] = carry[4];
-    sd.tc_tile_long[segs] = carry[5];
-    sd.counts[kCcShrinkAll] = carry[0];
-    sd.counts[kCcTileAll] = carry[1];
-    sd.counts[kCcShrinkShort] = carry[2];
-    sd.counts[kCcTileShort] = carry[3];
-    sd.counts[kTcTileAll] = carry[4];
-    sd.counts[kTcTileLong] = carry[5];
+  // (5) segment arrays built in shared memory go out to global memory
+  if (seg_smem) {
+    for (int s = tid; s < segs; s += nthr) {
+      sd.seg_adapter[s] = s_adapter[s];
+      sd.seg_rank[s] = s_rank[s];
+      sd.seg_order[s] = s_order[s];
+    }
+    for (int s = tid; s <= segs; s += nthr) sd.seg_start[s] = s_start[s];
   }
 }
 
@@ -968,15 +1038,29 @@ cudaError_t launch_pdl(Kern kernel, int grid, int block, size_t smem, cudaStream
 
 cudaError_t prepare_kernels(int /*device*/) {
   cudaError_t e = cudaFuncSetAttribute(build_segments_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)(sizeof(int32_t) * kMaxAdapters));
+                                       kSegSmemMax);
   if (e != cudaSuccess) return e;
   const int as = (int)sizeof(ApplySmem);
   if ((e = cudaFuncSetAttribute(apply_cc_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, as))) return e;
   return cudaFuncSetAttribute(apply_cc_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, as);
 }
 
-cudaError_t launch_build_segments(const SegBuildArgs& a, cudaStream_t st) {
-  const size_t smem = sizeof(int32_t) * (size_t)a.max_adapters;
+cudaError_t launch_build_segments(const SegBuildArgs& in, cudaStream_t st) {
+  // Shared memory: the histogram, then (if they fit) the rank cache and the
+  // segment arrays; anything that does not fit stays in global memory.
+  SegBuildArgs a = in;
+  const size_t hist = sizeof(int32_t) * (size_t)a.max_adapters;
+  const size_t seg_arrays = sizeof(int32_t) * (4 * (size_t)a.seg_cap + 1);
+  size_t smem = hist;
+  a.smem_flags = 0;
+  if (smem + hist <= (size_t)kSegSmemMax) {
+    smem += hist;
+    a.smem_flags |= kRankInSmem;
+  }
+  if (smem + seg_arrays <= (size_t)kSegSmemMax) {
+    smem += seg_arrays;
+    a.smem_flags |= kSegInSmem;
+  }
   build_segments_kernel<<<1, kSegThreads, smem, st>>>(a);
   return cudaGetLastError();
 }

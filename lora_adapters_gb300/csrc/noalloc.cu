@@ -168,6 +168,7 @@ extern "C" int slora_lora_apply_noalloc(const void* d_pool, int32_t page_elems, 
   SegBuildArgs b{};
   b.token_adapter = d_token_adapter;
   b.T = T;
+  b.seg_cap = T < max_adapters ? T : max_adapters;
   b.rank = rank_c;
   b.max_adapters = max_adapters;
   b.tc_threshold = 1 << 30;                 // every segment on the CUDA-core kernels

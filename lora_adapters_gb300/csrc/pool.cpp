@@ -577,6 +577,7 @@ int slora_build_segments(slora_pool* p, const int32_t* d_ta, int32_t T, slora_se
   SegBuildArgs args{};
   args.token_adapter = d_ta;
   args.T = T;
+  args.seg_cap = std::max(1, std::min(T, p->max_adapters));
   args.rank = p->d_rank;
   args.max_adapters = p->max_adapters;
   args.tc_threshold = p->tc_threshold;
