@@ -32,6 +32,7 @@ sys.path.insert(0, ROOT)
 METRIC = "lora_delta_tokens_per_s_per_layer"
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20
+TC_THRESHOLD = 64          # the library's default: segments of >= 64 tokens use the tensor cores
 
 # ncu DRAM counters of the dominant kernel (dram__bytes_read.sum + write.sum,
 # per launch) on the benchmark workload, with the hash of the kernel source
@@ -57,22 +58,27 @@ def _peaks():
 
 
 # ---------------------------------------------------------------- workload
-def algorithmic_bytes(wl, elt=2):
-    """Per kernel and per step: x read + distinct adapter rows + y read/write.
+def algorithmic_bytes(wl, tc_threshold=None, elt=2):
+    """Algorithmic bytes of one step, split by the path each segment takes.
 
-    shrink: T_a * H_in (x) + sum over distinct adapters r_a * H_in, per projection;
-    expand: 2 * T_a * H_out (y read + write) + sum over distinct adapters r_a * H_out;
-    T_a = tokens that carry an adapter.  Page tables, segments and the fp32
-    shrink scratch are metadata and not counted.
+    Per projection and segment of T_s tokens on adapter a (rank r_a):
+    shrink reads x (T_s * H_in) and A_a once (r_a * H_in); expand reads and
+    writes y (2 * T_s * H_out) and reads B_a once (r_a * H_out).  Segments of
+    at least `tc_threshold` tokens go to the tensor-core kernels (None: all
+    on the CUDA-core kernels).  Page tables, segments and the shrink
+    scratch are metadata and not counted.
     """
     ta = wl.token_adapter
-    Ta = int((ta >= 0).sum())
-    distinct = sorted(set(int(a) for a in ta if a >= 0))
-    rsum = int(sum(int(wl.ranks[a]) for a in distinct))
-    shrink = sum((Ta * p.h_in + rsum * p.h_in) * elt for p in wl.projections)
-    expand = sum((2 * Ta * p.h_out + rsum * p.h_out) * elt for p in wl.projections)
-    return {"shrink": shrink, "expand": expand, "apply_cc": shrink + expand, "step": shrink + expand,
-            "distinct_adapters": len(distinct), "tokens": Ta}
+    ids, counts = np.unique(ta[ta >= 0], return_counts=True)
+    out = {"apply_cc": 0, "apply_tc": 0}
+    for a, n in zip(ids, counts):
+        r = int(wl.ranks[a])
+        b = sum((int(n) * p.h_in + r * p.h_in + 2 * int(n) * p.h_out + r * p.h_out) * elt for p in wl.projections)
+        out["apply_tc" if tc_threshold is not None and n >= tc_threshold else "apply_cc"] += b
+    out["step"] = out["apply_cc"] + out["apply_tc"]
+    out["distinct_adapters"] = int(ids.shape[0])
+    out["tokens"] = int(counts.sum())
+    return out
 
 
 def setup_device(wl, device):
@@ -304,15 +310,16 @@ def main():
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms_step = float(t.item())
     value = world * wl.T / (ms_step * 1e-3)
-    launches_per_step = 2                 # build_segments, the fused apply
+
 
     # ---- per-kernel durations: the same steps again, each kernel bracketed by
     # events on the compute stream (this serialises the launches a little, so
     # the step time above is taken without it)
     slora.slora_timing_enable(pool.handle, True)
     slora.slora_timing_read(pool.handle)                  # reset the totals
+    hook_steps = min(args.steps, 500)
     with torch.cuda.stream(stream):
-        for k in range(min(args.steps, 500)):
+        for k in range(hook_steps):
             flush.fill_(k & 0xff)
             step()
     kern = slora.slora_timing_read(pool.handle)
@@ -320,26 +327,28 @@ def main():
 
     # ---- roofline of the dominant kernel
     hbm_peak, peak_kind = _peaks()
-    ab = algorithmic_bytes(wl)
+    ab = algorithmic_bytes(wl, None if args.mode == "decode" else TC_THRESHOLD)
     per_kernel = {}
     for name in ("apply_cc", "apply_tc", "build_segments"):
         tms, cnt = kern.get(name, (0.0, 0))
         if cnt:
-            per_kernel[name] = {"avg_us": 1e3 * tms / cnt, "launches": int(cnt)}
-            if name in ab:
-                per_kernel[name]["gbs"] = ab[name] / (tms / cnt * 1e-3) / 1e9
-    dom = max(("apply_cc", "apply_tc"), key=lambda k: per_kernel.get(k, {}).get("avg_us", 0))
+            # a path's launches per step (shrink + expand) share its bytes
+            per_step_us = 1e3 * tms / hook_steps
+            per_kernel[name] = {"avg_us": 1e3 * tms / cnt, "launches": int(cnt), "us_per_step": per_step_us}
+            if name in ab and per_step_us > 0:
+                per_kernel[name]["gbs"] = ab[name] / (per_step_us * 1e-6) / 1e9
+    dom = max(("apply_cc", "apply_tc"), key=lambda k: per_kernel.get(k, {}).get("us_per_step", 0))
     achieved = per_kernel[dom]["gbs"]
     src_hash = _kernel_source_hash()
     tr = NCU_TRAFFIC.get((dom, sp.name))
     traffic = tr[0] if tr and tr[1] == src_hash else None
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                 "frac": achieved / hbm_peak, "peak_source": peak_kind, "traffic": traffic,
-                "algorithmic_bytes_per_launch": ab[dom],
+                "algorithmic_bytes_per_step": ab[dom],
                 "step_achieved_gbs": ab["step"] / (ms_step * 1e-3) / 1e9,
                 "step_frac": ab["step"] / (ms_step * 1e-3) / 1e9 / hbm_peak,
                 "kernels": per_kernel, "source_hash": src_hash}
-    launches = launches_per_step * args.steps
+    launches = int(round(sum(c for _, c in kern.values()) / hook_steps)) * args.steps
 
     # ---- end to end through the C ABI with host buffers
     pin_x = [x.cpu().pin_memory() for x in xs]

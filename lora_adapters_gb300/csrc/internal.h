@@ -2,6 +2,7 @@
 // (kernels.cu).  Not installed; the public ABI is include/slora.h.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -21,8 +22,11 @@ constexpr int kExpandCols = kCcConsumerWarps * 32 * 8;  // 8 output columns (16 
 constexpr int kSegSmem = 1536;         // work-list prefix entries searched in shared memory
 constexpr int kSegThreads = 1024;
 
-// Tensor-core (tcgen05) kernels: M tile of tokens.
+// Tensor-core (tcgen05) kernels: M tile of tokens, K block (one 128-byte
+// swizzle row of 16-bit elements), expand N tile of output columns.
 constexpr int kTcM = 128;
+constexpr int kTcK = 64;
+constexpr int kTcN = 256;
 
 // Indices into SegDev::counts.
 enum CountIdx {
@@ -135,6 +139,21 @@ inline int32_t expand_col_tiles(int32_t h_out, int32_t H) {
   return n;
 }
 
+// Tensor-core path of one apply call (long segments).
+struct TcDev {
+  ApplyDev a;                        // projections, segments, v (fp32), error word
+  CUtensorMap pool_map;              // pool as [num_pages x H], box {64, 1} (gather4 rows)
+  CUtensorMap x_map[kMaxProj];       // x of each projection as [T x h_in], box {64, 1}
+  CUtensorMap vhi_map[kMaxProj];     // v halves as [max_tokens x v16_ld], box {64, 128}
+  CUtensorMap vlo_map[kMaxProj];
+  uint16_t* vhi[kMaxProj];
+  uint16_t* vlo[kMaxProj];
+  int32_t v16_ld;                    // multiple of kTcK
+  int32_t tc_ncol[kMaxProj];         // expand column tiles per projection (tc_col_tiles)
+  const int32_t* tc_off;             // prefix array of the tensor-core tile list
+  int32_t tc_total_idx;
+};
+
 // Adapter load: staging -> pages.
 struct ScatterDev {
   const uint16_t* staging;       // packed: per projection, A rows then B rows
@@ -156,6 +175,11 @@ cudaError_t launch_build_segments(const SegBuildArgs& a, cudaStream_t st);
 cudaError_t launch_apply_cc(const ApplyDev& a, int dtype, int grid, cudaStream_t st);
 cudaError_t launch_scatter(const ScatterDev& a, cudaStream_t st);
 cudaError_t prepare_kernels(int device);   // opt-in shared memory sizes
+// Tensor-core kernels (tc_kernels.cu); the page size must be a multiple of kTcK.
+cudaError_t prepare_tc_kernels();
+cudaError_t launch_tc_shrink(const TcDev& a, int dtype, int grid, cudaStream_t st);
+cudaError_t launch_tc_expand(const TcDev& a, int dtype, int grid, cudaStream_t st);
+int32_t tc_col_tiles(int32_t h_out, int32_t H);
 // Sets the message slora_last_error_string() returns on this thread (pool.cpp).
 void set_last_error(const char* msg);
 

@@ -10,9 +10,12 @@
 // abstract): one cudaMemcpyAsync per weight block into a device staging
 // buffer on the copy stream, then a scatter kernel that writes each row chunk
 // to its page; the compute stream waits on the load's event before using it.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -103,6 +106,12 @@ struct slora_pool {
   int num_sms = 0;
   int grid_cc = 0;
   bool fused_apply = false;      // one launch for shrink + expand (SLORA_FUSED_APPLY=1)
+  // tensor-core path (page size a multiple of kTcK)
+  bool tc_ok = false;
+  int32_t v16_ld = 0;            // row stride of the 16-bit v halves
+  uint16_t* d_v16 = nullptr;     // v_hi then v_lo, [kMaxProj][max_tokens][v16_ld] each
+  CUtensorMap pool_map{};
+  CUtensorMap vhi_map[kMaxProj]{}, vlo_map[kMaxProj]{};
 
   // timing
   bool timing = false;
@@ -162,6 +171,36 @@ void give_back(slora_pool* p, int64_t n, const int32_t* pages) {
 // Row stride of the fp32 shrink scratch: a multiple of 4 floats, so that
 // every row starts on a 16-byte boundary for the bulk copies that read it.
 int32_t v_ld(const slora_pool* p) { return (p->max_rank + 3) & ~3; }
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// A 2-D map of 16-bit elements, 128-byte swizzle: `cols` x `rows` with a
+// row stride of `row_bytes`, box of box_cols x box_rows.
+int encode_2d(CUtensorMap* m, const void* base, int dtype, uint64_t cols, uint64_t rows, uint64_t row_bytes,
+              uint32_t box_cols, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return fail(SLORA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, dtype == SLORA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                  const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SLORA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return SLORA_OK;
+}
 
 int check_pool(const slora_pool* p) {
   if (!p) return fail(SLORA_ERR_INVALID, "pool is NULL");
@@ -246,6 +285,7 @@ void free_device(slora_pool* p) {
   cudaFree(p->d_seg_mem);
   cudaFree(p->d_v);
   cudaFree(p->d_counters);
+  cudaFree(p->d_v16);
   cudaFree(p->d_staging);
   if (p->pt_h) cudaFreeHost(p->pt_h);
   if (p->rank_pin) cudaFreeHost(p->rank_pin);
@@ -379,6 +419,29 @@ int slora_pool_create(slora_pool** out, void* d_pool, int64_t num_pages, int32_t
     p->load_pending.assign((size_t)max_adapters, 0);
     p->grid_cc = p->num_sms;   // one persistent CTA per SM
     if (const char* f = std::getenv("SLORA_FUSED_APPLY")) p->fused_apply = f[0] == '1';
+    // Tensor-core path: needs pages of whole 64-element K blocks.
+    p->tc_ok = page_elems % kTcK == 0;
+    if (p->tc_ok) {
+      p->v16_ld = (max_rank + kTcK - 1) / kTcK * kTcK;
+      const int64_t rows = std::max(max_tokens, kTcM);   // at least one 128-row box
+      const size_t half_elems = (size_t)kMaxProj * rows * p->v16_ld;
+      CUDA_TRY(cudaMalloc(&p->d_v16, sizeof(uint16_t) * 2 * half_elems));
+      CUDA_TRY(cudaMemsetAsync(p->d_v16, 0, sizeof(uint16_t) * 2 * half_elems, p->compute));
+      if (int rc = encode_2d(&p->pool_map, p->d_pool, dtype, (uint64_t)page_elems, (uint64_t)num_pages,
+                             (uint64_t)page_elems * 2, kTcK, 1))
+        return rc;
+      for (int i = 0; i < kMaxProj; ++i) {
+        uint16_t* hi = p->d_v16 + (size_t)i * rows * p->v16_ld;
+        uint16_t* lo = hi + half_elems;
+        if (int rc = encode_2d(&p->vhi_map[i], hi, dtype, p->v16_ld, rows, (uint64_t)p->v16_ld * 2, kTcK, kTcM))
+          return rc;
+        if (int rc = encode_2d(&p->vlo_map[i], lo, dtype, p->v16_ld, rows, (uint64_t)p->v16_ld * 2, kTcK, kTcM))
+          return rc;
+      }
+      CUDA_TRY(prepare_tc_kernels());
+    } else {
+      p->tc_threshold = INT32_MAX;   // every segment stays on the CUDA-core kernels
+    }
     return SLORA_OK;
   };
   rc = setup();
@@ -646,16 +709,63 @@ int slora_lora_apply_multi(slora_pool* p, const slora_segments* seg, int32_t n, 
     P.v = p->d_v + (int64_t)i * std::max(p->max_tokens, 1) * v_ld(p);
   }
   if (p->seg_T == 0) return SLORA_OK;
-  // Until the tensor-core tiles are enabled every segment runs on the
-  // CUDA-core kernels, whatever the mode.
-  d.shrink_off = p->seg.cc_shrink_all;
-  d.tile_off = p->seg.cc_tile_all;
-  d.shrink_total_idx = kCcShrinkAll;
-  d.tile_total_idx = kCcTileAll;
-  d.ready = p->d_counters;
-  d.passed = p->d_counters + kMaxProj * (int64_t)p->max_tiles;
-  d.max_tiles = p->max_tiles;
-  if (p->fused_apply) {
+  const bool use_tc = p->tc_ok && mode != SLORA_MODE_DECODE;
+  if (use_tc) {
+    // short segments on the CUDA-core kernels, long ones on the tensor cores
+    d.shrink_off = p->seg.cc_shrink_short;
+    d.tile_off = p->seg.cc_tile_short;
+    d.shrink_total_idx = kCcShrinkShort;
+    d.tile_total_idx = kCcTileShort;
+  } else {
+    d.shrink_off = p->seg.cc_shrink_all;
+    d.tile_off = p->seg.cc_tile_all;
+    d.shrink_total_idx = kCcShrinkAll;
+    d.tile_total_idx = kCcTileAll;
+  }
+  if (use_tc) {
+    TcDev t;
+    memset(&t, 0, sizeof t);
+    t.a = d;
+    t.pool_map = p->pool_map;
+    t.v16_ld = p->v16_ld;
+    const int64_t rows = std::max(p->max_tokens, kTcM);
+    const size_t half_elems = (size_t)kMaxProj * rows * p->v16_ld;
+    for (int i = 0; i < n; ++i) {
+      const ProjDev& P = d.proj[i];
+      if (int rc = encode_2d(&t.x_map[i], P.x, p->dtype, (uint64_t)P.h_in, (uint64_t)p->seg_T,
+                             (uint64_t)P.ldx * 2, kTcK, 1))
+        return rc;
+      t.vhi_map[i] = p->vhi_map[i];
+      t.vlo_map[i] = p->vlo_map[i];
+      t.vhi[i] = p->d_v16 + (size_t)i * rows * p->v16_ld;
+      t.vlo[i] = t.vhi[i] + half_elems;
+      t.tc_ncol[i] = tc_col_tiles(P.h_out, p->H);
+    }
+    t.tc_off = p->seg.tc_tile_long;
+    t.tc_total_idx = kTcTileLong;
+    d.phases = kPhaseShrink;
+    {
+      Timed tm(p, kTApplyCC, p->compute);
+      CUDA_TRY(launch_apply_cc(d, p->dtype, p->grid_cc, p->compute));
+      tm.done();
+    }
+    {
+      Timed tm(p, kTApplyTC, p->compute);
+      CUDA_TRY(launch_tc_shrink(t, p->dtype, p->grid_cc, p->compute));
+      tm.done();
+    }
+    d.phases = kPhaseExpand;
+    {
+      Timed tm(p, kTApplyCC, p->compute);
+      CUDA_TRY(launch_apply_cc(d, p->dtype, p->grid_cc, p->compute));
+      tm.done();
+    }
+    {
+      Timed tm(p, kTApplyTC, p->compute);
+      CUDA_TRY(launch_tc_expand(t, p->dtype, p->grid_cc, p->compute));
+      tm.done();
+    }
+  } else if (p->fused_apply) {
     d.phases = kPhaseShrink | kPhaseExpand;
     Timed tm(p, kTApplyCC, p->compute);
     CUDA_TRY(launch_apply_cc(d, p->dtype, p->grid_cc, p->compute));

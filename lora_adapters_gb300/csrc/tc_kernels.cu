@@ -1,0 +1,562 @@
+// Tensor-core (tcgen05) kernels of the LoRA delta for long segments (prefill).
+//
+// A segment of many tokens on one adapter turns the per-token products into
+// dense contractions ("S-LoRA: Serving Thousands of Concurrent LoRA
+// Adapters": heterogeneous batching runs custom kernels directly on the
+// non-contiguous pool; the pages give no kernel internals).  Per work unit a
+// 128-token tile of one segment is multiplied on the 5th-generation tensor
+// cores, fp16/bf16 operands from shared memory, fp32 accumulators in TMEM:
+//
+//   tc_shrink:  V[128 x r] = X[128 x H_in] . A^T   (A rows = pages, K-major)
+//   tc_expand:  Y[128 x 256] += s * (V_hi + V_lo)[128 x r] . B[r x 256]
+//
+// Operands are gathered by the TMA engine straight from where they live:
+// token rows of x by `tile::gather4` through the segment's sorted token list,
+// adapter rows by `gather4` over the page pool viewed as a [pages x H] matrix,
+// v rows (consecutive in sorted order) by 2-D tiles; all land in shared
+// memory in the 128-byte-swizzled layout the MMA reads.  V is carried as two
+// 16-bit halves, V_hi = round(v) and V_lo = round(v - V_hi), so the expand
+// multiplies with ~fp32 accuracy on 16-bit tensor cores.
+//
+// Each kernel is persistent (one CTA per SM) and warp-specialised: warp 0
+// issues copies into a ring of shared-memory stages, warp 1 owns TMEM and
+// issues the MMAs (one thread), warps 2-5 drain a TMEM accumulator (two of
+// them, so the epilogue of one unit overlaps the MMAs of the next) and write
+// v or y.  Every wait is bounded (SLORA_ERR_TIMEOUT on give-up).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <string.h>
+
+#include <type_traits>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace slora {
+namespace {
+
+using namespace ptx;
+
+constexpr int kTcThreads = 6 * 32;
+constexpr int kRowBytes = kTcK * 2;  // one 64-element K (or N) row of a swizzle atom = 128 bytes
+
+__device__ __forceinline__ void report_err(int32_t* err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+// Largest q with off[q] <= item (prefix array, shared memory when it fits).
+__device__ __forceinline__ int find_pos_tc(const int32_t* s_off, const int32_t* g_off, bool in_smem, int S,
+                                           int item) {
+  int lo = 0, hi = S - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    const int v = in_smem ? s_off[mid] : __ldg(g_off + mid);
+    if (v <= item) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+struct TcUnit {
+  int p, j0, len, r, a, seg;
+};
+
+// Tile `tile` of the long-segment list: segment (in work order) and row range.
+__device__ __forceinline__ TcUnit tc_tile(const TcDev& t, const int32_t* s_off, bool in_smem, int S, int tile,
+                                          int p) {
+  const ApplyDev& d = t.a;
+  TcUnit u;
+  const int q = find_pos_tc(s_off, t.tc_off, in_smem, S, tile);
+  const int mt = tile - (in_smem ? s_off[q] : __ldg(t.tc_off + q));
+  const int s = __ldg(d.seg_order + q);
+  const int start = __ldg(d.seg_start + s), end = __ldg(d.seg_start + s + 1);
+  u.p = p;
+  u.j0 = start + mt * kTcM;
+  u.len = min(kTcM, end - u.j0);
+  u.r = __ldg(d.seg_rank + s);
+  u.a = __ldg(d.seg_adapter + s);
+  u.seg = s;
+  return u;
+}
+
+// Column tile nt of a row of h_out elements over pages of H: tiles of at most
+// kTcN columns that never cross a page.
+__device__ __forceinline__ void tc_col_tile(int nt, int h_out, int H, int& c, int& o, int& len) {
+  for (c = 0;; ++c) {
+    const int lenc = min(H, h_out - c * H);
+    const int n = (lenc + kTcN - 1) / kTcN;
+    if (nt < n) {
+      o = nt * kTcN;
+      len = min(kTcN, lenc - o);
+      return;
+    }
+    nt -= n;
+  }
+}
+
+template <class T>
+struct Elem;
+template <>
+struct Elem<__half> {
+  static __device__ __forceinline__ uint16_t from(float f) { return __half_as_ushort(__float2half_rn(f)); }
+  static __device__ __forceinline__ float to(uint16_t u) { return __half2float(__ushort_as_half(u)); }
+};
+template <>
+struct Elem<__nv_bfloat16> {
+  static __device__ __forceinline__ uint16_t from(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
+  static __device__ __forceinline__ float to(uint16_t u) { return __bfloat162float(__ushort_as_bfloat16(u)); }
+};
+
+// ================================================================ tc_shrink
+constexpr int kShrinkTcStages = 4;
+struct TcShrinkSmem {
+  uint8_t X[kShrinkTcStages][kTcM * kRowBytes];     // 128 token rows x 64 K, swizzled (16 KB)
+  uint8_t B[kShrinkTcStages][kMaxRank * kRowBytes]; // <= 256 adapter rows x 64 K (32 KB)
+  uint64_t full[kShrinkTcStages], empty[kShrinkTcStages], tfull[2], tempty[2];
+  uint32_t tmem_slot;
+  int32_t off[kSegSmem];
+};
+
+template <class E>
+__global__ void __launch_bounds__(kTcThreads, 1) tc_shrink_kernel(const __grid_constant__ TcDev t) {
+  extern __shared__ uint8_t smem_raw[];
+  TcShrinkSmem& sm = *reinterpret_cast<TcShrinkSmem*>(smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023));
+  const ApplyDev& d = t.a;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 1) tmem_alloc(&sm.tmem_slot, 2 * kTcN);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kShrinkTcStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.tfull[b], 1);
+      mbar_init(&sm.tempty[b], 4);
+    }
+    mbar_fence_init();
+  }
+  pdl_wait();
+  const int tiles = d.counts[t.tc_total_idx];
+  const int S = d.counts[kNumSegs];
+  const bool off_smem = S + 1 <= kSegSmem;
+  if (off_smem)
+    for (int i = threadIdx.x; i <= S; i += blockDim.x) sm.off[i] = t.tc_off[i];
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pdl_trigger();
+  const uint32_t tmem = sm.tmem_slot;
+  const int64_t G = (int64_t)tiles * d.nproj;
+  constexpr bool bf16 = std::is_same<E, __nv_bfloat16>::value;
+  bool ok = true;
+
+  if (warp == 0) {  // ------------------------------------------ producer
+    uint32_t stage = 0, phase = 0;
+    for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x) {
+      const int tile = (int)(g / d.nproj);
+      const TcUnit u = tc_tile(t, sm.off, off_smem, S, tile, (int)(g - (int64_t)tile * d.nproj));
+      const ProjDev& P = d.proj[u.p];
+      const int r16 = (u.r + 15) & ~15;
+      const int nx4 = (u.len + 3) >> 2;  // gather4 ops for the token rows
+      const int nb4 = r16 >> 2;          // gather4 ops for the adapter rows
+      int tok[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int m = 4 * lane + i;
+        tok[i] = __ldg(d.perm + u.j0 + (m < u.len ? m : 0));
+      }
+      const int32_t* pt = d.page_table + (int64_t)u.a * d.pt_stride + (int64_t)u.r * P.rows_before;
+      const int nkb = (P.h_in + kTcK - 1) / kTcK;
+      int chunk = -1;
+      int pg[2][4];
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int k0 = kb * kTcK, c = k0 / d.H, o = k0 - c * d.H;
+        if (c != chunk) {  // page of each adapter row for this page chunk
+          chunk = c;
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int row = 128 * h + 4 * lane + i;
+              pg[h][i] = __ldg(pt + (int64_t)(row < u.r ? row : 0) * P.ppi + c);
+            }
+        }
+        bool got = true;
+        if (lane == 0) got = mbar_wait(&sm.empty[stage], phase ^ 1);
+        if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) mbar_expect_tx(&sm.full[stage], (uint32_t)(4 * nx4 + 4 * nb4) * kRowBytes);
+        __syncwarp();
+        if (lane < nx4)
+          tma_gather4(&sm.X[stage][4 * lane * kRowBytes], &t.x_map[u.p], k0, tok[0], tok[1], tok[2], tok[3],
+                      &sm.full[stage]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          if (32 * h + lane < nb4)
+            tma_gather4(&sm.B[stage][(128 * h + 4 * lane) * kRowBytes], &t.pool_map, o, pg[h][0], pg[h][1],
+                        pg[h][2], pg[h][3], &sm.full[stage]);
+        if (++stage == kShrinkTcStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+  } else if (warp == 1) {  // ----------------------------------- MMA issuer
+    uint32_t stage = 0, phase = 0;
+    int n = 0;
+    for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x, ++n) {
+      const int tile = (int)(g / d.nproj);
+      const int p = (int)(g - (int64_t)tile * d.nproj);
+      int r = 0;
+      if (lane == 0) r = tc_tile(t, sm.off, off_smem, S, tile, p).r;
+      r = __shfl_sync(0xffffffffu, r, 0);
+      const int r16 = (r + 15) & ~15;
+      const int ab = n & 1;
+      const ProjDev& P = d.proj[p];
+      const int nkb = (P.h_in + kTcK - 1) / kTcK;
+      bool got = true;
+      if (lane == 0) got = mbar_wait(&sm.tempty[ab], ((n >> 1) & 1) ^ 1);
+      if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t idesc = umma_idesc_f16(kTcM, r16, bf16, false);
+      const uint32_t dtm = tmem + (uint32_t)(ab * kTcN);
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (lane == 0) got = mbar_wait(&sm.full[stage], phase);
+        if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t xa = smem_addr(sm.X[stage]), ba = smem_addr(sm.B[stage]);
+#pragma unroll
+          for (int ks = 0; ks < kTcK / 16; ++ks)
+            umma_f16(dtm, umma_desc_sw128(xa + ks * 32, 16, 1024), umma_desc_sw128(ba + ks * 32, 16, 1024), idesc,
+                     (kb | ks) ? 1u : 0u);
+          umma_commit(&sm.empty[stage]);  // the stage is free once these MMAs have read it
+        }
+        __syncwarp();
+        if (++stage == kShrinkTcStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) umma_commit(&sm.tfull[ab]);
+      __syncwarp();
+    }
+  } else {  // ------------------------------------------------- epilogue (warps 2-5)
+    const int quarter = warp & 3;  // TMEM lanes this warp may read
+    const int m = 32 * quarter + lane;
+    int n = 0;
+    for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x, ++n) {
+      const int tile = (int)(g / d.nproj);
+      const TcUnit u = tc_tile(t, sm.off, off_smem, S, tile, (int)(g - (int64_t)tile * d.nproj));
+      const int r16 = (u.r + 15) & ~15;
+      const int ab = n & 1;
+      bool got = true;
+      if (lane == 0) got = mbar_wait(&sm.tfull[ab], (n >> 1) & 1);
+      if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int j = u.j0 + m;
+      float* vrow = d.proj[u.p].v + (int64_t)j * d.v_ld;
+      uint16_t* hrow = t.vhi[u.p] + (int64_t)j * t.v16_ld;
+      uint16_t* lrow = t.vlo[u.p] + (int64_t)j * t.v16_ld;
+      for (int c0 = 0; c0 < r16; c0 += 16) {
+        float v[16];
+        tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(ab * kTcN + c0), v);
+        if (m < u.len) {
+          uint16_t hi[16], lo[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const bool in = c0 + i < u.r;
+            const float x = in ? v[i] : 0.f;
+            hi[i] = Elem<E>::from(x);
+            lo[i] = Elem<E>::from(x - Elem<E>::to(hi[i]));
+            if (in) vrow[c0 + i] = x;
+          }
+          uint4 h0, h1, l0, l1;
+          memcpy(&h0, hi, 16);
+          memcpy(&h1, hi + 8, 16);
+          memcpy(&l0, lo, 16);
+          memcpy(&l1, lo + 8, 16);
+          *reinterpret_cast<uint4*>(hrow + c0) = h0;
+          *reinterpret_cast<uint4*>(hrow + c0 + 8) = h1;
+          *reinterpret_cast<uint4*>(lrow + c0) = l0;
+          *reinterpret_cast<uint4*>(lrow + c0 + 8) = l1;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.tempty[ab]);
+    }
+  }
+  if (!ok && lane == 0) report_err(d.error, kErrTimeout);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 2 * kTcN);
+  }
+}
+
+// ================================================================ tc_expand
+constexpr int kExpandTcStages = 3;
+struct TcExpandSmem {
+  uint8_t Ahi[kExpandTcStages][kTcM * kRowBytes];          // 128 x 64 ranks (16 KB)
+  uint8_t Alo[kExpandTcStages][kTcM * kRowBytes];          // 16 KB
+  uint8_t B[kExpandTcStages][(kTcN / 64) * kTcK * kRowBytes];  // 4 column atoms x 64 rank rows (32 KB)
+  uint64_t full[kExpandTcStages], empty[kExpandTcStages], tfull[2], tempty[2];
+  uint32_t tmem_slot;
+  int32_t off[kSegSmem];
+};
+
+template <class E>
+__global__ void __launch_bounds__(kTcThreads, 1) tc_expand_kernel(const __grid_constant__ TcDev t) {
+  extern __shared__ uint8_t smem_raw[];
+  TcExpandSmem& sm = *reinterpret_cast<TcExpandSmem*>(smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023));
+  const ApplyDev& d = t.a;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 1) tmem_alloc(&sm.tmem_slot, 2 * kTcN);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kExpandTcStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.tfull[b], 1);
+      mbar_init(&sm.tempty[b], 4);
+    }
+    mbar_fence_init();
+  }
+  pdl_wait();
+  const int tiles = d.counts[t.tc_total_idx];
+  const int S = d.counts[kNumSegs];
+  const bool off_smem = S + 1 <= kSegSmem;
+  if (off_smem)
+    for (int i = threadIdx.x; i <= S; i += blockDim.x) sm.off[i] = t.tc_off[i];
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pdl_trigger();
+  const uint32_t tmem = sm.tmem_slot;
+  int per_tile = 0;
+  for (int p = 0; p < d.nproj; ++p) per_tile += t.tc_ncol[p];
+  const int64_t G = (int64_t)tiles * per_tile;
+  constexpr bool bf16 = std::is_same<E, __nv_bfloat16>::value;
+  bool ok = true;
+
+  // unit g -> (tile, projection, column tile)
+  auto decode = [&](int64_t g, TcUnit& u, int& c, int& o, int& ncols) {
+    const int tile = (int)(g / per_tile);
+    int nt = (int)(g - (int64_t)tile * per_tile), p = 0;
+    while (nt >= t.tc_ncol[p]) nt -= t.tc_ncol[p++];
+    u = tc_tile(t, sm.off, off_smem, S, tile, p);
+    tc_col_tile(nt, d.proj[p].h_out, d.H, c, o, ncols);
+  };
+
+  if (warp == 0) {  // ------------------------------------------ producer
+    uint32_t stage = 0, phase = 0;
+    for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x) {
+      TcUnit u;
+      int c, o, ncols;
+      decode(g, u, c, o, ncols);
+      const ProjDev& P = d.proj[u.p];
+      const int r16 = (u.r + 15) & ~15;
+      const int natoms = (ncols + 63) >> 6;
+      const int32_t* ptB = d.page_table + (int64_t)u.a * d.pt_stride + (int64_t)u.r * (P.rows_before + P.ppi) + c;
+      for (int k0 = 0; k0 < r16 && ok; k0 += kTcK) {
+        const int nk = min(kTcK, r16 - k0);  // multiple of 16
+        int pg[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int row = k0 + 4 * lane + i;
+          pg[i] = __ldg(ptB + (int64_t)(row < u.r ? row : 0) * P.ppo);
+        }
+        bool got = true;
+        if (lane == 0) got = mbar_wait(&sm.empty[stage], phase ^ 1);
+        if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          mbar_expect_tx(&sm.full[stage], 2u * kTcM * kRowBytes + (uint32_t)(natoms * nk) * kRowBytes);
+          tma_load_2d(sm.Ahi[stage], &t.vhi_map[u.p], k0, u.j0, &sm.full[stage]);
+          tma_load_2d(sm.Alo[stage], &t.vlo_map[u.p], k0, u.j0, &sm.full[stage]);
+        }
+        __syncwarp();
+        if (4 * lane < nk)
+          for (int nb = 0; nb < natoms; ++nb)
+            tma_gather4(&sm.B[stage][(nb * kTcK + 4 * lane) * kRowBytes], &t.pool_map, o + 64 * nb, pg[0], pg[1],
+                        pg[2], pg[3], &sm.full[stage]);
+        if (++stage == kExpandTcStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+  } else if (warp == 1) {  // ----------------------------------- MMA issuer
+    uint32_t stage = 0, phase = 0;
+    int n = 0;
+    for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x, ++n) {
+      int r = 0, ncols = 0;
+      if (lane == 0) {
+        TcUnit u;
+        int c, o;
+        decode(g, u, c, o, ncols);
+        r = u.r;
+      }
+      r = __shfl_sync(0xffffffffu, r, 0);
+      ncols = __shfl_sync(0xffffffffu, ncols, 0);
+      const int r16 = (r + 15) & ~15;
+      const int ab = n & 1;
+      bool got = true;
+      if (lane == 0) got = mbar_wait(&sm.tempty[ab], ((n >> 1) & 1) ^ 1);
+      if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t idesc = umma_idesc_f16(kTcM, (ncols + 15) & ~15, bf16, true);
+      const uint32_t dtm = tmem + (uint32_t)(ab * kTcN);
+      for (int k0 = 0; k0 < r16; k0 += kTcK) {
+        const int nk = min(kTcK, r16 - k0);
+        if (lane == 0) got = mbar_wait(&sm.full[stage], phase);
+        if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t ha = smem_addr(sm.Ahi[stage]), la = smem_addr(sm.Alo[stage]), ba = smem_addr(sm.B[stage]);
+          for (int ks = 0; ks < nk / 16; ++ks) {
+            // B is N-major: 64-column atoms kTcK rows apart, 8-row groups 1 KB apart
+            const uint64_t bdesc = umma_desc_sw128(ba + ks * 16 * kRowBytes, kTcK * kRowBytes, 1024);
+            umma_f16(dtm, umma_desc_sw128(ha + ks * 32, 16, 1024), bdesc, idesc, (k0 | ks) ? 1u : 0u);
+            umma_f16(dtm, umma_desc_sw128(la + ks * 32, 16, 1024), bdesc, idesc, 1u);
+          }
+          umma_commit(&sm.empty[stage]);
+        }
+        __syncwarp();
+        if (++stage == kExpandTcStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) umma_commit(&sm.tfull[ab]);
+      __syncwarp();
+    }
+  } else {  // ------------------------------------------------- epilogue (warps 2-5)
+    const int quarter = warp & 3;
+    const int m = 32 * quarter + lane;
+    int n = 0;
+    for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x, ++n) {
+      TcUnit u;
+      int c, o, ncols;
+      decode(g, u, c, o, ncols);
+      const ProjDev& P = d.proj[u.p];
+      const int ab = n & 1;
+      const int token = m < u.len ? __ldg(d.perm + u.j0 + m) : 0;
+      bool got = true;
+      if (lane == 0) got = mbar_wait(&sm.tfull[ab], (n >> 1) & 1);
+      if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint16_t* yrow = static_cast<uint16_t*>(P.y) + (int64_t)token * P.ldy + c * d.H + o;
+      for (int c0 = 0; c0 < ncols; c0 += 16) {
+        float acc[16];
+        tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(ab * kTcN + c0), acc);
+        if (m < u.len) {
+          const int nv = min(2, (ncols - c0) >> 3);  // 16-byte vectors in this chunk (ncols % 8 == 0)
+          for (int h = 0; h < nv; ++h) {
+            uint4 yv = *reinterpret_cast<const uint4*>(yrow + c0 + 8 * h);
+            uint16_t e[8];
+            memcpy(e, &yv, 16);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) e[i] = Elem<E>::from(Elem<E>::to(e[i]) + d.s * acc[8 * h + i]);
+            memcpy(&yv, e, 16);
+            *reinterpret_cast<uint4*>(yrow + c0 + 8 * h) = yv;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.tempty[ab]);
+    }
+  }
+  if (!ok && lane == 0) report_err(d.error, kErrTimeout);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 2 * kTcN);
+  }
+}
+
+template <typename Kern>
+cudaError_t launch_pdl_tc(Kern kernel, int grid, size_t smem, cudaStream_t st, const TcDev& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+constexpr size_t kShrinkTcSmem = sizeof(TcShrinkSmem) + 1024;
+constexpr size_t kExpandTcSmem = sizeof(TcExpandSmem) + 1024;
+
+}  // namespace
+
+cudaError_t prepare_tc_kernels() {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(tc_shrink_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kShrinkTcSmem)))
+    return e;
+  if ((e = cudaFuncSetAttribute(tc_shrink_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kShrinkTcSmem)))
+    return e;
+  if ((e = cudaFuncSetAttribute(tc_expand_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kExpandTcSmem)))
+    return e;
+  return cudaFuncSetAttribute(tc_expand_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)kExpandTcSmem);
+}
+
+cudaError_t launch_tc_shrink(const TcDev& a, int dtype, int grid, cudaStream_t st) {
+  if (dtype == 0) return launch_pdl_tc(tc_shrink_kernel<__half>, grid, kShrinkTcSmem, st, a);
+  return launch_pdl_tc(tc_shrink_kernel<__nv_bfloat16>, grid, kShrinkTcSmem, st, a);
+}
+
+cudaError_t launch_tc_expand(const TcDev& a, int dtype, int grid, cudaStream_t st) {
+  if (dtype == 0) return launch_pdl_tc(tc_expand_kernel<__half>, grid, kExpandTcSmem, st, a);
+  return launch_pdl_tc(tc_expand_kernel<__nv_bfloat16>, grid, kExpandTcSmem, st, a);
+}
+
+int32_t tc_col_tiles(int32_t h_out, int32_t H) {
+  int32_t n = 0;
+  for (int32_t c = 0; c * H < h_out; ++c) {
+    const int32_t len = (h_out - c * H) < H ? (h_out - c * H) : H;
+    n += (len + kTcN - 1) / kTcN;
+  }
+  return n;
+}
+
+}  // namespace slora

@@ -99,6 +99,11 @@ def test_small_cases_all_modes(name):
         seg, want = _run_and_check(case, mode, want)
         _check_segments(case, seg)
     _run_and_check(case, slora.MODE_AUTO, want, multi=False)
+    # every segment on the tensor-core kernels, then a mixed split
+    for thr in (0, 3):
+        slora.slora_set_tc_threshold(case.pool.handle, thr)
+        seg, _ = _run_and_check(case, slora.MODE_PREFILL, want)
+        _check_segments(case, seg)
     case.pool.close()
 
 
@@ -125,7 +130,7 @@ def test_full_size_llama7b_prefill_sampled():
     case = G.build_case(wl, weights="touched")
     rows = _sample_rows(wl, 384)
     want = G.oracle_outputs(case, tokens=rows)
-    for mode in (slora.MODE_AUTO, slora.MODE_PREFILL):
+    for mode in (slora.MODE_DECODE, slora.MODE_AUTO, slora.MODE_PREFILL):
         seg, _ = _run_and_check(case, mode, want, rows=rows)
     _check_segments(case, seg)
     case.pool.close()
