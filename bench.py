@@ -329,15 +329,18 @@ def main():
     hbm_peak, peak_kind = _peaks()
     ab = algorithmic_bytes(wl, None if args.mode == "decode" else TC_THRESHOLD)
     per_kernel = {}
-    for name in ("apply_cc", "apply_tc", "build_segments"):
-        tms, cnt = kern.get(name, (0.0, 0))
+    for name, (tms, cnt) in kern.items():
         if cnt:
-            # a path's launches per step (shrink + expand) share its bytes
-            per_step_us = 1e3 * tms / hook_steps
-            per_kernel[name] = {"avg_us": 1e3 * tms / cnt, "launches": int(cnt), "us_per_step": per_step_us}
-            if name in ab and per_step_us > 0:
-                per_kernel[name]["gbs"] = ab[name] / (per_step_us * 1e-6) / 1e9
-    dom = max(("apply_cc", "apply_tc"), key=lambda k: per_kernel.get(k, {}).get("us_per_step", 0))
+            per_kernel[name] = {"avg_us": 1e3 * tms / cnt, "launches": int(cnt),
+                                "us_per_step": 1e3 * tms / hook_steps}
+    # a path (CUDA-core or tensor-core) = its shrink + expand launches; they
+    # share the path's algorithmic bytes
+    paths = {"apply_cc": ("shrink_cc", "expand_cc", "apply_fused"), "apply_tc": ("shrink_tc", "expand_tc")}
+    path_us = {k: sum(per_kernel.get(n, {}).get("us_per_step", 0.0) for n in v) for k, v in paths.items()}
+    for k in paths:
+        if path_us[k] > 0:
+            per_kernel[k] = {"us_per_step": path_us[k], "gbs": ab[k] / (path_us[k] * 1e-6) / 1e9}
+    dom = max(paths, key=lambda k: path_us[k])
     achieved = per_kernel[dom]["gbs"]
     src_hash = _kernel_source_hash()
     tr = NCU_TRAFFIC.get((dom, sp.name))

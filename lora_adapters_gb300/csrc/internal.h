@@ -62,7 +62,7 @@ struct SegDev {
 
 // Shared memory of the segment kernel (its own static arrays take ~10 KB).
 constexpr int kSegSmemMax = 200 * 1024;
-constexpr int32_t kRankInSmem = 1, kSegInSmem = 2;
+constexpr int32_t kRankInSmem = 1, kSegInSmem = 2, kKeysInSmem = 4;
 
 struct SegBuildArgs {
   const int32_t* token_adapter;  // [T]
@@ -144,6 +144,11 @@ struct TcDev {
   ApplyDev a;                        // projections, segments, v (fp32), error word
   CUtensorMap pool_map;              // pool as [num_pages x H], box {64, 1} (gather4 rows)
   CUtensorMap x_map[kMaxProj];       // x of each projection as [T x h_in], box {64, 1}
+  CUtensorMap x128_map[kMaxProj];    // the same, box {64, 128} (tiles of consecutive tokens)
+  CUtensorMap x16_map[kMaxProj];     // the same, box {64, 16}
+  CUtensorMap y_map[kMaxProj];       // y of each projection as [T x h_out], box {64, 1}
+  CUtensorMap y128_map[kMaxProj];    // box {64, 128}
+  CUtensorMap y16_map[kMaxProj];     // box {64, 16}
   CUtensorMap vhi_map[kMaxProj];     // v halves as [max_tokens x v16_ld], box {64, 128}
   CUtensorMap vlo_map[kMaxProj];
   uint16_t* vhi[kMaxProj];

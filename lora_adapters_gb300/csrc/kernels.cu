@@ -191,9 +191,10 @@ __device__ __forceinline__ int pick(const int (&a)[N], int i) {
 //  (2) one block scan over the histogram (each thread owns a run of adapter
 //      ids) -> one segment per adapter present, in ascending id;
 //  (3) stable scatter of token indices: tokens are visited in order, 1024 at
-//      a time; a token's position is its adapter's running start + the number
-//      of earlier tokens of that adapter in the tile (same warp: match_any +
-//      popc; earlier warps: their per-warp (adapter, count) groups);
+//      a time; each warp groups its tokens by adapter (match_any), one warp
+//      then gives every (warp, adapter) group its first position by walking
+//      the warps in order, and a token's position is its group's first
+//      position + its rank inside the group;
 //  (4) work order: segments by rank, largest first (so that the persistent
 //      apply kernels hand out the longest work units first), then the
 //      per-position work-unit counts and their prefix sums.  Ties between
@@ -209,6 +210,7 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
   extern __shared__ int32_t smem_i[];
   __shared__ int32_t grp_key[32][32];
   __shared__ int32_t grp_cnt[32][32];
+  __shared__ int32_t grp_base[32][32];
   __shared__ int32_t ngrp[32];
   __shared__ int32_t scan_sh[33 * 6];
   __shared__ int32_t rcount[kMaxRank + 1];
@@ -227,6 +229,8 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
   int32_t* s_start = seg_smem ? sbase + cap : sd.seg_start;      // [cap + 1]
   int32_t* s_rank = seg_smem ? sbase + 2 * cap + 1 : sd.seg_rank;
   int32_t* s_order = seg_smem ? sbase + 3 * cap + 1 : sd.seg_order;
+  const bool keys_smem = (args.smem_flags & kKeysInSmem) != 0;
+  int32_t* skeys = sbase + (seg_smem ? 4 * cap + 1 : 0);         // [T] when keys_smem
   // The apply kernels may start their prologue now; they wait for this
   // kernel's results (griddepcontrol.wait) before reading any of them.
   pdl_trigger();
@@ -266,9 +270,41 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
     return key;
   };
   int keys[kCachedTiles];
+  if (keys_smem) {
+    // all keys staged in shared memory with independent loads, validated in
+    // a second independent pass (no per-tile chain of dependent round trips)
+    for (int i = tid; i < T; i += nthr) skeys[i] = args.token_adapter[i];
+    __syncthreads();
+    for (int i = tid; i < T; i += nthr) {
+      const int a = skeys[i];
+      int key = -1;
+      if (a >= 0 && a < A) {
+        const int r = args.rank[a];
+        if (r > 0) {
+          key = a;
+          if (rank_smem) rank_s[a] = r;
+        } else {
+          atomicAdd(&s_bad, 1);
+          atomicCAS(&s_err, 0, -4 /* SLORA_ERR_NOT_RESIDENT */);
+        }
+      } else if (a != -1) {
+        atomicAdd(&s_bad, 1);
+        atomicCAS(&s_err, 0, -1 /* SLORA_ERR_INVALID */);
+      }
+      skeys[i] = key;
+    }
+    __syncthreads();
+    for (int base = 0; base < T; base += nthr) {
+      const int i = base + tid;
+      const int key = i < T ? skeys[i] : -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, key);
+      if (key >= 0 && (peers & ((1u << lane) - 1u)) == 0u) atomicAdd(&hist[key], __popc(peers));
+    }
+  } else {
 #pragma unroll
-  for (int c = 0; c < kCachedTiles; ++c) keys[c] = classify(c * kSegThreads + tid);
-  for (int base = kCachedTiles * kSegThreads; base < T; base += nthr) classify(base + tid);
+    for (int c = 0; c < kCachedTiles; ++c) keys[c] = classify(c * kSegThreads + tid);
+    for (int base = kCachedTiles * kSegThreads; base < T; base += nthr) classify(base + tid);
+  }
   __syncthreads();
 
   // (2) segments in ascending adapter id; hist[a] becomes a's running start
@@ -313,7 +349,9 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
   for (int c = 0, base = 0; base < T; ++c, base += nthr) {
     const int i = base + tid;
     int key = -1;
-    if (c < kCachedTiles) {
+    if (keys_smem) {
+      key = i < T ? skeys[i] : -1;
+    } else if (c < kCachedTiles) {
       key = pick(keys, c);
     } else if (i < T) {
       const int a = args.token_adapter[i];
@@ -324,38 +362,32 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
     const int rank_w = __popc(peers & lt);
     const bool leader = (peers & lt) == 0u;
     const unsigned lead_mask = __ballot_sync(0xffffffffu, valid && leader);
+    // my group's slot in this warp's list: the slot of my group's leader
+    const int slot = __shfl_sync(0xffffffffu, __popc(lead_mask & lt), valid ? __ffs(peers) - 1 : 0);
     if (valid && leader) {
-      const int slot = __popc(lead_mask & lt);
       grp_key[warp][slot] = key;
       grp_cnt[warp][slot] = __popc(peers);
     }
     if (lane == 0) ngrp[warp] = __popc(lead_mask);
     __syncthreads();
-    if (valid) {
-      // same-key tokens of earlier warps in this tile: scan their groups,
-      // eight entries per step so the shared-memory loads overlap
-      int p = hist[key] + rank_w;
-      for (int w = 0; w < warp; ++w) {
+    // One warp hands every (warp, adapter) group its first position, walking
+    // the warps in token order; the groups of one warp have distinct
+    // adapters, so its lanes update distinct running starts.
+    if (warp == 0) {
+      const int nw = nthr >> 5;
+      for (int w = 0; w < nw; ++w) {
         const int ng = ngrp[w];
-        const int* gk = grp_key[w];
-        const int* gc = grp_cnt[w];
-        int g = 0;
-        for (; g + 8 <= ng; g += 8) {
-          int kk[8], cc[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            kk[u] = gk[g + u];
-            cc[u] = gc[g + u];
-          }
-#pragma unroll
-          for (int u = 0; u < 8; ++u) p += kk[u] == key ? cc[u] : 0;
+        if (lane < ng) {
+          const int k = grp_key[w][lane];
+          const int b = hist[k];
+          grp_base[w][lane] = b;
+          hist[k] = b + grp_cnt[w][lane];
         }
-        for (; g < ng; ++g) p += gk[g] == key ? gc[g] : 0;
+        __syncwarp();
       }
-      sd.perm[p] = i;
     }
     __syncthreads();
-    if (valid && leader) atomicAdd(&hist[key], __popc(peers));
+    if (valid) sd.perm[grp_base[warp][slot] + rank_w] = i;
   }
 
   // (4a) histogram of segment ranks
@@ -1060,6 +1092,11 @@ cudaError_t launch_build_segments(const SegBuildArgs& in, cudaStream_t st) {
   if (smem + seg_arrays <= (size_t)kSegSmemMax) {
     smem += seg_arrays;
     a.smem_flags |= kSegInSmem;
+    const size_t keys = sizeof(int32_t) * (size_t)a.T;
+    if (smem + keys <= (size_t)kSegSmemMax) {
+      smem += keys;
+      a.smem_flags |= kKeysInSmem;
+    }
   }
   build_segments_kernel<<<1, kSegThreads, smem, st>>>(a);
   return cudaGetLastError();

@@ -56,8 +56,9 @@ constexpr int32_t kOwnerFree = -1;
 constexpr int32_t kOwnerKV = -2;
 constexpr int32_t kOwnerPending = -3;
 
-enum TimerKind { kTBuild = 0, kTApplyCC, kTApplyTC, kTScatter, kTNum };
-const char* kTimerNames[kTNum] = {"build_segments", "apply_cc", "apply_tc", "scatter"};
+enum TimerKind { kTBuild = 0, kTShrinkCC, kTExpandCC, kTShrinkTC, kTExpandTC, kTApplyFused, kTScatter, kTNum };
+const char* kTimerNames[kTNum] = {"build_segments", "shrink_cc", "expand_cc", "shrink_tc",
+                                  "expand_tc",      "apply_fused", "scatter"};
 
 }  // namespace
 
@@ -732,9 +733,17 @@ int slora_lora_apply_multi(slora_pool* p, const slora_segments* seg, int32_t n, 
     const size_t half_elems = (size_t)kMaxProj * rows * p->v16_ld;
     for (int i = 0; i < n; ++i) {
       const ProjDev& P = d.proj[i];
-      if (int rc = encode_2d(&t.x_map[i], P.x, p->dtype, (uint64_t)P.h_in, (uint64_t)p->seg_T,
-                             (uint64_t)P.ldx * 2, kTcK, 1))
-        return rc;
+      for (int b = 0; b < 3; ++b) {
+        const uint32_t box_rows = b == 0 ? 1 : b == 1 ? kTcM : 16;
+        CUtensorMap* mx = b == 0 ? &t.x_map[i] : b == 1 ? &t.x128_map[i] : &t.x16_map[i];
+        CUtensorMap* my = b == 0 ? &t.y_map[i] : b == 1 ? &t.y128_map[i] : &t.y16_map[i];
+        if (int rc = encode_2d(mx, P.x, p->dtype, (uint64_t)P.h_in, (uint64_t)p->seg_T, (uint64_t)P.ldx * 2, kTcK,
+                               box_rows))
+          return rc;
+        if (int rc = encode_2d(my, P.y, p->dtype, (uint64_t)P.h_out, (uint64_t)p->seg_T, (uint64_t)P.ldy * 2, kTcK,
+                               box_rows))
+          return rc;
+      }
       t.vhi_map[i] = p->vhi_map[i];
       t.vlo_map[i] = p->vlo_map[i];
       t.vhi[i] = p->d_v16 + (size_t)i * rows * p->v16_ld;
@@ -745,38 +754,44 @@ int slora_lora_apply_multi(slora_pool* p, const slora_segments* seg, int32_t n, 
     t.tc_total_idx = kTcTileLong;
     d.phases = kPhaseShrink;
     {
-      Timed tm(p, kTApplyCC, p->compute);
+      Timed tm(p, kTShrinkCC, p->compute);
       CUDA_TRY(launch_apply_cc(d, p->dtype, p->grid_cc, p->compute));
       tm.done();
     }
     {
-      Timed tm(p, kTApplyTC, p->compute);
+      Timed tm(p, kTShrinkTC, p->compute);
       CUDA_TRY(launch_tc_shrink(t, p->dtype, p->grid_cc, p->compute));
       tm.done();
     }
     d.phases = kPhaseExpand;
     {
-      Timed tm(p, kTApplyCC, p->compute);
+      Timed tm(p, kTExpandCC, p->compute);
       CUDA_TRY(launch_apply_cc(d, p->dtype, p->grid_cc, p->compute));
       tm.done();
     }
     {
-      Timed tm(p, kTApplyTC, p->compute);
+      Timed tm(p, kTExpandTC, p->compute);
       CUDA_TRY(launch_tc_expand(t, p->dtype, p->grid_cc, p->compute));
       tm.done();
     }
   } else if (p->fused_apply) {
     d.phases = kPhaseShrink | kPhaseExpand;
-    Timed tm(p, kTApplyCC, p->compute);
+    Timed tm(p, kTApplyFused, p->compute);
     CUDA_TRY(launch_apply_cc(d, p->dtype, p->grid_cc, p->compute));
     tm.done();
   } else {
-    Timed tm(p, kTApplyCC, p->compute);
     d.phases = kPhaseShrink;
-    CUDA_TRY(launch_apply_cc(d, p->dtype, p->grid_cc, p->compute));
+    {
+      Timed tm(p, kTShrinkCC, p->compute);
+      CUDA_TRY(launch_apply_cc(d, p->dtype, p->grid_cc, p->compute));
+      tm.done();
+    }
     d.phases = kPhaseExpand;
-    CUDA_TRY(launch_apply_cc(d, p->dtype, p->grid_cc, p->compute));
-    tm.done();
+    {
+      Timed tm(p, kTExpandCC, p->compute);
+      CUDA_TRY(launch_apply_cc(d, p->dtype, p->grid_cc, p->compute));
+      tm.done();
+    }
   }
   return SLORA_OK;
 }

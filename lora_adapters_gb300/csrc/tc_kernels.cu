@@ -80,21 +80,6 @@ __device__ __forceinline__ TcUnit tc_tile(const TcDev& t, const int32_t* s_off, 
   return u;
 }
 
-// Column tile nt of a row of h_out elements over pages of H: tiles of at most
-// kTcN columns that never cross a page.
-__device__ __forceinline__ void tc_col_tile(int nt, int h_out, int H, int& c, int& o, int& len) {
-  for (c = 0;; ++c) {
-    const int lenc = min(H, h_out - c * H);
-    const int n = (lenc + kTcN - 1) / kTcN;
-    if (nt < n) {
-      o = nt * kTcN;
-      len = min(kTcN, lenc - o);
-      return;
-    }
-    nt -= n;
-  }
-}
-
 template <class T>
 struct Elem;
 template <>
@@ -166,6 +151,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_shrink_kernel(const __grid_c
         const int m = 4 * lane + i;
         tok[i] = __ldg(d.perm + u.j0 + (m < u.len ? m : 0));
       }
+      // Tokens of a segment are in increasing order, so the tile is one run
+      // of consecutive rows of x exactly when its last token is first + len - 1
+      // (prefill requests): then 2-D boxes replace the row gathers.
+      const int t_first = __shfl_sync(0xffffffffu, tok[0], 0);
+      const int t_last = __ldg(d.perm + u.j0 + u.len - 1);
+      const bool run = t_last - t_first == u.len - 1;
+      const int n16 = (u.len + 15) >> 4;  // 16-row boxes of a partial run tile
+      const uint32_t x_bytes = run ? (u.len == kTcM ? (uint32_t)kTcM * kRowBytes : (uint32_t)n16 * 16 * kRowBytes)
+                                   : (uint32_t)(4 * nx4) * kRowBytes;
       const int32_t* pt = d.page_table + (int64_t)u.a * d.pt_stride + (int64_t)u.r * P.rows_before;
       const int nkb = (P.h_in + kTcK - 1) / kTcK;
       int chunk = -1;
@@ -188,11 +182,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_shrink_kernel(const __grid_c
           ok = false;
           break;
         }
-        if (lane == 0) mbar_expect_tx(&sm.full[stage], (uint32_t)(4 * nx4 + 4 * nb4) * kRowBytes);
+        if (lane == 0) mbar_expect_tx(&sm.full[stage], x_bytes + (uint32_t)(4 * nb4) * kRowBytes);
         __syncwarp();
-        if (lane < nx4)
-          tma_gather4(&sm.X[stage][4 * lane * kRowBytes], &t.x_map[u.p], k0, tok[0], tok[1], tok[2], tok[3],
-                      &sm.full[stage]);
+        if (!run) {
+          if (lane < nx4)
+            tma_gather4(&sm.X[stage][4 * lane * kRowBytes], &t.x_map[u.p], k0, tok[0], tok[1], tok[2], tok[3],
+                        &sm.full[stage]);
+        } else if (u.len == kTcM) {
+          if (lane == 0) tma_load_2d(sm.X[stage], &t.x128_map[u.p], k0, t_first, &sm.full[stage]);
+        } else if (lane < n16) {
+          tma_load_2d(&sm.X[stage][16 * lane * kRowBytes], &t.x16_map[u.p], k0, t_first + 16 * lane, &sm.full[stage]);
+        }
 #pragma unroll
         for (int h = 0; h < 2; ++h)
           if (32 * h + lane < nb4)
@@ -310,15 +310,56 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_shrink_kernel(const __grid_c
 }
 
 // ================================================================ tc_expand
-constexpr int kExpandTcStages = 3;
+// Work unit = (segment in work order, projection, column tile of <= kTcNe
+// columns inside one page).  The adapter's B rows for the column tile are
+// gathered once per unit (all rank rows, N-major) and reused by every 128-token
+// tile of the segment; per token tile the producer loads the tile's v halves
+// (2-D boxes, rows consecutive in sorted order) and its y rows (2-D boxes when
+// the tile is a run of consecutive tokens, row gathers otherwise) into
+// double-buffered stages, so the epilogue reads y from shared memory and its
+// global stores are fire-and-forget.
+constexpr int kTcNe = 128;                        // expand column tile
+constexpr int kEAtoms = kTcNe / 64;               // 64-column swizzle atoms per tile
+constexpr int kEKBlocks = kMaxRank / kTcK;        // B row blocks of 64 ranks
 struct TcExpandSmem {
-  uint8_t Ahi[kExpandTcStages][kTcM * kRowBytes];          // 128 x 64 ranks (16 KB)
-  uint8_t Alo[kExpandTcStages][kTcM * kRowBytes];          // 16 KB
-  uint8_t B[kExpandTcStages][(kTcN / 64) * kTcK * kRowBytes];  // 4 column atoms x 64 rank rows (32 KB)
-  uint64_t full[kExpandTcStages], empty[kExpandTcStages], tfull[2], tempty[2];
+  uint8_t B[kEKBlocks][kEAtoms][kTcK * kRowBytes];   // <= 256 rank rows x 128 columns, N-major (64 KB)
+  uint8_t Vhi[2][kTcM * kRowBytes];                  // 128 tokens x 64 ranks (16 KB)
+  uint8_t Vlo[2][kTcM * kRowBytes];
+  uint8_t Y[2][kEAtoms][kTcM * kRowBytes];           // 128 tokens x 128 columns (32 KB)
+  uint64_t b_full, b_empty, v_full[2], v_empty[2], y_full[2], y_empty[2], tfull[2], tempty[2];
   uint32_t tmem_slot;
-  int32_t off[kSegSmem];
 };
+
+// Unit g of the expand list: segment position q (any segment; those with no
+// tensor-core tile do nothing), projection and column tile.
+struct TcEUnit {
+  int p, start, len, r, a, c, o, ncols, ntm;  // ntm = 128-token tiles (0: skip)
+};
+__device__ __forceinline__ TcEUnit tc_eunit(const TcDev& t, int64_t g, int per_seg) {
+  const ApplyDev& d = t.a;
+  TcEUnit u;
+  const int q = (int)(g / per_seg);
+  int nt = (int)(g - (int64_t)q * per_seg);
+  u.p = 0;
+  while (nt >= t.tc_ncol[u.p]) nt -= t.tc_ncol[u.p++];
+  u.ntm = __ldg(t.tc_off + q + 1) - __ldg(t.tc_off + q);
+  const int s = __ldg(d.seg_order + q);
+  u.start = __ldg(d.seg_start + s);
+  u.len = __ldg(d.seg_start + s + 1) - u.start;
+  u.r = __ldg(d.seg_rank + s);
+  u.a = __ldg(d.seg_adapter + s);
+  for (u.c = 0;; ++u.c) {  // column tile within one page chunk
+    const int lenc = min(d.H, d.proj[u.p].h_out - u.c * d.H);
+    const int n = (lenc + kTcNe - 1) / kTcNe;
+    if (nt < n) {
+      u.o = nt * kTcNe;
+      u.ncols = min(kTcNe, lenc - u.o);
+      break;
+    }
+    nt -= n;
+  }
+  return u;
+}
 
 template <class E>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_expand_kernel(const __grid_constant__ TcDev t) {
@@ -326,174 +367,206 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expand_kernel(const __grid_c
   TcExpandSmem& sm = *reinterpret_cast<TcExpandSmem*>(smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023));
   const ApplyDev& d = t.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp == 1) tmem_alloc(&sm.tmem_slot, 2 * kTcN);
+  if (warp == 1) tmem_alloc(&sm.tmem_slot, 2 * kTcNe);
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kExpandTcStages; ++s) {
-      mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], 1);
-    }
+    mbar_init(&sm.b_full, 1);
+    mbar_init(&sm.b_empty, 1);
     for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.v_full[b], 1);
+      mbar_init(&sm.v_empty[b], 1);
+      mbar_init(&sm.y_full[b], 1);
+      mbar_init(&sm.y_empty[b], 4);
       mbar_init(&sm.tfull[b], 1);
       mbar_init(&sm.tempty[b], 4);
     }
     mbar_fence_init();
   }
   pdl_wait();
-  const int tiles = d.counts[t.tc_total_idx];
   const int S = d.counts[kNumSegs];
-  const bool off_smem = S + 1 <= kSegSmem;
-  if (off_smem)
-    for (int i = threadIdx.x; i <= S; i += blockDim.x) sm.off[i] = t.tc_off[i];
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   pdl_trigger();
   const uint32_t tmem = sm.tmem_slot;
-  int per_tile = 0;
-  for (int p = 0; p < d.nproj; ++p) per_tile += t.tc_ncol[p];
-  const int64_t G = (int64_t)tiles * per_tile;
+  int per_seg = 0;
+  for (int p = 0; p < d.nproj; ++p) per_seg += t.tc_ncol[p];
+  const int64_t G = (int64_t)S * per_seg;
   constexpr bool bf16 = std::is_same<E, __nv_bfloat16>::value;
   bool ok = true;
-
-  // unit g -> (tile, projection, column tile)
-  auto decode = [&](int64_t g, TcUnit& u, int& c, int& o, int& ncols) {
-    const int tile = (int)(g / per_tile);
-    int nt = (int)(g - (int64_t)tile * per_tile), p = 0;
-    while (nt >= t.tc_ncol[p]) nt -= t.tc_ncol[p++];
-    u = tc_tile(t, sm.off, off_smem, S, tile, p);
-    tc_col_tile(nt, d.proj[p].h_out, d.H, c, o, ncols);
+  auto wait_lane0 = [&](uint64_t* bar, uint32_t parity) -> bool {
+    bool got = true;
+    if (lane == 0) got = mbar_wait(bar, parity);
+    return __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
   };
 
   if (warp == 0) {  // ------------------------------------------ producer
-    uint32_t stage = 0, phase = 0;
+    uint32_t nb_ = 0, nv = 0, ny = 0;  // B units, v stages, y tiles issued
     for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x) {
-      TcUnit u;
-      int c, o, ncols;
-      decode(g, u, c, o, ncols);
+      const TcEUnit u = tc_eunit(t, g, per_seg);
+      if (u.ntm == 0) continue;
       const ProjDev& P = d.proj[u.p];
       const int r16 = (u.r + 15) & ~15;
-      const int natoms = (ncols + 63) >> 6;
-      const int32_t* ptB = d.page_table + (int64_t)u.a * d.pt_stride + (int64_t)u.r * (P.rows_before + P.ppi) + c;
-      for (int k0 = 0; k0 < r16 && ok; k0 += kTcK) {
-        const int nk = min(kTcK, r16 - k0);  // multiple of 16
+      const int nkb = (r16 + kTcK - 1) / kTcK;
+      const int natoms = (u.ncols + 63) >> 6;
+      const int col0 = u.c * d.H + u.o;
+      // B rows of this column tile, all rank blocks (rows >= r: row 0 again;
+      // the matching v columns are zero)
+      if (!wait_lane0(&sm.b_empty, (nb_ & 1) ^ 1)) { ok = false; break; }
+      ++nb_;
+      if (lane == 0) mbar_expect_tx(&sm.b_full, (uint32_t)(natoms * r16) * kRowBytes);
+      __syncwarp();
+      const int32_t* ptB = d.page_table + (int64_t)u.a * d.pt_stride + (int64_t)u.r * (P.rows_before + P.ppi) + u.c;
+      for (int k4 = lane; 4 * k4 < r16; k4 += 32) {
         int pg[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int row = k0 + 4 * lane + i;
+          const int row = 4 * k4 + i;
           pg[i] = __ldg(ptB + (int64_t)(row < u.r ? row : 0) * P.ppo);
         }
-        bool got = true;
-        if (lane == 0) got = mbar_wait(&sm.empty[stage], phase ^ 1);
-        if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
-          ok = false;
-          break;
+        const int kb = (4 * k4) / kTcK, kr = (4 * k4) % kTcK;
+        for (int nb = 0; nb < natoms; ++nb)
+          tma_gather4(&sm.B[kb][nb][kr * kRowBytes], &t.pool_map, u.o + 64 * nb, pg[0], pg[1], pg[2], pg[3],
+                      &sm.b_full);
+      }
+      for (int mt = 0; mt < u.ntm && ok; ++mt) {
+        const int j0 = u.start + mt * kTcM;
+        const int len = min(kTcM, u.start + u.len - j0);
+        int tok[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int m = 4 * lane + i;
+          tok[i] = __ldg(d.perm + j0 + (m < len ? m : 0));
         }
-        if (lane == 0) {
-          mbar_expect_tx(&sm.full[stage], 2u * kTcM * kRowBytes + (uint32_t)(natoms * nk) * kRowBytes);
-          tma_load_2d(sm.Ahi[stage], &t.vhi_map[u.p], k0, u.j0, &sm.full[stage]);
-          tma_load_2d(sm.Alo[stage], &t.vlo_map[u.p], k0, u.j0, &sm.full[stage]);
-        }
+        const int t_first = __shfl_sync(0xffffffffu, tok[0], 0);
+        const bool run = __ldg(d.perm + j0 + len - 1) - t_first == len - 1;
+        const int n16 = (len + 15) >> 4, nx4 = (len + 3) >> 2;
+        // y tile
+        const int yb = ny & 1;
+        if (!wait_lane0(&sm.y_empty[yb], ((ny >> 1) & 1) ^ 1)) { ok = false; break; }
+        ++ny;
+        const uint32_t ybytes = (uint32_t)natoms * (run ? (len == kTcM ? kTcM : 16 * n16) : 4 * nx4) * kRowBytes;
+        if (lane == 0) mbar_expect_tx(&sm.y_full[yb], ybytes);
         __syncwarp();
-        if (4 * lane < nk)
-          for (int nb = 0; nb < natoms; ++nb)
-            tma_gather4(&sm.B[stage][(nb * kTcK + 4 * lane) * kRowBytes], &t.pool_map, o + 64 * nb, pg[0], pg[1],
-                        pg[2], pg[3], &sm.full[stage]);
-        if (++stage == kExpandTcStages) {
-          stage = 0;
-          phase ^= 1;
+        for (int nb = 0; nb < natoms; ++nb) {
+          if (run && len == kTcM) {
+            if (lane == 0) tma_load_2d(sm.Y[yb][nb], &t.y128_map[u.p], col0 + 64 * nb, t_first, &sm.y_full[yb]);
+          } else if (run) {
+            if (lane < n16)
+              tma_load_2d(&sm.Y[yb][nb][16 * lane * kRowBytes], &t.y16_map[u.p], col0 + 64 * nb, t_first + 16 * lane,
+                          &sm.y_full[yb]);
+          } else if (lane < nx4) {
+            tma_gather4(&sm.Y[yb][nb][4 * lane * kRowBytes], &t.y_map[u.p], col0 + 64 * nb, tok[0], tok[1], tok[2],
+                        tok[3], &sm.y_full[yb]);
+          }
+        }
+        // v halves, one 64-rank block per stage
+        for (int kb = 0; kb < nkb; ++kb) {
+          const int vb = nv & 1;
+          if (!wait_lane0(&sm.v_empty[vb], ((nv >> 1) & 1) ^ 1)) { ok = false; break; }
+          ++nv;
+          if (lane == 0) {
+            mbar_expect_tx(&sm.v_full[vb], 2u * kTcM * kRowBytes);
+            tma_load_2d(sm.Vhi[vb], &t.vhi_map[u.p], kb * kTcK, j0, &sm.v_full[vb]);
+            tma_load_2d(sm.Vlo[vb], &t.vlo_map[u.p], kb * kTcK, j0, &sm.v_full[vb]);
+          }
+          __syncwarp();
         }
       }
     }
   } else if (warp == 1) {  // ----------------------------------- MMA issuer
-    uint32_t stage = 0, phase = 0;
-    int n = 0;
-    for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x, ++n) {
-      int r = 0, ncols = 0;
-      if (lane == 0) {
-        TcUnit u;
-        int c, o;
-        decode(g, u, c, o, ncols);
-        r = u.r;
-      }
-      r = __shfl_sync(0xffffffffu, r, 0);
-      ncols = __shfl_sync(0xffffffffu, ncols, 0);
+    uint32_t nb_ = 0, nv = 0, nt = 0;
+    for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x) {
+      TcEUnit u;
+      if (lane == 0) u = tc_eunit(t, g, per_seg);
+      const int ntm = __shfl_sync(0xffffffffu, lane == 0 ? u.ntm : 0, 0);
+      if (ntm == 0) continue;
+      const int r = __shfl_sync(0xffffffffu, lane == 0 ? u.r : 0, 0);
+      const int ncols = __shfl_sync(0xffffffffu, lane == 0 ? u.ncols : 0, 0);
       const int r16 = (r + 15) & ~15;
-      const int ab = n & 1;
-      bool got = true;
-      if (lane == 0) got = mbar_wait(&sm.tempty[ab], ((n >> 1) & 1) ^ 1);
-      if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
+      const int nkb = (r16 + kTcK - 1) / kTcK;
       const uint32_t idesc = umma_idesc_f16(kTcM, (ncols + 15) & ~15, bf16, true);
-      const uint32_t dtm = tmem + (uint32_t)(ab * kTcN);
-      for (int k0 = 0; k0 < r16; k0 += kTcK) {
-        const int nk = min(kTcK, r16 - k0);
-        if (lane == 0) got = mbar_wait(&sm.full[stage], phase);
-        if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
-          ok = false;
-          break;
-        }
+      if (!wait_lane0(&sm.b_full, nb_ & 1)) { ok = false; break; }
+      ++nb_;
+      tc_fence_after();
+      for (int mt = 0; mt < ntm && ok; ++mt) {
+        const int ab = nt & 1;
+        if (!wait_lane0(&sm.tempty[ab], ((nt >> 1) & 1) ^ 1)) { ok = false; break; }
+        ++nt;
         tc_fence_after();
-        if (lane == 0) {
-          const uint32_t ha = smem_addr(sm.Ahi[stage]), la = smem_addr(sm.Alo[stage]), ba = smem_addr(sm.B[stage]);
-          for (int ks = 0; ks < nk / 16; ++ks) {
-            // B is N-major: 64-column atoms kTcK rows apart, 8-row groups 1 KB apart
-            const uint64_t bdesc = umma_desc_sw128(ba + ks * 16 * kRowBytes, kTcK * kRowBytes, 1024);
-            umma_f16(dtm, umma_desc_sw128(ha + ks * 32, 16, 1024), bdesc, idesc, (k0 | ks) ? 1u : 0u);
-            umma_f16(dtm, umma_desc_sw128(la + ks * 32, 16, 1024), bdesc, idesc, 1u);
+        const uint32_t dtm = tmem + (uint32_t)(ab * kTcNe);
+        for (int kb = 0; kb < nkb; ++kb) {
+          const int vb = nv & 1;
+          if (!wait_lane0(&sm.v_full[vb], (nv >> 1) & 1)) { ok = false; break; }
+          ++nv;
+          tc_fence_after();
+          if (lane == 0) {
+            const int nk = min(kTcK, r16 - kb * kTcK);
+            const uint32_t ha = smem_addr(sm.Vhi[vb]), la = smem_addr(sm.Vlo[vb]);
+            const uint32_t ba = smem_addr(sm.B[kb][0]);
+            for (int ks = 0; ks < nk / 16; ++ks) {
+              // B is N-major: 64-column atoms kTcK rows apart, 8-row groups 1 KB apart
+              const uint64_t bdesc = umma_desc_sw128(ba + ks * 16 * kRowBytes, kTcK * kRowBytes, 1024);
+              umma_f16(dtm, umma_desc_sw128(ha + ks * 32, 16, 1024), bdesc, idesc, (kb | ks) ? 1u : 0u);
+              umma_f16(dtm, umma_desc_sw128(la + ks * 32, 16, 1024), bdesc, idesc, 1u);
+            }
+            umma_commit(&sm.v_empty[vb]);
           }
-          umma_commit(&sm.empty[stage]);
+          __syncwarp();
         }
+        if (!ok) break;
+        if (lane == 0) umma_commit(&sm.tfull[ab]);
         __syncwarp();
-        if (++stage == kExpandTcStages) {
-          stage = 0;
-          phase ^= 1;
-        }
       }
       if (!ok) break;
-      if (lane == 0) umma_commit(&sm.tfull[ab]);
+      if (lane == 0) umma_commit(&sm.b_empty);  // B free once this unit's MMAs are done
       __syncwarp();
     }
   } else {  // ------------------------------------------------- epilogue (warps 2-5)
     const int quarter = warp & 3;
     const int m = 32 * quarter + lane;
-    int n = 0;
-    for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x, ++n) {
-      TcUnit u;
-      int c, o, ncols;
-      decode(g, u, c, o, ncols);
+    uint32_t nt = 0;
+    for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x) {
+      const TcEUnit u = tc_eunit(t, g, per_seg);
+      if (u.ntm == 0) continue;
       const ProjDev& P = d.proj[u.p];
-      const int ab = n & 1;
-      const int token = m < u.len ? __ldg(d.perm + u.j0 + m) : 0;
-      bool got = true;
-      if (lane == 0) got = mbar_wait(&sm.tfull[ab], (n >> 1) & 1);
-      if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint16_t* yrow = static_cast<uint16_t*>(P.y) + (int64_t)token * P.ldy + c * d.H + o;
-      for (int c0 = 0; c0 < ncols; c0 += 16) {
-        float acc[16];
-        tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(ab * kTcN + c0), acc);
-        if (m < u.len) {
-          const int nv = min(2, (ncols - c0) >> 3);  // 16-byte vectors in this chunk (ncols % 8 == 0)
-          for (int h = 0; h < nv; ++h) {
-            uint4 yv = *reinterpret_cast<const uint4*>(yrow + c0 + 8 * h);
-            uint16_t e[8];
-            memcpy(e, &yv, 16);
+      const int col0 = u.c * d.H + u.o;
+      for (int mt = 0; mt < u.ntm && ok; ++mt) {
+        const int j0 = u.start + mt * kTcM;
+        const int len = min(kTcM, u.start + u.len - j0);
+        const int token = m < len ? __ldg(d.perm + j0 + m) : 0;
+        const int ab = nt & 1;
+        if (!wait_lane0(&sm.tfull[ab], (nt >> 1) & 1) || !wait_lane0(&sm.y_full[ab], (nt >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        ++nt;
+        tc_fence_after();
+        uint16_t* yrow = static_cast<uint16_t*>(P.y) + (int64_t)token * P.ldy + col0;
+        for (int c0 = 0; c0 < u.ncols; c0 += 16) {
+          float acc[16];
+          tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(ab * kTcNe + c0), acc);
+          if (m < len) {
+            const int nv8 = min(2, (u.ncols - c0) >> 3);
+            const uint8_t* ytile = sm.Y[ab][c0 >> 6] + m * kRowBytes;
+            for (int h = 0; h < nv8; ++h) {
+              const int chunk = ((c0 & 63) >> 3) + h;  // 16-byte chunk of the 128-byte row, swizzled
+              uint4 yv = *reinterpret_cast<const uint4*>(ytile + ((chunk ^ (m & 7)) << 4));
+              uint16_t e[8];
+              memcpy(e, &yv, 16);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) e[i] = Elem<E>::from(Elem<E>::to(e[i]) + d.s * acc[8 * h + i]);
-            memcpy(&yv, e, 16);
-            *reinterpret_cast<uint4*>(yrow + c0 + 8 * h) = yv;
+              for (int i = 0; i < 8; ++i) e[i] = Elem<E>::from(Elem<E>::to(e[i]) + d.s * acc[8 * h + i]);
+              memcpy(&yv, e, 16);
+              *reinterpret_cast<uint4*>(yrow + c0 + 8 * h) = yv;
+            }
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&sm.tempty[ab]);
+          mbar_arrive(&sm.y_empty[ab]);
+        }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.tempty[ab]);
     }
   }
   if (!ok && lane == 0) report_err(d.error, kErrTimeout);
@@ -501,7 +574,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expand_kernel(const __grid_c
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 2 * kTcN);
+    tmem_dealloc(tmem, 2 * kTcNe);
   }
 }
 
@@ -554,7 +627,7 @@ int32_t tc_col_tiles(int32_t h_out, int32_t H) {
   int32_t n = 0;
   for (int32_t c = 0; c * H < h_out; ++c) {
     const int32_t len = (h_out - c * H) < H ? (h_out - c * H) : H;
-    n += (len + kTcN - 1) / kTcN;
+    n += (len + kTcNe - 1) / kTcNe;
   }
   return n;
 }
