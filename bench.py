@@ -59,7 +59,7 @@ def _peaks():
 
 # ---------------------------------------------------------------- workload
 def algorithmic_bytes(wl, tc_threshold=None, elt=2):
-    """Algorithmic bytes of one step, split by the path each segment takes.
+    """Algorithmic bytes of one step, split by kernel.
 
     Per projection and segment of T_s tokens on adapter a (rank r_a):
     shrink reads x (T_s * H_in) and A_a once (r_a * H_in); expand reads and
@@ -70,12 +70,14 @@ def algorithmic_bytes(wl, tc_threshold=None, elt=2):
     """
     ta = wl.token_adapter
     ids, counts = np.unique(ta[ta >= 0], return_counts=True)
-    out = {"apply_cc": 0, "apply_tc": 0}
+    out = {"shrink_cc": 0, "expand_cc": 0, "shrink_tc": 0, "expand_tc": 0}
     for a, n in zip(ids, counts):
-        r = int(wl.ranks[a])
-        b = sum((int(n) * p.h_in + r * p.h_in + 2 * int(n) * p.h_out + r * p.h_out) * elt for p in wl.projections)
-        out["apply_tc" if tc_threshold is not None and n >= tc_threshold else "apply_cc"] += b
-    out["step"] = out["apply_cc"] + out["apply_tc"]
+        r, n = int(wl.ranks[a]), int(n)
+        path = "tc" if tc_threshold is not None and n >= tc_threshold else "cc"
+        out["shrink_" + path] += sum((n + r) * p.h_in * elt for p in wl.projections)
+        out["expand_" + path] += sum((2 * n + r) * p.h_out * elt for p in wl.projections)
+    out["apply_fused"] = out["shrink_cc"] + out["expand_cc"]
+    out["step"] = out["shrink_cc"] + out["expand_cc"] + out["shrink_tc"] + out["expand_tc"]
     out["distinct_adapters"] = int(ids.shape[0])
     out["tokens"] = int(counts.sum())
     return out
@@ -204,10 +206,14 @@ def run_reference(args, wl, cfg):
     if rank != 0:
         return
     threads = cpu_threads()
-    sample = args.ref_tokens
     orc = OracleSample(wl)
+    wt, wn = 0.0, 0
     for _ in range(args.warmup):
-        orc.run(max(1, sample // 4), threads)
+        t, n = orc.run(max(1, args.ref_tokens // 4), threads)
+        wt, wn = wt + t, wn + n
+    # tokens per step: at most --ref-tokens, fewer when K steps of that size
+    # would take more than about a minute of CPU time
+    sample = int(max(1, min(args.ref_tokens, 60.0 / max(args.steps * wt / max(wn, 1), 1e-9))))
     total_t, total_n = 0.0, 0
     for k in range(args.steps):
         t, n = orc.run(sample, threads, seed=k)
@@ -333,21 +339,23 @@ def main():
         if cnt:
             per_kernel[name] = {"avg_us": 1e3 * tms / cnt, "launches": int(cnt),
                                 "us_per_step": 1e3 * tms / hook_steps}
-    # a path (CUDA-core or tensor-core) = its shrink + expand launches; they
-    # share the path's algorithmic bytes
-    paths = {"apply_cc": ("shrink_cc", "expand_cc", "apply_fused"), "apply_tc": ("shrink_tc", "expand_tc")}
-    path_us = {k: sum(per_kernel.get(n, {}).get("us_per_step", 0.0) for n in v) for k, v in paths.items()}
-    for k in paths:
-        if path_us[k] > 0:
-            per_kernel[k] = {"us_per_step": path_us[k], "gbs": ab[k] / (path_us[k] * 1e-6) / 1e9}
-    dom = max(paths, key=lambda k: path_us[k])
+            if name in ab:
+                per_launch = ab[name] * hook_steps / cnt
+                per_kernel[name]["bytes_per_launch"] = per_launch
+                per_kernel[name]["gbs"] = per_launch / (per_kernel[name]["avg_us"] * 1e-6) / 1e9
+    # the dominant kernel: the one with the most device time per step among
+    # those that move the path's algorithmic bytes
+    movers = [k for k in per_kernel if "gbs" in per_kernel[k]]
+    dom = max(movers, key=lambda k: per_kernel[k]["us_per_step"])
     achieved = per_kernel[dom]["gbs"]
     src_hash = _kernel_source_hash()
     tr = NCU_TRAFFIC.get((dom, sp.name))
     traffic = tr[0] if tr and tr[1] == src_hash else None
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                 "frac": achieved / hbm_peak, "peak_source": peak_kind, "traffic": traffic,
-                "algorithmic_bytes_per_step": ab[dom],
+                "algorithmic_bytes_per_launch": per_kernel[dom]["bytes_per_launch"],
+                "avg_launch_us": per_kernel[dom]["avg_us"],
+                "step_algorithmic_bytes": ab["step"],
                 "step_achieved_gbs": ab["step"] / (ms_step * 1e-3) / 1e9,
                 "step_frac": ab["step"] / (ms_step * 1e-3) / 1e9 / hbm_peak,
                 "kernels": per_kernel, "source_hash": src_hash}
