@@ -5,9 +5,10 @@ adapter (build_segments), then y += s (x A_a) B_a for the layer's q, k, v, o
 projections (one multi-projection apply).  The workload is the Llama-7B-shaped
 decode batch: H = 4096, 256 tokens (one per request), 1000 adapters of ranks
 {8, 16, 32, 64} resident in a pre-fragmented pool, token -> adapter Zipf(1),
-fp16.  L2 is flushed (a 256 MiB device write) before every timed step, so
-adapter pages, x and y come from HBM; only the steps themselves are timed,
-with CUDA events on the compute stream.
+fp16.  L2 is flushed before every timed step (a 256 MiB device write, then a
+256 MiB device read, so that the write's dirty lines leave L2 before the step
+starts), so adapter pages, x and y come from HBM; only the steps themselves
+are timed, with CUDA events on the compute stream.
 
 Printed: one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
 on a bounded sample of the same workload instead (the reference arm).
@@ -76,7 +77,7 @@ def algorithmic_bytes(wl, tc_threshold=None, elt=2):
         path = "tc" if tc_threshold is not None and n >= tc_threshold else "cc"
         out["shrink_" + path] += sum((n + r) * p.h_in * elt for p in wl.projections)
         out["expand_" + path] += sum((2 * n + r) * p.h_out * elt for p in wl.projections)
-    out["apply_fused"] = out["shrink_cc"] + out["expand_cc"]
+    out["apply_cc"] = out["shrink_cc"] + out["expand_cc"]     # one launch does both phases
     out["step"] = out["shrink_cc"] + out["expand_cc"] + out["shrink_tc"] + out["expand_tc"]
     out["distinct_adapters"] = int(ids.shape[0])
     out["tokens"] = int(counts.sum())
@@ -256,7 +257,7 @@ def main():
            "adapters_resident": sp.num_adapters, "ranks": list(sp.rank_set),
            "popularity": f"{sp.popularity}{'(alpha=%g)' % sp.zipf_alpha if sp.popularity == 'zipf' else ''}",
            "pool_pages": wl.pool_pages, "page_bytes": sp.H * 2, "mode": args.mode,
-           "l2": "flushed before every timed step (256 MiB device write)",
+           "l2": "flushed before every timed step: 256 MiB device write, then 256 MiB device read",
            "parallelism": f"replicas x{args.gpus}"}
     if args.impl == "reference":
         run_reference(args, wl, cfg)
@@ -280,7 +281,14 @@ def main():
     n = len(sp.projections)
     projs = list(range(n))
     stream = pool.compute_stream
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush_r = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.int64, device=device)
+
+    def flush(k):
+        # evict L2: write a buffer larger than L2, then read another one so
+        # that the written lines are back in HBM before the timed step
+        flush_w.fill_(k & 0xff)
+        flush_r.sum()
 
     def step():
         seg = pool.build_segments(ta)
@@ -300,7 +308,7 @@ def main():
     wall0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for k in range(args.steps):
-            flush.fill_(k & 0xff)
+            flush(k)
             starts[k].record(stream)
             step()
             ends[k].record(stream)
@@ -326,7 +334,7 @@ def main():
     hook_steps = min(args.steps, 500)
     with torch.cuda.stream(stream):
         for k in range(hook_steps):
-            flush.fill_(k & 0xff)
+            flush(k)
             step()
     kern = slora.slora_timing_read(pool.handle)
     slora.slora_timing_enable(pool.handle, False)
@@ -385,7 +393,7 @@ def main():
         torch.cuda.synchronize()
         e_ms = 0.0
         for k in range(args.steps):
-            flush.fill_(k & 0xff)
+            flush(k)
             s0 = torch.cuda.Event(enable_timing=True)
             s1 = torch.cuda.Event(enable_timing=True)
             s0.record(stream)

@@ -74,6 +74,7 @@ struct SegBuildArgs {
   int32_t tc_threshold;
   SegDev seg;
   int32_t* error;                // first device error (0 = none)
+  int32_t* grid_sync;            // the apply kernel's grid barrier: arrival count reset here
 };
 
 // One projection of an apply call.
@@ -109,24 +110,11 @@ struct ApplyDev {
   int32_t v_ld;                  // multiple of 4 (v rows are bulk-copied)
   float s;
   int32_t* error;                // first device error (0 = none)
-  // Per (projection, token tile) counters of the fused apply kernel: ready =
-  // rank rows of v published, passed = expand units past their wait.  Zero
-  // between calls (each call leaves them zero again).
-  int32_t* ready;                // [kMaxProj][max_tiles]
-  int32_t* passed;               // [kMaxProj][max_tiles]
-  int32_t max_tiles;
-  // Which units this launch runs: kPhaseShrink | kPhaseExpand in one launch
-  // (expand units wait on the tile counters), or one phase per launch (the
-  // kernel boundary orders them; no counters are touched).
-  int32_t phases;
+  // Grid barrier between the shrink and expand phases of one launch:
+  // [0] = CTAs arrived (back to 0 when the last arrives), [1] = generation
+  // (incremented when the barrier opens).  Zero-initialised with the pool.
+  int32_t* grid_sync;
 };
-constexpr int32_t kPhaseShrink = 1, kPhaseExpand = 2;
-
-// Token tiles of a batch of at most max_tokens tokens in at most max_segs
-// segments (each segment's last tile may be partial).
-inline int32_t max_token_tiles(int32_t max_tokens, int32_t max_segs) {
-  return (max_tokens + kTT - 1) / kTT + max_segs;
-}
 
 // Column tiles of a row of h_out elements over pages of H: tiles of at most
 // kExpandCols columns that never cross a page boundary.
@@ -176,7 +164,8 @@ struct ScatterDev {
 
 // Launchers (kernels.cu).  dtype: 0 = fp16, 1 = bf16.
 cudaError_t launch_build_segments(const SegBuildArgs& a, cudaStream_t st);
-// The fused CUDA-core apply (shrink units, then expand units); grid = SMs.
+// The CUDA-core apply (shrink units, grid barrier, expand units); grid = SMs,
+// every CTA resident at once.
 cudaError_t launch_apply_cc(const ApplyDev& a, int dtype, int grid, cudaStream_t st);
 cudaError_t launch_scatter(const ScatterDev& a, cudaStream_t st);
 cudaError_t prepare_kernels(int device);   // opt-in shared memory sizes

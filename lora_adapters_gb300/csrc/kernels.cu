@@ -1,8 +1,9 @@
 // CUDA-core kernels of the heterogeneous-batch LoRA path (sm_103a):
 //   build_segments  -- stable grouping of the batch's tokens by adapter, and
-//                      the work lists of the apply kernels
-//   shrink_cc       -- v[j, k] = x[perm[j], :] . A_a[:, k]
-//   expand_cc       -- y[perm[j], n] += s * sum_k v[j, k] B_a[k, n]
+//                      the work lists of the apply kernel
+//   apply_cc        -- one launch: shrink v[j, k] = x[perm[j], :] . A_a[:, k],
+//                      a grid barrier, then expand
+//                      y[perm[j], n] += s * sum_k v[j, k] B_a[k, n]
 //   scatter         -- adapter load: staged rows -> their pool pages
 //
 // The method ("S-LoRA: Serving Thousands of Concurrent LoRA Adapters";
@@ -118,10 +119,6 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 __device__ __forceinline__ void mbar_fence_init() {
   asm volatile("fence.mbarrier_init.release.cluster;\n\tfence.proxy.async.shared::cta;" ::: "memory");
 }
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
-               : "memory");
-}
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
@@ -140,16 +137,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   for (uint32_t i = 0; i < kWaitLimit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
-}
-// 1-D bulk copy global -> shared through the TMA engine; completion is
-// counted in bytes on the mbarrier.  Both addresses 16-byte aligned, bytes a
-// multiple of 16.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
 }
 // Programmatic dependent launch: wait for the preceding kernel's results /
 // let the next kernel's CTAs start their prologue.
@@ -240,6 +227,10 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
   if (tid == 0) {
     s_bad = 0;
     s_err = 0;
+    // No apply kernel runs now (this kernel is not launched early), so the
+    // apply kernel's grid-barrier count can be reset: a call that gave up
+    // part-way cannot leave later calls a stale count.
+    if (args.grid_sync) args.grid_sync[0] = 0;
   }
   __syncthreads();
 
@@ -486,36 +477,38 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
   }
 }
 
-// ---- the fused apply kernel: shrink then expand (CUDA cores, bulk-copy pipeline) ----
-// Persistent CTA per SM (grid = number of SMs): warp 8 is the producer, warps
-// 0-7 consume.  Every CTA first runs its shrink units, then its expand units;
-// both kinds stream through the same 4-deep ring of 48 KB stages.
+// ---- the CUDA-core apply kernel: shrink, grid barrier, expand (one launch) --------
+// Persistent CTA per SM (grid = number of SMs, all CTAs resident at once):
+// warp 8 is the producer, warps 0-7 consume.  Every CTA first runs its shrink
+// units, then its expand units; both kinds stream through the same 4-deep ring
+// of 48 KB shared-memory stages.  The producer fills a stage with 1-D bulk
+// copies (TMA engine) of whole row chunks, one per lane, and lane 0 announces
+// the stage's bytes on its mbarrier after writing the stage's metadata.
 //
 // Shrink unit = (segment position q, token tile of <= kTT tokens, chunk of 8
 // rank rows, projection); projection varies fastest.  Per K chunk of <=
-// kShrinkK elements (never crossing a page) producer lane i bulk-copies A row
-// k0+i straight from its pool page and lanes 8..11 the tile's x rows; consumer
-// warp w dots A row w against the x rows, keeping per-lane partial sums across
-// the unit's chunks, reduces them with shuffles and writes v; lane 0 then
-// publishes the row (release add on the tile's ready counter).
+// kShrinkK elements (never crossing a page) a stage holds the 8 A rows, read
+// straight from their pool pages, and the tile's x rows; consumer warp w dots
+// A row w against the x rows, keeps per-lane partial sums across the unit's
+// chunks, reduces them with shuffles and writes v (fp32).
+//
+// Between the phases the CTAs meet once (a grid barrier on two counters in
+// global memory): the expand phase reads v rows that any CTA may have written.
+// The producer does not wait for it before streaming the expand phase's B and
+// y rows; only the v rows of an expand unit are held back until the barrier
+// has opened, and they land on a separate mbarrier per v buffer.
 //
 // Expand unit = (segment position q, token tile, projection, column tile of
 // <= kExpandCols columns inside one page); projection and column tile vary
-// fastest.  Before its first stage the producer waits (acquire, bounded) until
-// the tile's ready counter shows all r rows of v, then bulk-copies the tile's
-// v rows into an item ring; stages carry kExpandRK B rows each, and the last
-// stage also carries the tile's y rows.  Each consumer thread owns 8 adjacent
-// columns: fp32 accumulation over the unit's rank rows for every token of the
-// tile, then y + s * acc, one rounding, a 16-byte store.  The last of a tile's
-// expand units to pass the wait resets the tile's counters for the next call.
+// fastest.  Stages carry kExpandRK B rows each, and the unit's last stage also
+// carries the tile's y rows.  Each consumer thread owns 8 adjacent columns:
+// fp32 accumulation over the unit's rank rows for every token of the tile,
+// then y + s * acc, one rounding, a 16-byte store.
 //
 // The producer resolves units 32 at a time (one per lane), so page-table and
 // segment lookups of a whole batch of units cost one round of loads, and it
 // fetches the next expand unit's page indices while it streams the current one.
-#ifndef SLORA_STAGES
-#define SLORA_STAGES 4
-#endif
-constexpr int kStages = SLORA_STAGES;                  // ring depth (also the v item-ring depth)
+constexpr int kStages = 4;                             // ring depth (also the v item-ring depth)
 constexpr int kShrinkK = 2048;                         // K chunk (elements) of a shrink stage
 constexpr int kExpandRK = 8;                           // B rows per expand stage
 constexpr int kStageElems = kShrinkRows * kShrinkK + kTT * kShrinkK;   // 48 KB of 16-bit elements
@@ -528,16 +521,21 @@ static_assert(32 % kExpandRK == 0, "a stage's B rows come from one 32-row block 
 enum : int { kKindShrink = 0, kKindExpand = 1 };
 struct __align__(16) StageMeta {
   int kind, ntok, p, len, last;
-  int j0, k0, nrows, tile;          // shrink
-  int col0, nk, buf;                // expand (k0 = first B row of the stage)
+  int j0, k0, nrows;                // shrink
+  int col0, nk, buf, vph;           // expand (k0 = first B row of the stage)
   int rows[kTT];
+};
+struct VPending {                   // an expand unit whose v rows wait for the grid barrier
+  int buf, vph, p, j0, ntok, r;
 };
 struct ApplySmem {
   uint16_t st[kStages][kStageElems];
   float V[kStages][kTT][kMaxRank];
   StageMeta meta[kStages];
-  uint64_t full[kStages], empty[kStages];
+  VPending pend[kStages];
+  uint64_t full[kStages], empty[kStages], vfull[kStages];
   int32_t off_s[kSegSmem], off_e[kSegSmem];
+  int32_t gen0;
 };
 
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
@@ -561,6 +559,29 @@ __device__ __forceinline__ int ld_acquire(const int32_t* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+
+// 1-D bulk copy global -> shared through the TMA engine; completion is
+// counted in bytes on the mbarrier.  Both addresses 16-byte aligned, bytes a
+// multiple of 16.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+// v rows (fp32, `n` floats, a multiple of 4) of one expand unit onto the unit's
+// v-buffer barrier: lane 0 announces the bytes, lanes 0..ntok-1 copy a row each.
+__device__ __forceinline__ void load_vrows(float (*dst)[kMaxRank], const float* src, int64_t ld, int ntok, int n,
+                                           uint64_t* bar, int lane) {
+  if (lane == 0) mbar_expect_tx(bar, (uint32_t)ntok * (uint32_t)n * 4u);
+  __syncwarp();
+  if (lane < ntok) bulk_load(&dst[lane][0], src + (int64_t)lane * ld, (uint32_t)n * 4u, bar);
 }
 
 // Column tile ct of a row of h_out elements stored in pages of H: tiles never
@@ -589,13 +610,6 @@ __device__ __forceinline__ void load_b_pages(const ApplyDev& d, int a, int r, in
     const int row = lane + 32 * m;
     pg[m] = row < r ? __ldg(ptB + (int64_t)row * P.ppo) : 0;
   }
-}
-
-// Producer: acquire the next stage slot (lane 0 waits, the warp learns the outcome).
-__device__ __forceinline__ bool acquire_slot(ApplySmem& sm, uint32_t stage, uint32_t phase, int lane) {
-  bool got = true;
-  if (lane == 0) got = mbar_wait(&sm.empty[stage], phase ^ 1);
-  return __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
 }
 
 // Stage compute of the consumer warps, specialised on the tile's token count
@@ -655,10 +669,14 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], kCcConsumerWarps);
+      mbar_init(&sm.vfull[s], 1);
     }
     mbar_fence_init();
   }
-  pdl_wait();  // the work lists come from the segment kernel
+  pdl_wait();  // the work lists come from the segment kernel; an earlier apply has finished
+  // The barrier generation before this launch's CTAs arrive: it changes only
+  // once every CTA of this launch has arrived, and this CTA has not.
+  if (threadIdx.x == 0) sm.gen0 = ld_acquire(d.grid_sync + 1);
   const int units_s = d.counts[d.shrink_total_idx];
   const int tiles = d.counts[d.tile_total_idx];
   const int S = d.counts[kNumSegs];
@@ -672,18 +690,59 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
   pdl_trigger();
   int per_tile = 0;  // expand units of one token tile: (projection, column tile)
   for (int p = 0; p < d.nproj; ++p) per_tile += d.proj[p].ncol_tiles;
-  const int64_t Gs = (d.phases & kPhaseShrink) ? (int64_t)units_s * d.nproj : 0;
-  const int64_t Ge = (d.phases & kPhaseExpand) ? (int64_t)tiles * per_tile : 0;
-  const bool fused = d.phases == (kPhaseShrink | kPhaseExpand);  // expand waits on tile counters
+  const int64_t Gs = (int64_t)units_s * d.nproj;
+  const int64_t Ge = (int64_t)tiles * per_tile;
   const int64_t stride = gridDim.x;
 
   if (warp == kCcConsumerWarps) {  // ============================ producer warp
     uint32_t stage = 0, phase = 0, nitem = 0;
     bool ok = true;
+    bool opened = false;  // the grid barrier has opened (v rows may be read)
+    int npend = 0;        // expand units whose v rows wait for it
+    // slots (bit s) with copies issued, and the parity of that phase: what a
+    // CTA that gives up must wait for before it exits
+    uint32_t issued = 0, ipar = 0, vissued = 0, vpar = 0;
+    auto mark = [](uint32_t& set, uint32_t& par, int s2, uint32_t ph) {
+      set |= 1u << s2;
+      par = (par & ~(1u << s2)) | (ph << s2);
+    };
+    const int gen0 = sm.gen0;
+    // v rows of the units held back, once the barrier has opened
+    auto release_pending = [&]() {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      for (int i = 0; i < npend; ++i) {
+        const VPending e = sm.pend[i];
+        load_vrows(sm.V[e.buf], d.proj[e.p].v + (int64_t)e.j0 * d.v_ld, d.v_ld, e.ntok, (e.r + 3) & ~3,
+                   &sm.vfull[e.buf], lane);
+        mark(vissued, vpar, e.buf, (uint32_t)e.vph);
+      }
+      npend = 0;
+    };
+    // Has the grid barrier opened?  Every lane reads the generation with
+    // acquire semantics, so that each lane's later copies of v rows are
+    // ordered after the other CTAs' writes of them.
+    auto barrier_open = [&]() -> bool {
+      return __all_sync(0xffffffffu, ld_acquire(d.grid_sync + 1) != gen0);
+    };
+    // Next stage slot; while expand units wait for v rows, the wait for a
+    // free slot also watches the grid barrier (the consumers cannot free a
+    // slot before those v rows arrive).
+    auto acquire = [&]() -> bool {
+      for (uint32_t it = 0; it < kWaitLimit; ++it) {
+        int got = 0;
+        if (lane == 0) got = mbar_try_wait(&sm.empty[stage], phase ^ 1) ? 1 : 0;
+        if (__shfl_sync(0xffffffffu, got, 0)) return true;
+        if (npend > 0 && barrier_open()) {
+          opened = true;
+          release_pending();
+        }
+      }
+      return false;
+    };
     // ---- shrink units
     for (int64_t gb = blockIdx.x; gb < Gs && ok; gb += 32 * stride) {
       const int64_t gl = gb + (int64_t)lane * stride;   // lane l resolves unit gb + l * stride
-      int m_p = 0, m_j0 = 0, m_ntok = 0, m_k0 = 0, m_nrows = 0, m_r = 0, m_a = 0, m_tile = 0;
+      int m_p = 0, m_j0 = 0, m_ntok = 0, m_k0 = 0, m_nrows = 0, m_r = 0, m_a = 0;
       int pg[kShrinkRows], xt[kTT];
 #pragma unroll
       for (int i = 0; i < kShrinkRows; ++i) pg[i] = 0;
@@ -699,7 +758,6 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
         m_a = __ldg(d.seg_adapter + s);
         const int nrc = (m_r + kShrinkRows - 1) / kShrinkRows;
         const int tt = local / nrc, rc = local - tt * nrc;
-        m_tile = (off_smem ? sm.off_e[q] : __ldg(d.tile_off + q)) + tt;
         m_j0 = __ldg(d.seg_start + s) + tt * kTT;
         m_ntok = min(kTT, __ldg(d.seg_start + s + 1) - m_j0);
         m_k0 = rc * kShrinkRows;
@@ -723,33 +781,31 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
         const int nrows = __shfl_sync(0xffffffffu, m_nrows, l);
         const int r = __shfl_sync(0xffffffffu, m_r, l);
         const int a = __shfl_sync(0xffffffffu, m_a, l);
-        const int tile = __shfl_sync(0xffffffffu, m_tile, l);
-        int my_page = 0, my_tok = 0;
+        // lane i < nrows holds A row k0 + i's page, lane 8 + t token t of the tile
+        int my = 0;
 #pragma unroll
         for (int i = 0; i < kShrinkRows; ++i) {
           const int v = __shfl_sync(0xffffffffu, pg[i], l);
-          if (lane == i) my_page = v;
+          if (lane == i) my = v;
         }
 #pragma unroll
         for (int t = 0; t < kTT; ++t) {
           const int v = __shfl_sync(0xffffffffu, xt[t], l);
-          if (lane == kShrinkRows + t) my_tok = v;
+          if (lane == kShrinkRows + t) my = v;
         }
         const ProjDev& P = d.proj[p];
         const bool has_row = lane < nrows;
-        const bool has_x = lane >= kShrinkRows && lane < kShrinkRows + ntok;
         const int32_t* pt_row = d.page_table + (int64_t)a * d.pt_stride + (int64_t)r * P.rows_before +
                                 (int64_t)(k0 + lane) * P.ppi;
-        const uint16_t* xrow = static_cast<const uint16_t*>(P.x) + (int64_t)my_tok * P.ldx;
-        int64_t page = my_page;
+        const uint16_t* xbase = static_cast<const uint16_t*>(P.x);
         for (int c = 0; c < P.ppi && ok; ++c) {
           const int lenc = min(d.H, P.h_in - c * d.H);
-          // the next page of this row, fetched while this one streams
-          const int64_t next_page = (has_row && c + 1 < P.ppi) ? (int64_t)__ldg(pt_row + c + 1) : 0;
+          // the next page of this lane's row, fetched while this one streams
+          const int next = (has_row && c + 1 < P.ppi) ? __ldg(pt_row + c + 1) : 0;
           for (int o = 0; o < lenc; o += kShrinkK) {
             const int len = min(kShrinkK, lenc - o);
             const int last = (c == P.ppi - 1) && (o + len >= lenc);
-            if (!acquire_slot(sm, stage, phase, lane)) {
+            if (!acquire()) {
               ok = false;
               break;
             }
@@ -763,38 +819,38 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
               m.j0 = j0;
               m.k0 = k0;
               m.nrows = nrows;
-              m.tile = tile;
               mbar_expect_tx(&sm.full[stage], (uint32_t)(nrows + ntok) * (uint32_t)len * 2u);
             }
             __syncwarp();
-            if (has_row)
-              bulk_load(&sm.st[stage][lane * kShrinkK], d.pool + page * d.H + o, (uint32_t)len * 2u,
-                        &sm.full[stage]);
-            if (has_x)
-              bulk_load(&sm.st[stage][kRowsOff + (lane - kShrinkRows) * kShrinkK], xrow + (int64_t)c * d.H + o,
+            uint16_t* dst = sm.st[stage];
+            if (lane < nrows)
+              bulk_load(dst + lane * kShrinkK, d.pool + (int64_t)my * d.H + o, (uint32_t)len * 2u, &sm.full[stage]);
+            else if (lane >= kShrinkRows && lane < kShrinkRows + ntok)
+              bulk_load(dst + kRowsOff + (lane - kShrinkRows) * kShrinkK, xbase + (int64_t)my * P.ldx + (int64_t)c * d.H + o,
                         (uint32_t)len * 2u, &sm.full[stage]);
+            mark(issued, ipar, stage, phase);
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1;
             }
           }
-          page = next_page;
+          if (lane < kShrinkRows) my = next;
         }
       }
     }
     // ---- expand units
     for (int64_t gb = blockIdx.x; gb < Ge && ok; gb += 32 * stride) {
       const int64_t gl = gb + (int64_t)lane * stride;   // lane l resolves unit gb + l * stride
-      int m_p = 0, m_j0 = 0, m_ntok = 0, m_r = 0, m_a = 0, m_c = 0, m_o = 0, m_len = 0, m_tile = 0;
+      int m_p = 0, m_j0 = 0, m_ntok = 0, m_r = 0, m_a = 0, m_c = 0, m_o = 0, m_len = 0;
       int rws[kTT];
 #pragma unroll
       for (int t = 0; t < kTT; ++t) rws[t] = 0;
       if (gl < Ge) {
-        m_tile = (int)(gl / per_tile);
-        int ct = (int)(gl - (int64_t)m_tile * per_tile);
+        const int tile = (int)(gl / per_tile);
+        int ct = (int)(gl - (int64_t)tile * per_tile);
         while (ct >= d.proj[m_p].ncol_tiles) ct -= d.proj[m_p++].ncol_tiles;
-        const int q = find_pos(sm.off_e, d.tile_off, off_smem, S, m_tile);
-        const int tt = m_tile - (off_smem ? sm.off_e[q] : __ldg(d.tile_off + q));
+        const int q = find_pos(sm.off_e, d.tile_off, off_smem, S, tile);
+        const int tt = tile - (off_smem ? sm.off_e[q] : __ldg(d.tile_off + q));
         const int s = __ldg(d.seg_order + q);
         m_j0 = __ldg(d.seg_start + s) + tt * kTT;
         m_ntok = min(kTT, __ldg(d.seg_start + s + 1) - m_j0);
@@ -817,7 +873,6 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
         const int o = __shfl_sync(0xffffffffu, m_o, l);
         const int c = __shfl_sync(0xffffffffu, m_c, l);
         const int len = __shfl_sync(0xffffffffu, m_len, l);
-        const int tile = __shfl_sync(0xffffffffu, m_tile, l);
         int rows[kTT];
 #pragma unroll
         for (int t = 0; t < kTT; ++t) rows[t] = __shfl_sync(0xffffffffu, rws[t], l);
@@ -827,38 +882,37 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
         load_b_pages(d, __shfl_sync(0xffffffffu, m_a, ln), __shfl_sync(0xffffffffu, m_r, ln),
                      __shfl_sync(0xffffffffu, m_p, ln), __shfl_sync(0xffffffffu, m_c, ln), pgn, lane);
         const ProjDev& P = d.proj[p];
-        // wait until every rank row of this tile's v has been published
-        if (fused && lane == 0) {
-          const int32_t* rp = d.ready + (int64_t)p * d.max_tiles + tile;
-          uint32_t it = 0;
-          while (ld_acquire(rp) < r && it < kWaitLimit) {
-            __nanosleep(32);
-            ++it;
-          }
-          if (it == kWaitLimit) ok = false;
-          asm volatile("fence.proxy.async.global;" ::: "memory");  // v is read by bulk copies below
-          if (ok && atomicAdd(d.passed + (int64_t)p * d.max_tiles + tile, 1) == P.ncol_tiles - 1) {
-            d.ready[(int64_t)p * d.max_tiles + tile] = 0;    // every unit of the tile has passed:
-            d.passed[(int64_t)p * d.max_tiles + tile] = 0;   // reset for the next call
-          }
-        }
-        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
-          ok = false;
-          break;
-        }
         const int col0 = c * d.H + o;
         const int buf = (int)(nitem % kStages);
-        const uint32_t vbytes = (uint32_t)((r + 3) & ~3) * 4u;
+        const int vph = (int)((nitem / kStages) & 1);
         for (int k0 = 0; k0 < r; k0 += kExpandRK) {
           const int nk = min(kExpandRK, r - k0);
           const bool first = k0 == 0;
           const int last = k0 + nk >= r;
-          // page of B row k0 + lane: held by lane (k0 % 32) + lane, slot k0 / 32
-          const int page_i = __shfl_sync(0xffffffffu, pick(pg, k0 >> 5), (k0 & 31) + (lane % kExpandRK));
-          if (!acquire_slot(sm, stage, phase, lane)) {
+          if (!acquire()) {
             ok = false;
             break;
           }
+          if (first) {
+            // v rows of the unit: now if the barrier has opened, else held back
+            if (!opened) {
+              opened = barrier_open();
+              // v rows are read by bulk copies (async proxy) after this
+              // lane's acquire of the other CTAs' generic-proxy writes
+              if (opened) asm volatile("fence.proxy.async.global;" ::: "memory");
+            }
+            if (opened) {
+              if (npend > 0) release_pending();
+              load_vrows(sm.V[buf], P.v + (int64_t)j0 * d.v_ld, d.v_ld, ntok, (r + 3) & ~3, &sm.vfull[buf], lane);
+              mark(vissued, vpar, buf, (uint32_t)vph);
+            } else {
+              if (lane == 0) sm.pend[npend] = VPending{buf, vph, p, j0, ntok, r};
+              __syncwarp();
+              ++npend;
+            }
+          }
+          // B row k0 + i's page: held by lane (k0 % 32) + i, slot k0 / 32
+          const int page_i = __shfl_sync(0xffffffffu, pick(pg, k0 >> 5), (k0 & 31) + (lane % kExpandRK));
           if (lane == 0) {
             StageMeta& m = sm.meta[stage];
             m.kind = kKindExpand;
@@ -870,29 +924,23 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
             m.col0 = col0;
             m.nk = nk;
             m.buf = buf;
+            m.vph = vph;
 #pragma unroll
             for (int t = 0; t < kTT; ++t) m.rows[t] = rows[t];
             uint32_t bytes = (uint32_t)nk * (uint32_t)len * 2u;
-            if (first) bytes += (uint32_t)ntok * vbytes;
             if (last) bytes += (uint32_t)ntok * (uint32_t)len * 2u;
             mbar_expect_tx(&sm.full[stage], bytes);
           }
           __syncwarp();
+          uint16_t* dst = sm.st[stage];
           if (lane < nk)
-            bulk_load(&sm.st[stage][lane * kExpandCols], d.pool + (int64_t)page_i * d.H + o, (uint32_t)len * 2u,
+            bulk_load(dst + lane * kExpandCols, d.pool + (int64_t)page_i * d.H + o, (uint32_t)len * 2u,
                       &sm.full[stage]);
-          if (last && lane >= 8 && lane < 8 + ntok) {
-            const int t = lane - 8;
-            bulk_load(&sm.st[stage][kRowsOff + t * kExpandCols],
-                      static_cast<const uint16_t*>(P.y) + (int64_t)pick(rows, t) * P.ldy + col0,
+          else if (last && lane >= kExpandRK && lane < kExpandRK + ntok)
+            bulk_load(dst + kRowsOff + (lane - kExpandRK) * kExpandCols,
+                      static_cast<const uint16_t*>(P.y) + (int64_t)pick(rows, lane - kExpandRK) * P.ldy + col0,
                       (uint32_t)len * 2u, &sm.full[stage]);
-          }
-          if (first && lane == 0) {
-            // issued by the lane that acquired the tile's ready counter and
-            // fenced the async proxy, so the copies see the published v rows
-            for (int t = 0; t < ntok; ++t)
-              bulk_load(&sm.V[buf][t][0], P.v + (int64_t)(j0 + t) * d.v_ld, vbytes, &sm.full[stage]);
-          }
+          mark(issued, ipar, stage, phase);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
@@ -900,6 +948,23 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
         }
 #pragma unroll
         for (int m = 0; m < kPagesPerLane; ++m) pg[m] = pgn[m];
+      }
+    }
+    // v rows still held back (a CTA whose ring never filled up): wait for the
+    // barrier here
+    if (ok && npend > 0) {
+      bool open = false;
+      for (uint32_t it = 0; it < kWaitLimit && !open; ++it) open = barrier_open();
+      if (open) release_pending();
+      else ok = false;
+    }
+    // No copy may still be landing when the CTA exits.  On the normal path
+    // the consumers have waited for every stage and every v buffer; after a
+    // time-out, wait (bounded) for the last phase issued on each barrier.
+    if (!ok && lane == 0) {
+      for (int s2 = 0; s2 < kStages; ++s2) {
+        if (issued >> s2 & 1u) (void)mbar_wait(&sm.full[s2], ipar >> s2 & 1u);
+        if (vissued >> s2 & 1u) (void)mbar_wait(&sm.vfull[s2], vpar >> s2 & 1u);
       }
     }
     if (!ok && lane == 0) report(d.error, kErrTimeout);
@@ -918,7 +983,7 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
         }
         const StageMeta& ms = sm.meta[stage];
         const int ntok = ms.ntok, len = ms.len, nrows = ms.nrows, last = ms.last;
-        const int p = ms.p, j0 = ms.j0, k0 = ms.k0, tile = ms.tile;
+        const int p = ms.p, j0 = ms.j0, k0 = ms.k0;
         if (warp < nrows) {
           float accs[kTT];
 #pragma unroll
@@ -955,14 +1020,21 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
 #pragma unroll
               for (int t = 0; t < kTT; ++t)
                 if (t < ntok) vrow[(int64_t)t * d.v_ld] = tot[t];
-              if (fused) {
-                __threadfence();  // v row visible before it is published
-                atomicAdd(d.ready + (int64_t)p * d.max_tiles + tile, 1);
-              }
             }
           }
           break;
         }
+      }
+    }
+    // ---- grid barrier: this CTA's v rows are written
+    if (lane == 0) __threadfence();
+    asm volatile("bar.sync 1, %0;" ::"n"(kCcConsumerWarps * 32) : "memory");
+    if (threadIdx.x == 0) {
+      if (atomicAdd(d.grid_sync, 1) == (int)gridDim.x - 1) {
+        // the last CTA to arrive: reset the count for the next launch, open
+        d.grid_sync[0] = 0;
+        __threadfence();
+        atomicAdd(d.grid_sync + 1, 1);
       }
     }
     // ---- expand units: thread owns 8 adjacent columns of the unit's tile
@@ -973,6 +1045,7 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
       for (int t = 0; t < kTT; ++t)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[t][e] = make_float2(0.f, 0.f);
+      bool first = true;
       while (true) {
         if (!mbar_wait(&sm.full[stage], phase)) {
           ok = false;
@@ -980,6 +1053,13 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
         }
         const StageMeta& me = sm.meta[stage];
         const int ntok = me.ntok, len = me.len, nk = me.nk, k0 = me.k0, buf = me.buf, last = me.last;
+        if (first) {
+          first = false;
+          if (!mbar_wait(&sm.vfull[buf], (uint32_t)me.vph)) {
+            ok = false;
+            break;
+          }
+        }
         if (col < len) {
           const uint16_t* brows = &sm.st[stage][0];
           switch (ntok) {
@@ -1053,18 +1133,24 @@ __global__ void __launch_bounds__(128) scatter_kernel(const __grid_constant__ Sc
 
 }  // namespace
 
+// Programmatic dependent launch; `cooperative` also asks for every CTA of
+// the grid to be resident at once (the apply kernel's CTAs wait on one
+// another at its grid barrier).
 template <typename Kern>
-cudaError_t launch_pdl(Kern kernel, int grid, int block, size_t smem, cudaStream_t st, const ApplyDev& a) {
+cudaError_t launch_pdl(Kern kernel, int grid, int block, size_t smem, cudaStream_t st, const ApplyDev& a,
+                       bool cooperative) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(block);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = cooperative ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
@@ -1103,8 +1189,8 @@ cudaError_t launch_build_segments(const SegBuildArgs& in, cudaStream_t st) {
 }
 
 cudaError_t launch_apply_cc(const ApplyDev& a, int dtype, int grid, cudaStream_t st) {
-  if (dtype == 0) return launch_pdl(apply_cc_kernel<F16>, grid, kCcThreads, sizeof(ApplySmem), st, a);
-  return launch_pdl(apply_cc_kernel<BF16>, grid, kCcThreads, sizeof(ApplySmem), st, a);
+  if (dtype == 0) return launch_pdl(apply_cc_kernel<F16>, grid, kCcThreads, sizeof(ApplySmem), st, a, true);
+  return launch_pdl(apply_cc_kernel<BF16>, grid, kCcThreads, sizeof(ApplySmem), st, a, true);
 }
 
 cudaError_t launch_scatter(const ScatterDev& a, cudaStream_t st) {

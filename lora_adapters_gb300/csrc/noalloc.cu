@@ -31,9 +31,8 @@ namespace {
 constexpr int kNaMaxTokens = 2048;
 constexpr int kNaMaxSegs = kNaMaxTokens;
 constexpr int kNaMaxAdapters = kMaxAdapters;
-constexpr int kNaMaxTiles = (kNaMaxTokens + kTT - 1) / kTT + kNaMaxSegs;
 constexpr size_t kNaIntsSeg =
-    kNumCounts + kNaMaxTokens + 10 * (size_t)(kNaMaxSegs + 1) + 1 + 2 * (size_t)kMaxProj * kNaMaxTiles;
+    kNumCounts + kNaMaxTokens + 10 * (size_t)(kNaMaxSegs + 1) + 1 + 2;
 constexpr size_t kNaIntsRank = kNaMaxAdapters;
 constexpr size_t kNaIntBytes = ((kNaIntsSeg + kNaIntsRank) * sizeof(int32_t) + 255) / 256 * 256;
 constexpr size_t kNaVFloats = (size_t)kNaMaxTokens * kMaxRank;
@@ -152,9 +151,9 @@ extern "C" int slora_lora_apply_noalloc(const void* d_pool, int32_t page_elems, 
   sd.tc_tile_all = q; q += S1;
   sd.tc_tile_long = q; q += S1;
   int32_t* err = q; q += 1;
-  // ready / passed counters: zero when the module loads, and every call
-  // leaves them zero again
-  int32_t* counters = q; q += 2 * kMaxProj * kNaMaxTiles;
+  // grid barrier of the apply kernel: zero when the module loads; the
+  // segment kernel resets its arrival count on every call
+  int32_t* grid_sync = q; q += 2;
   int32_t* rank_c = ints + kNaIntsSeg;
   float* v = reinterpret_cast<float*>(base + kNaIntBytes);
 
@@ -174,6 +173,7 @@ extern "C" int slora_lora_apply_noalloc(const void* d_pool, int32_t page_elems, 
   b.tc_threshold = 1 << 30;                 // every segment on the CUDA-core kernels
   b.seg = sd;
   b.error = err;
+  b.grid_sync = grid_sync;
   if ((e = launch_build_segments(b, st)) != cudaSuccess) return na_fail(SLORA_ERR_CUDA, "segment build launch", e);
 
   ApplyDev d{};
@@ -207,13 +207,8 @@ extern "C" int slora_lora_apply_noalloc(const void* d_pool, int32_t page_elems, 
   P.rows_before = (int32_t)before;
   P.ncol_tiles = expand_col_tiles(P.h_out, page_elems);
   P.v = v;
-  d.ready = counters;
-  d.passed = counters + kMaxProj * kNaMaxTiles;
-  d.max_tiles = kNaMaxTiles;
-  d.phases = kPhaseShrink;
-  if ((e = launch_apply_cc(d, dtype, g_grid[dev], st)) != cudaSuccess) return na_fail(SLORA_ERR_CUDA, "shrink launch", e);
-  d.phases = kPhaseExpand;
-  if ((e = launch_apply_cc(d, dtype, g_grid[dev], st)) != cudaSuccess) return na_fail(SLORA_ERR_CUDA, "expand launch", e);
+  d.grid_sync = grid_sync;
+  if ((e = launch_apply_cc(d, dtype, g_grid[dev], st)) != cudaSuccess) return na_fail(SLORA_ERR_CUDA, "apply launch", e);
   return SLORA_OK;
 }
 

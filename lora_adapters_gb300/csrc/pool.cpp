@@ -56,9 +56,8 @@ constexpr int32_t kOwnerFree = -1;
 constexpr int32_t kOwnerKV = -2;
 constexpr int32_t kOwnerPending = -3;
 
-enum TimerKind { kTBuild = 0, kTShrinkCC, kTExpandCC, kTShrinkTC, kTExpandTC, kTApplyFused, kTScatter, kTNum };
-const char* kTimerNames[kTNum] = {"build_segments", "shrink_cc", "expand_cc", "shrink_tc",
-                                  "expand_tc",      "apply_fused", "scatter"};
+enum TimerKind { kTBuild = 0, kTApplyCC, kTShrinkTC, kTExpandTC, kTScatter, kTNum };
+const char* kTimerNames[kTNum] = {"build_segments", "apply_cc", "shrink_tc", "expand_tc", "scatter"};
 
 }  // namespace
 
@@ -95,8 +94,7 @@ struct slora_pool {
   int32_t* d_seg_mem = nullptr;
   SegDev seg{};
   float* d_v = nullptr;
-  int32_t* d_counters = nullptr;         // ready + passed counters of the fused apply
-  int32_t max_tiles = 0;
+  int32_t* d_grid_sync = nullptr;        // grid barrier of the apply kernel (2 ints)
   uint16_t* d_staging = nullptr;
   std::vector<cudaEvent_t> load_event;   // per adapter id (created lazily)
   std::vector<char> load_pending;        // load event recorded, maybe not yet complete
@@ -106,7 +104,6 @@ struct slora_pool {
   int32_t seg_T = 0;
   int num_sms = 0;
   int grid_cc = 0;
-  bool fused_apply = false;      // one launch for shrink + expand (SLORA_FUSED_APPLY=1)
   // tensor-core path (page size a multiple of kTcK)
   bool tc_ok = false;
   int32_t v16_ld = 0;            // row stride of the 16-bit v halves
@@ -285,7 +282,7 @@ void free_device(slora_pool* p) {
   cudaFree(p->d_error);
   cudaFree(p->d_seg_mem);
   cudaFree(p->d_v);
-  cudaFree(p->d_counters);
+  cudaFree(p->d_grid_sync);
   cudaFree(p->d_v16);
   cudaFree(p->d_staging);
   if (p->pt_h) cudaFreeHost(p->pt_h);
@@ -406,10 +403,8 @@ int slora_pool_create(slora_pool** out, void* d_pool, int64_t num_pages, int32_t
     p->seg.tc_tile_long = q; q += S1;
     CUDA_TRY(cudaMalloc(&p->d_v, sizeof(float) * (size_t)kMaxProj * std::max(max_tokens, 1) * v_ld(p)));
     CUDA_TRY(cudaMalloc(&p->d_staging, sizeof(uint16_t) * (size_t)p->staging_elems));
-    p->max_tiles = max_token_tiles(std::max(max_tokens, 1), p->max_segs);
-    const size_t counter_bytes = sizeof(int32_t) * 2 * kMaxProj * (size_t)p->max_tiles;
-    CUDA_TRY(cudaMalloc(&p->d_counters, counter_bytes));
-    CUDA_TRY(cudaMemsetAsync(p->d_counters, 0, counter_bytes, p->compute));
+    CUDA_TRY(cudaMalloc(&p->d_grid_sync, 2 * sizeof(int32_t)));
+    CUDA_TRY(cudaMemsetAsync(p->d_grid_sync, 0, 2 * sizeof(int32_t), p->compute));
     CUDA_TRY(cudaMemsetAsync(p->d_pt, 0xff, sizeof(int32_t) * (size_t)pt_entries, p->compute));
     CUDA_TRY(cudaMemsetAsync(p->d_rank, 0, sizeof(int32_t) * (size_t)max_adapters, p->compute));
     CUDA_TRY(cudaMemsetAsync(p->d_error, 0, sizeof(int32_t), p->compute));
@@ -419,7 +414,6 @@ int slora_pool_create(slora_pool** out, void* d_pool, int64_t num_pages, int32_t
     p->load_event.assign((size_t)max_adapters, nullptr);
     p->load_pending.assign((size_t)max_adapters, 0);
     p->grid_cc = p->num_sms;   // one persistent CTA per SM
-    if (const char* f = std::getenv("SLORA_FUSED_APPLY")) p->fused_apply = f[0] == '1';
     // Tensor-core path: needs pages of whole 64-element K blocks.
     p->tc_ok = page_elems % kTcK == 0;
     if (p->tc_ok) {
@@ -647,6 +641,7 @@ int slora_build_segments(slora_pool* p, const int32_t* d_ta, int32_t T, slora_se
   args.tc_threshold = p->tc_threshold;
   args.seg = p->seg;
   args.error = p->d_error;
+  args.grid_sync = p->d_grid_sync;
   {
     Timed tm(p, kTBuild, p->compute);
     CUDA_TRY(launch_build_segments(args, p->compute));
@@ -687,6 +682,7 @@ int slora_lora_apply_multi(slora_pool* p, const slora_segments* seg, int32_t n, 
   d.counts = p->seg.counts;
   d.v_ld = v_ld(p);
   d.error = p->d_error;
+  d.grid_sync = p->d_grid_sync;
   d.s = s;
   for (int i = 0; i < n; ++i) {
     const int q = projs[i];
@@ -752,9 +748,8 @@ int slora_lora_apply_multi(slora_pool* p, const slora_segments* seg, int32_t n, 
     }
     t.tc_off = p->seg.tc_tile_long;
     t.tc_total_idx = kTcTileLong;
-    d.phases = kPhaseShrink;
     {
-      Timed tm(p, kTShrinkCC, p->compute);
+      Timed tm(p, kTApplyCC, p->compute);
       CUDA_TRY(launch_apply_cc(d, p->dtype, p->grid_cc, p->compute));
       tm.done();
     }
@@ -763,35 +758,15 @@ int slora_lora_apply_multi(slora_pool* p, const slora_segments* seg, int32_t n, 
       CUDA_TRY(launch_tc_shrink(t, p->dtype, p->grid_cc, p->compute));
       tm.done();
     }
-    d.phases = kPhaseExpand;
-    {
-      Timed tm(p, kTExpandCC, p->compute);
-      CUDA_TRY(launch_apply_cc(d, p->dtype, p->grid_cc, p->compute));
-      tm.done();
-    }
     {
       Timed tm(p, kTExpandTC, p->compute);
       CUDA_TRY(launch_tc_expand(t, p->dtype, p->grid_cc, p->compute));
       tm.done();
     }
-  } else if (p->fused_apply) {
-    d.phases = kPhaseShrink | kPhaseExpand;
-    Timed tm(p, kTApplyFused, p->compute);
+  } else {
+    Timed tm(p, kTApplyCC, p->compute);
     CUDA_TRY(launch_apply_cc(d, p->dtype, p->grid_cc, p->compute));
     tm.done();
-  } else {
-    d.phases = kPhaseShrink;
-    {
-      Timed tm(p, kTShrinkCC, p->compute);
-      CUDA_TRY(launch_apply_cc(d, p->dtype, p->grid_cc, p->compute));
-      tm.done();
-    }
-    d.phases = kPhaseExpand;
-    {
-      Timed tm(p, kTExpandCC, p->compute);
-      CUDA_TRY(launch_apply_cc(d, p->dtype, p->grid_cc, p->compute));
-      tm.done();
-    }
   }
   return SLORA_OK;
 }
@@ -811,9 +786,9 @@ int slora_device_status(slora_pool* p, int32_t* status) {
   CUDA_TRY(cudaMemsetAsync(p->d_error, 0, sizeof(int32_t), p->compute));
   CUDA_TRY(cudaStreamSynchronize(p->compute));
   if (v == SLORA_ERR_TIMEOUT) {
-    // A call that gave up may have left the fused kernel's tile counters
-    // non-zero; clear them so that the next call starts clean.
-    CUDA_TRY(cudaMemsetAsync(p->d_counters, 0, sizeof(int32_t) * 2 * kMaxProj * (size_t)p->max_tiles, p->compute));
+    // A call that gave up may have left the apply kernel's grid barrier
+    // part-way; clear it so that the next call starts clean.
+    CUDA_TRY(cudaMemsetAsync(p->d_grid_sync, 0, 2 * sizeof(int32_t), p->compute));
     CUDA_TRY(cudaStreamSynchronize(p->compute));
   }
   *status = v;
