@@ -275,7 +275,7 @@ const char* slora_last_error_string(void);
  * caller.
  */
 #define SLORA_NOALLOC_MAX_TOKENS 2048
-#define SLORA_NOALLOC_SCRATCH_BYTES 2318592u /* 2.21 MiB: grouping of 2048 tokens, 32768 ranks, v */
+#define SLORA_NOALLOC_SCRATCH_BYTES 2351360u /* 2.24 MiB: grouping of 2048 tokens, 32768 ranks, v */
 int slora_lora_apply_noalloc(const void* d_pool, int32_t page_elems, int32_t dtype,
                              const int32_t* d_page_table, int64_t pt_stride, const int32_t* d_rank,
                              int32_t max_adapters, int32_t num_proj, const int32_t* proj_in,

@@ -46,6 +46,7 @@ enum CountIdx {
 // max_segs + 1 entries over work-order positions: prefix[q] = work units of
 // the segments seg_order[0..q-1].
 struct SegDev {
+  int4* seg_desc;           // [max_segs] by work-order position: {adapter, rank, start, end}
   int32_t* perm;            // [max_tokens]
   int32_t* seg_start;       // [max_segs + 1]
   int32_t* seg_adapter;     // [max_segs]
@@ -110,11 +111,14 @@ struct ApplyDev {
   int32_t v_ld;                  // multiple of 4 (v rows are bulk-copied)
   float s;
   int32_t* error;                // first device error (0 = none)
-  // Grid barrier between the shrink and expand phases of one launch:
-  // [0] = CTAs arrived (back to 0 when the last arrives), [1] = generation
-  // (incremented when the barrier opens).  Zero-initialised with the pool.
+  const int4* seg_desc;          // per work-order position: {adapter, rank, start, end}
+  // The grid barrier between the apply kernel's shrink and expand phases:
+  // [kSyncCount] CTAs arrived (back to 0 when the last arrives; the segment
+  // kernel also zeroes it), [kSyncGen] generation (incremented when the
+  // barrier opens).  Zero-initialised with the pool.
   int32_t* grid_sync;
 };
+enum : int { kSyncCount = 0, kSyncGen = 1, kGridSyncInts = 2 };
 
 // Column tiles of a row of h_out elements over pages of H: tiles of at most
 // kExpandCols columns that never cross a page boundary.

@@ -60,10 +60,12 @@ __device__ __forceinline__ void unpack8(uint4 v, float (&f)[8]) {
   f[4] = c.x; f[5] = c.y; f[6] = e.x; f[7] = e.y;
 }
 
-// Block-wide exclusive scan of K ints per thread; sh holds 33*K ints.
+// Block-wide exclusive scan of K ints per thread; sh holds 33*K ints.  The
+// second level scans the K per-warp totals in K warps at once.
 template <int K>
 __device__ __forceinline__ void block_scan_excl(int (&v)[K], int (&total)[K], int* sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  static_assert(K <= 32, "one warp per scanned value");
   int inc[K];
 #pragma unroll
   for (int k = 0; k < K; ++k) inc[k] = v[k];
@@ -80,19 +82,16 @@ __device__ __forceinline__ void block_scan_excl(int (&v)[K], int (&total)[K], in
     for (int k = 0; k < K; ++k) sh[warp * K + k] = inc[k];
   }
   __syncthreads();
-  if (warp == 0) {
+  for (int k = warp; k < K; k += nw) {   // warp k scans value k over the warps
+    int w = lane < nw ? sh[lane * K + k] : 0;
+    int ws = w;
 #pragma unroll
-    for (int k = 0; k < K; ++k) {
-      int w = lane < nw ? sh[lane * K + k] : 0;
-      int ws = w;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        int n = __shfl_up_sync(0xffffffffu, ws, off);
-        if (lane >= off) ws += n;
-      }
-      if (lane < nw) sh[lane * K + k] = ws - w;
-      if (lane == 31) sh[32 * K + k] = ws;
+    for (int off = 1; off < 32; off <<= 1) {
+      int n = __shfl_up_sync(0xffffffffu, ws, off);
+      if (lane >= off) ws += n;
     }
+    if (lane < nw) sh[lane * K + k] = ws - w;
+    if (lane == 31) sh[32 * K + k] = ws;
   }
   __syncthreads();
 #pragma unroll
@@ -126,6 +125,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Non-blocking test of the phase of the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(smem_addr(bar)), "r"(parity)
@@ -228,9 +238,9 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
     s_bad = 0;
     s_err = 0;
     // No apply kernel runs now (this kernel is not launched early), so the
-    // apply kernel's grid-barrier count can be reset: a call that gave up
-    // part-way cannot leave later calls a stale count.
-    if (args.grid_sync) args.grid_sync[0] = 0;
+    // apply kernel's barrier count can be reset: a call that gave up part-way
+    // cannot leave later calls a stale count.
+    if (args.grid_sync) args.grid_sync[kSyncCount] = 0;
   }
   __syncthreads();
 
@@ -362,10 +372,11 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
     if (lane == 0) ngrp[warp] = __popc(lead_mask);
     __syncthreads();
     // One warp hands every (warp, adapter) group its first position, walking
-    // the warps in token order; the groups of one warp have distinct
-    // adapters, so its lanes update distinct running starts.
+    // the warps that hold tokens of this tile in token order; the groups of
+    // one warp have distinct adapters, so its lanes update distinct running
+    // starts.
     if (warp == 0) {
-      const int nw = nthr >> 5;
+      const int nw = min(nthr, T - base + 31) >> 5;
       for (int w = 0; w < nw; ++w) {
         const int ng = ngrp[w];
         if (lane < ng) {
@@ -466,7 +477,12 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
       sd.counts[kTcTileLong] = tot[5];
     }
   }
-  // (5) segment arrays built in shared memory go out to global memory
+  // (5) the per-position descriptors; segment arrays built in shared memory
+  // go out to global memory
+  for (int q = tid; q < segs; q += nthr) {
+    const int s = s_order[q];
+    sd.seg_desc[q] = make_int4(s_adapter[s], s_rank[s], s_start[s], s_start[s + 1]);
+  }
   if (seg_smem) {
     for (int s = tid; s < segs; s += nthr) {
       sd.seg_adapter[s] = s_adapter[s];
@@ -676,7 +692,7 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
   pdl_wait();  // the work lists come from the segment kernel; an earlier apply has finished
   // The barrier generation before this launch's CTAs arrive: it changes only
   // once every CTA of this launch has arrived, and this CTA has not.
-  if (threadIdx.x == 0) sm.gen0 = ld_acquire(d.grid_sync + 1);
+  if (threadIdx.x == 0) sm.gen0 = ld_acquire(d.grid_sync + kSyncGen);
   const int units_s = d.counts[d.shrink_total_idx];
   const int tiles = d.counts[d.tile_total_idx];
   const int S = d.counts[kNumSegs];
@@ -692,7 +708,17 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
   for (int p = 0; p < d.nproj; ++p) per_tile += d.proj[p].ncol_tiles;
   const int64_t Gs = (int64_t)units_s * d.nproj;
   const int64_t Ge = (int64_t)tiles * per_tile;
-  const int64_t stride = gridDim.x;
+  // Units in "snake" order: round i gives CTA b unit i * G + b on even rounds
+  // and i * G + (G - 1 - b) on odd rounds.  The lists run largest work first,
+  // so the CTA that drew a larger unit in one round draws a smaller one in the
+  // next, and the CTAs' totals stay close.
+  const int64_t G = gridDim.x, b = blockIdx.x;
+  auto snake_unit = [&](int64_t i) -> int64_t { return i * G + ((i & 1) ? G - 1 - b : b); };
+  auto snake_count = [&](int64_t total) -> int64_t {
+    const int64_t R = total / G, rem = total - R * G;
+    return R + (((R & 1) ? G - 1 - b : b) < rem ? 1 : 0);
+  };
+  const int64_t ns = snake_count(Gs), ne = snake_count(Ge);   // this CTA's units
 
   if (warp == kCcConsumerWarps) {  // ============================ producer warp
     uint32_t stage = 0, phase = 0, nitem = 0;
@@ -709,7 +735,6 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
     const int gen0 = sm.gen0;
     // v rows of the units held back, once the barrier has opened
     auto release_pending = [&]() {
-      asm volatile("fence.proxy.async.global;" ::: "memory");
       for (int i = 0; i < npend; ++i) {
         const VPending e = sm.pend[i];
         load_vrows(sm.V[e.buf], d.proj[e.p].v + (int64_t)e.j0 * d.v_ld, d.v_ld, e.ntok, (e.r + 3) & ~3,
@@ -722,15 +747,19 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
     // acquire semantics, so that each lane's later copies of v rows are
     // ordered after the other CTAs' writes of them.
     auto barrier_open = [&]() -> bool {
-      return __all_sync(0xffffffffu, ld_acquire(d.grid_sync + 1) != gen0);
+      const bool o = __all_sync(0xffffffffu, ld_acquire(d.grid_sync + kSyncGen) != gen0);
+      if (o) asm volatile("fence.proxy.async.global;" ::: "memory");
+      return o;
     };
-    // Next stage slot; while expand units wait for v rows, the wait for a
+    // Next stage slot.  While expand units wait for v rows, the wait for a
     // free slot also watches the grid barrier (the consumers cannot free a
-    // slot before those v rows arrive).
+    // slot before those v rows arrive), without blocking on the slot.
     auto acquire = [&]() -> bool {
       for (uint32_t it = 0; it < kWaitLimit; ++it) {
         int got = 0;
-        if (lane == 0) got = mbar_try_wait(&sm.empty[stage], phase ^ 1) ? 1 : 0;
+        if (lane == 0)
+          got = (npend > 0 ? mbar_test_wait(&sm.empty[stage], phase ^ 1) : mbar_try_wait(&sm.empty[stage], phase ^ 1))
+                    ? 1 : 0;
         if (__shfl_sync(0xffffffffu, got, 0)) return true;
         if (npend > 0 && barrier_open()) {
           opened = true;
@@ -740,26 +769,27 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
       return false;
     };
     // ---- shrink units
-    for (int64_t gb = blockIdx.x; gb < Gs && ok; gb += 32 * stride) {
-      const int64_t gl = gb + (int64_t)lane * stride;   // lane l resolves unit gb + l * stride
+    for (int64_t i0 = 0; i0 < ns && ok; i0 += 32) {
+      const int64_t gl = snake_unit(i0 + lane);   // lane l resolves this CTA's unit i0 + l
+      const int nb = (int)min((int64_t)32, ns - i0);
       int m_p = 0, m_j0 = 0, m_ntok = 0, m_k0 = 0, m_nrows = 0, m_r = 0, m_a = 0;
       int pg[kShrinkRows], xt[kTT];
 #pragma unroll
       for (int i = 0; i < kShrinkRows; ++i) pg[i] = 0;
 #pragma unroll
       for (int t = 0; t < kTT; ++t) xt[t] = 0;
-      if (gl < Gs) {
+      if (lane < nb) {
         const int unit = (int)(gl / d.nproj);
         m_p = (int)(gl - (int64_t)unit * d.nproj);
         const int q = find_pos(sm.off_s, d.shrink_off, off_smem, S, unit);
         const int local = unit - (off_smem ? sm.off_s[q] : __ldg(d.shrink_off + q));
-        const int s = __ldg(d.seg_order + q);
-        m_r = __ldg(d.seg_rank + s);
-        m_a = __ldg(d.seg_adapter + s);
+        const int4 sd = __ldg(d.seg_desc + q);   // adapter, rank, start, end
+        m_a = sd.x;
+        m_r = sd.y;
         const int nrc = (m_r + kShrinkRows - 1) / kShrinkRows;
         const int tt = local / nrc, rc = local - tt * nrc;
-        m_j0 = __ldg(d.seg_start + s) + tt * kTT;
-        m_ntok = min(kTT, __ldg(d.seg_start + s + 1) - m_j0);
+        m_j0 = sd.z + tt * kTT;
+        m_ntok = min(kTT, sd.w - m_j0);
         m_k0 = rc * kShrinkRows;
         m_nrows = min(kShrinkRows, m_r - m_k0);
         const ProjDev& P = d.proj[m_p];
@@ -772,7 +802,6 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
         for (int t = 0; t < kTT; ++t)
           if (t < m_ntok) xt[t] = __ldg(d.perm + m_j0 + t);
       }
-      const int nb = (int)min((int64_t)32, (Gs - gb + stride - 1) / stride);
       for (int l = 0; l < nb && ok; ++l) {
         const int p = __shfl_sync(0xffffffffu, m_p, l);
         const int j0 = __shfl_sync(0xffffffffu, m_j0, l);
@@ -839,29 +868,29 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
       }
     }
     // ---- expand units
-    for (int64_t gb = blockIdx.x; gb < Ge && ok; gb += 32 * stride) {
-      const int64_t gl = gb + (int64_t)lane * stride;   // lane l resolves unit gb + l * stride
+    for (int64_t i0 = 0; i0 < ne && ok; i0 += 32) {
+      const int64_t gl = snake_unit(i0 + lane);   // lane l resolves this CTA's unit i0 + l
+      const int nb = (int)min((int64_t)32, ne - i0);
       int m_p = 0, m_j0 = 0, m_ntok = 0, m_r = 0, m_a = 0, m_c = 0, m_o = 0, m_len = 0;
       int rws[kTT];
 #pragma unroll
       for (int t = 0; t < kTT; ++t) rws[t] = 0;
-      if (gl < Ge) {
+      if (lane < nb) {
         const int tile = (int)(gl / per_tile);
         int ct = (int)(gl - (int64_t)tile * per_tile);
         while (ct >= d.proj[m_p].ncol_tiles) ct -= d.proj[m_p++].ncol_tiles;
         const int q = find_pos(sm.off_e, d.tile_off, off_smem, S, tile);
         const int tt = tile - (off_smem ? sm.off_e[q] : __ldg(d.tile_off + q));
-        const int s = __ldg(d.seg_order + q);
-        m_j0 = __ldg(d.seg_start + s) + tt * kTT;
-        m_ntok = min(kTT, __ldg(d.seg_start + s + 1) - m_j0);
-        m_r = __ldg(d.seg_rank + s);
-        m_a = __ldg(d.seg_adapter + s);
+        const int4 sd = __ldg(d.seg_desc + q);   // adapter, rank, start, end
+        m_a = sd.x;
+        m_r = sd.y;
+        m_j0 = sd.z + tt * kTT;
+        m_ntok = min(kTT, sd.w - m_j0);
         col_tile(ct, d.proj[m_p].h_out, d.H, m_c, m_o, m_len);
 #pragma unroll
         for (int t = 0; t < kTT; ++t)
           if (t < m_ntok) rws[t] = __ldg(d.perm + m_j0 + t);
       }
-      const int nb = (int)min((int64_t)32, (Ge - gb + stride - 1) / stride);
       int pg[kPagesPerLane];
       load_b_pages(d, __shfl_sync(0xffffffffu, m_a, 0), __shfl_sync(0xffffffffu, m_r, 0),
                    __shfl_sync(0xffffffffu, m_p, 0), __shfl_sync(0xffffffffu, m_c, 0), pg, lane);
@@ -895,12 +924,7 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
           }
           if (first) {
             // v rows of the unit: now if the barrier has opened, else held back
-            if (!opened) {
-              opened = barrier_open();
-              // v rows are read by bulk copies (async proxy) after this
-              // lane's acquire of the other CTAs' generic-proxy writes
-              if (opened) asm volatile("fence.proxy.async.global;" ::: "memory");
-            }
+            if (!opened) opened = barrier_open();
             if (opened) {
               if (npend > 0) release_pending();
               load_vrows(sm.V[buf], P.v + (int64_t)j0 * d.v_ld, d.v_ld, ntok, (r + 3) & ~3, &sm.vfull[buf], lane);
@@ -972,7 +996,7 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
     uint32_t stage = 0, phase = 0;
     bool ok = true;
     // ---- shrink units: warp w owns rank row k0 + w of the unit
-    for (int64_t g = blockIdx.x; g < Gs && ok; g += stride) {
+    for (int64_t i = 0; i < ns && ok; ++i) {
       float acc[kTT];
 #pragma unroll
       for (int t = 0; t < kTT; ++t) acc[t] = 0.f;
@@ -1026,20 +1050,22 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
         }
       }
     }
-    // ---- grid barrier: this CTA's v rows are written
-    if (lane == 0) __threadfence();
+    // ---- grid barrier: this CTA's v rows are written.  The CTA barrier
+    // orders every consumer warp's v stores before thread 0's release add,
+    // which makes them visible at GPU scope with it.
     asm volatile("bar.sync 1, %0;" ::"n"(kCcConsumerWarps * 32) : "memory");
     if (threadIdx.x == 0) {
-      if (atomicAdd(d.grid_sync, 1) == (int)gridDim.x - 1) {
+      int prev;
+      asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(prev) : "l"(d.grid_sync + kSyncCount) : "memory");
+      if (prev == (int)gridDim.x - 1) {
         // the last CTA to arrive: reset the count for the next launch, open
-        d.grid_sync[0] = 0;
-        __threadfence();
-        atomicAdd(d.grid_sync + 1, 1);
+        d.grid_sync[kSyncCount] = 0;
+        asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(d.grid_sync + kSyncGen) : "memory");
       }
     }
     // ---- expand units: thread owns 8 adjacent columns of the unit's tile
     const int col = threadIdx.x * 8;  // threads 0..255
-    for (int64_t g = blockIdx.x; g < Ge && ok; g += stride) {
+    for (int64_t i = 0; i < ne && ok; ++i) {
       float2 acc[kTT][4];
 #pragma unroll
       for (int t = 0; t < kTT; ++t)

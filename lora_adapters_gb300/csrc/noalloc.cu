@@ -32,7 +32,7 @@ constexpr int kNaMaxTokens = 2048;
 constexpr int kNaMaxSegs = kNaMaxTokens;
 constexpr int kNaMaxAdapters = kMaxAdapters;
 constexpr size_t kNaIntsSeg =
-    kNumCounts + kNaMaxTokens + 10 * (size_t)(kNaMaxSegs + 1) + 1 + 2;
+    4 * (size_t)(kNaMaxSegs + 1) + kNumCounts + kNaMaxTokens + 10 * (size_t)(kNaMaxSegs + 1) + 1 + kGridSyncInts;
 constexpr size_t kNaIntsRank = kNaMaxAdapters;
 constexpr size_t kNaIntBytes = ((kNaIntsSeg + kNaIntsRank) * sizeof(int32_t) + 255) / 256 * 256;
 constexpr size_t kNaVFloats = (size_t)kNaMaxTokens * kMaxRank;
@@ -138,6 +138,7 @@ extern "C" int slora_lora_apply_noalloc(const void* d_pool, int32_t page_elems, 
   SegDev sd{};
   int32_t* q = ints;
   const int64_t S1 = kNaMaxSegs + 1;
+  sd.seg_desc = reinterpret_cast<int4*>(q); q += 4 * S1;   // 16-byte aligned: first in the array
   sd.counts = q; q += kNumCounts;
   sd.perm = q; q += kNaMaxTokens;
   sd.seg_start = q; q += S1;
@@ -151,9 +152,9 @@ extern "C" int slora_lora_apply_noalloc(const void* d_pool, int32_t page_elems, 
   sd.tc_tile_all = q; q += S1;
   sd.tc_tile_long = q; q += S1;
   int32_t* err = q; q += 1;
-  // grid barrier of the apply kernel: zero when the module loads; the
+  // the apply kernel's grid barrier: zero when the module loads; the
   // segment kernel resets its arrival count on every call
-  int32_t* grid_sync = q; q += 2;
+  int32_t* grid_sync = q; q += kGridSyncInts;
   int32_t* rank_c = ints + kNaIntsSeg;
   float* v = reinterpret_cast<float*>(base + kNaIntBytes);
 
@@ -208,6 +209,7 @@ extern "C" int slora_lora_apply_noalloc(const void* d_pool, int32_t page_elems, 
   P.ncol_tiles = expand_col_tiles(P.h_out, page_elems);
   P.v = v;
   d.grid_sync = grid_sync;
+  d.seg_desc = sd.seg_desc;
   if ((e = launch_apply_cc(d, dtype, g_grid[dev], st)) != cudaSuccess) return na_fail(SLORA_ERR_CUDA, "apply launch", e);
   return SLORA_OK;
 }

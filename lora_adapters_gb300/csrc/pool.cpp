@@ -94,7 +94,7 @@ struct slora_pool {
   int32_t* d_seg_mem = nullptr;
   SegDev seg{};
   float* d_v = nullptr;
-  int32_t* d_grid_sync = nullptr;        // grid barrier of the apply kernel (2 ints)
+  int32_t* d_grid_sync = nullptr;        // the apply kernel's grid barrier
   uint16_t* d_staging = nullptr;
   std::vector<cudaEvent_t> load_event;   // per adapter id (created lazily)
   std::vector<char> load_pending;        // load event recorded, maybe not yet complete
@@ -384,11 +384,13 @@ int slora_pool_create(slora_pool** out, void* d_pool, int64_t num_pages, int32_t
     CUDA_TRY(cudaMalloc(&p->d_pt, sizeof(int32_t) * (size_t)pt_entries));
     CUDA_TRY(cudaMalloc(&p->d_rank, sizeof(int32_t) * (size_t)max_adapters));
     CUDA_TRY(cudaMalloc(&p->d_error, sizeof(int32_t)));
-    // segment arrays: perm, seg_start, seg_adapter, seg_rank, counts, 6 prefix arrays
+    // segment arrays: per-position descriptors (16-byte aligned, first),
+    // counts, perm, seg_start, seg_adapter, seg_rank, seg_order, 6 prefix arrays
     const int64_t S1 = p->max_segs + 1;
-    const int64_t seg_ints = std::max<int64_t>(max_tokens, 1) + S1 * 10 + kNumCounts;
+    const int64_t seg_ints = 4 * S1 + std::max<int64_t>(max_tokens, 1) + S1 * 10 + kNumCounts;
     CUDA_TRY(cudaMalloc(&p->d_seg_mem, sizeof(int32_t) * (size_t)seg_ints));
     int32_t* q = p->d_seg_mem;
+    p->seg.seg_desc = reinterpret_cast<int4*>(q); q += 4 * S1;
     p->seg.counts = q; q += kNumCounts;
     p->seg.perm = q; q += std::max<int64_t>(max_tokens, 1);
     p->seg.seg_start = q; q += S1;
@@ -403,8 +405,8 @@ int slora_pool_create(slora_pool** out, void* d_pool, int64_t num_pages, int32_t
     p->seg.tc_tile_long = q; q += S1;
     CUDA_TRY(cudaMalloc(&p->d_v, sizeof(float) * (size_t)kMaxProj * std::max(max_tokens, 1) * v_ld(p)));
     CUDA_TRY(cudaMalloc(&p->d_staging, sizeof(uint16_t) * (size_t)p->staging_elems));
-    CUDA_TRY(cudaMalloc(&p->d_grid_sync, 2 * sizeof(int32_t)));
-    CUDA_TRY(cudaMemsetAsync(p->d_grid_sync, 0, 2 * sizeof(int32_t), p->compute));
+    CUDA_TRY(cudaMalloc(&p->d_grid_sync, kGridSyncInts * sizeof(int32_t)));
+    CUDA_TRY(cudaMemsetAsync(p->d_grid_sync, 0, kGridSyncInts * sizeof(int32_t), p->compute));
     CUDA_TRY(cudaMemsetAsync(p->d_pt, 0xff, sizeof(int32_t) * (size_t)pt_entries, p->compute));
     CUDA_TRY(cudaMemsetAsync(p->d_rank, 0, sizeof(int32_t) * (size_t)max_adapters, p->compute));
     CUDA_TRY(cudaMemsetAsync(p->d_error, 0, sizeof(int32_t), p->compute));
@@ -683,6 +685,7 @@ int slora_lora_apply_multi(slora_pool* p, const slora_segments* seg, int32_t n, 
   d.v_ld = v_ld(p);
   d.error = p->d_error;
   d.grid_sync = p->d_grid_sync;
+  d.seg_desc = p->seg.seg_desc;
   d.s = s;
   for (int i = 0; i < n; ++i) {
     const int q = projs[i];
@@ -788,7 +791,7 @@ int slora_device_status(slora_pool* p, int32_t* status) {
   if (v == SLORA_ERR_TIMEOUT) {
     // A call that gave up may have left the apply kernel's grid barrier
     // part-way; clear it so that the next call starts clean.
-    CUDA_TRY(cudaMemsetAsync(p->d_grid_sync, 0, 2 * sizeof(int32_t), p->compute));
+    CUDA_TRY(cudaMemsetAsync(p->d_grid_sync, 0, kGridSyncInts * sizeof(int32_t), p->compute));
     CUDA_TRY(cudaStreamSynchronize(p->compute));
   }
   *status = v;
