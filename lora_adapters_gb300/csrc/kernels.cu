@@ -184,7 +184,8 @@ __device__ __forceinline__ int pick(const int (&a)[N], int i) {
 // ---- build_segments ----------------------------------------------------------------
 // One CTA of 1024 threads.
 //  (1) histogram of adapter ids in shared memory (ids out of range or not
-//      resident are left out and reported), caching each adapter's rank;
+//      resident are left out and reported); every adapter's rank is read
+//      into shared memory first when it fits;
 //  (2) one block scan over the histogram (each thread owns a run of adapter
 //      ids) -> one segment per adapter present, in ascending id;
 //  (3) stable scatter of token indices: tokens are visited in order, 1024 at
@@ -232,7 +233,15 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
   // kernel's results (griddepcontrol.wait) before reading any of them.
   pdl_trigger();
 
-  for (int a = tid; a < A; a += nthr) hist[a] = 0;
+  // Zero the histogram and, with independent loads in flight together, bring
+  // in every adapter's rank (when the cache fits) and the batch's keys (when
+  // they fit): no dependent round trip per token.
+  for (int a = tid; a < A; a += nthr) {
+    hist[a] = 0;
+    if (rank_smem) rank_s[a] = args.rank[a];
+  }
+  if (keys_smem)
+    for (int i = tid; i < T; i += nthr) skeys[i] = args.token_adapter[i];
   for (int r = tid; r <= kMaxRank; r += nthr) rcount[r] = 0;
   if (tid == 0) {
     s_bad = 0;
@@ -244,7 +253,7 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
   }
   __syncthreads();
 
-  // (1) histogram and rank cache; keys of the first tiles are kept for (3)
+  // (1) histogram; keys of the first tiles are kept for (3)
   // Whole warps call this (inactive lanes pass i >= T); equal keys within a
   // warp are counted with one shared-memory atomic (prefill batches hold long
   // runs of one adapter, which would otherwise serialise on one address).
@@ -253,10 +262,9 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
     if (i < T) {
       const int a = args.token_adapter[i];
       if (a >= 0 && a < A) {
-        const int r = args.rank[a];
+        const int r = rank_smem ? rank_s[a] : args.rank[a];
         if (r > 0) {
           key = a;
-          if (rank_smem) rank_s[a] = r;
         } else {
           atomicAdd(&s_bad, 1);
           atomicCAS(&s_err, 0, -4 /* SLORA_ERR_NOT_RESIDENT */);
@@ -272,18 +280,14 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
   };
   int keys[kCachedTiles];
   if (keys_smem) {
-    // all keys staged in shared memory with independent loads, validated in
-    // a second independent pass (no per-tile chain of dependent round trips)
-    for (int i = tid; i < T; i += nthr) skeys[i] = args.token_adapter[i];
-    __syncthreads();
+    // all keys were staged in shared memory above; validated here
     for (int i = tid; i < T; i += nthr) {
       const int a = skeys[i];
       int key = -1;
       if (a >= 0 && a < A) {
-        const int r = args.rank[a];
+        const int r = rank_smem ? rank_s[a] : args.rank[a];
         if (r > 0) {
           key = a;
-          if (rank_smem) rank_s[a] = r;
         } else {
           atomicAdd(&s_bad, 1);
           atomicCAS(&s_err, 0, -4 /* SLORA_ERR_NOT_RESIDENT */);
@@ -356,7 +360,7 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
       key = pick(keys, c);
     } else if (i < T) {
       const int a = args.token_adapter[i];
-      if (a >= 0 && a < A && args.rank[a] > 0) key = a;
+      if (a >= 0 && a < A && (rank_smem ? rank_s[a] : args.rank[a]) > 0) key = a;
     }
     const bool valid = key >= 0;
     const unsigned peers = __match_any_sync(0xffffffffu, key);
