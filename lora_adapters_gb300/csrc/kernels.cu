@@ -280,9 +280,11 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
   };
   int keys[kCachedTiles];
   if (keys_smem) {
-    // all keys were staged in shared memory above; validated here
-    for (int i = tid; i < T; i += nthr) {
-      const int a = skeys[i];
+    // all keys were staged in shared memory above; validated and counted in
+    // one pass (whole warps take part in every iteration for match_any)
+    for (int base = 0; base < T; base += nthr) {
+      const int i = base + tid;
+      const int a = i < T ? skeys[i] : -1;
       int key = -1;
       if (a >= 0 && a < A) {
         const int r = rank_smem ? rank_s[a] : args.rank[a];
@@ -296,19 +298,14 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
         atomicAdd(&s_bad, 1);
         atomicCAS(&s_err, 0, -1 /* SLORA_ERR_INVALID */);
       }
-      skeys[i] = key;
-    }
-    __syncthreads();
-    for (int base = 0; base < T; base += nthr) {
-      const int i = base + tid;
-      const int key = i < T ? skeys[i] : -1;
+      if (i < T) skeys[i] = key;
       const unsigned peers = __match_any_sync(0xffffffffu, key);
       if (key >= 0 && (peers & ((1u << lane) - 1u)) == 0u) atomicAdd(&hist[key], __popc(peers));
     }
   } else {
 #pragma unroll
-    for (int c = 0; c < kCachedTiles; ++c) keys[c] = classify(c * kSegThreads + tid);
-    for (int base = kCachedTiles * kSegThreads; base < T; base += nthr) classify(base + tid);
+    for (int c = 0; c < kCachedTiles; ++c) keys[c] = classify(c * nthr + tid);
+    for (int base = kCachedTiles * nthr; base < T; base += nthr) classify(base + tid);
   }
   __syncthreads();
 
@@ -331,7 +328,9 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
       if (c > 0) {
         s_adapter[s] = a;
         s_start[s] = pos;
-        s_rank[s] = rank_smem ? rank_s[a] : args.rank[a];
+        const int r = rank_smem ? rank_s[a] : args.rank[a];
+        s_rank[s] = r;
+        atomicAdd(&rcount[r], 1);   // (4a) folded in: segments per rank
         hist[a] = pos;
         pos += c;
         ++s;
@@ -396,9 +395,6 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
     if (valid) sd.perm[grp_base[warp][slot] + rank_w] = i;
   }
 
-  // (4a) histogram of segment ranks
-  for (int s = tid; s < segs; s += nthr) atomicAdd(&rcount[s_rank[s]], 1);
-  __syncthreads();
   // (4b) start of each rank's run, largest rank first (warp 0; 9 ranks per lane)
   if (warp == 0) {
     int run = 0;
@@ -1214,7 +1210,9 @@ cudaError_t launch_build_segments(const SegBuildArgs& in, cudaStream_t st) {
       a.smem_flags |= kKeysInSmem;
     }
   }
-  build_segments_kernel<<<1, kSegThreads, smem, st>>>(a);
+  // Small batches take a smaller block: its barriers are cheaper.
+  const int threads = a.T <= 256 ? 256 : a.T <= 512 ? 512 : kSegThreads;
+  build_segments_kernel<<<1, threads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
