@@ -106,6 +106,8 @@ struct ApplyDev {
   const int32_t* counts;
   const int32_t* shrink_off;     // prefix array of the chosen work list
   const int32_t* tile_off;
+  int32_t off_n;                 // prefix entries the kernel may stage in shared memory:
+                                 // min(kSegSmem, segments this batch can have + 1)
   int32_t shrink_total_idx;      // counts[] index of the list's totals
   int32_t tile_total_idx;
   int32_t v_ld;                  // multiple of 4 (v rows are bulk-copied)

@@ -693,15 +693,17 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
   // The barrier generation before this launch's CTAs arrive: it changes only
   // once every CTA of this launch has arrived, and this CTA has not.
   if (threadIdx.x == 0) sm.gen0 = ld_acquire(d.grid_sync + kSyncGen);
+  // The work-list prefixes are loaded for as many positions as the batch can
+  // have segments (d.off_n, set by the host), together with the counts, so
+  // that the prologue costs one round of loads.
+  for (int i = threadIdx.x; i < d.off_n; i += blockDim.x) {
+    sm.off_s[i] = d.shrink_off[i];
+    sm.off_e[i] = d.tile_off[i];
+  }
   const int units_s = d.counts[d.shrink_total_idx];
   const int tiles = d.counts[d.tile_total_idx];
   const int S = d.counts[kNumSegs];
-  const bool off_smem = S + 1 <= kSegSmem;
-  if (off_smem)
-    for (int i = threadIdx.x; i <= S; i += blockDim.x) {
-      sm.off_s[i] = d.shrink_off[i];
-      sm.off_e[i] = d.tile_off[i];
-    }
+  const bool off_smem = S + 1 <= d.off_n;
   __syncthreads();
   pdl_trigger();
   int per_tile = 0;  // expand units of one token tile: (projection, column tile)
@@ -1058,9 +1060,10 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
       int prev;
       asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(prev) : "l"(d.grid_sync + kSyncCount) : "memory");
       if (prev == (int)gridDim.x - 1) {
-        // the last CTA to arrive: reset the count for the next launch, open
-        d.grid_sync[kSyncCount] = 0;
+        // the last CTA to arrive opens the barrier, then resets the count for
+        // the next launch (whose CTAs arrive only after this grid has ended)
         asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(d.grid_sync + kSyncGen) : "memory");
+        d.grid_sync[kSyncCount] = 0;
       }
     }
     // ---- expand units: thread owns 8 adjacent columns of the unit's tile

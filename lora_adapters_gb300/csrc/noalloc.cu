@@ -210,6 +210,7 @@ extern "C" int slora_lora_apply_noalloc(const void* d_pool, int32_t page_elems, 
   P.v = v;
   d.grid_sync = grid_sync;
   d.seg_desc = sd.seg_desc;
+  d.off_n = (T < max_adapters ? T : max_adapters) + 1 < kSegSmem ? (T < max_adapters ? T : max_adapters) + 1 : kSegSmem;
   if ((e = launch_apply_cc(d, dtype, g_grid[dev], st)) != cudaSuccess) return na_fail(SLORA_ERR_CUDA, "apply launch", e);
   return SLORA_OK;
 }

@@ -686,6 +686,7 @@ int slora_lora_apply_multi(slora_pool* p, const slora_segments* seg, int32_t n, 
   d.error = p->d_error;
   d.grid_sync = p->d_grid_sync;
   d.seg_desc = p->seg.seg_desc;
+  d.off_n = std::min<int32_t>(kSegSmem, std::max(1, std::min(p->seg_T, p->max_adapters)) + 1);
   d.s = s;
   for (int i = 0; i < n; ++i) {
     const int q = projs[i];
