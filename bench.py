@@ -344,7 +344,7 @@ def main():
 
     # ---- roofline of the dominant kernel
     hbm_peak, peak_kind = _peaks()
-    ab = algorithmic_bytes(wl, None if args.mode == "decode" else TC_THRESHOLD)
+    ab = algorithmic_bytes(wl, {"decode": None, "auto": TC_THRESHOLD, "prefill": 0}[args.mode])
     per_kernel = {}
     for name, (tms, cnt) in kern.items():
         if cnt:

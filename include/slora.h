@@ -65,7 +65,7 @@ extern "C" {
 
 #define SLORA_MODE_AUTO 0    /* CUDA-core tiles below the tensor-core threshold, tcgen05 tiles above */
 #define SLORA_MODE_DECODE 1  /* every segment on the CUDA-core gather kernels */
-#define SLORA_MODE_PREFILL 2 /* every segment on the tcgen05 tensor-core kernels */
+#define SLORA_MODE_PREFILL 2 /* every segment on the tcgen05 kernels (CUDA-core kernels when the page size is not a multiple of 64) */
 
 /* Library limits (also checked at run time). */
 #define SLORA_MAX_PROJ 8           /* projections per pool */

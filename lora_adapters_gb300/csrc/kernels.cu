@@ -374,21 +374,47 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
     }
     if (lane == 0) ngrp[warp] = __popc(lead_mask);
     __syncthreads();
-    // One warp hands every (warp, adapter) group its first position, walking
-    // the warps that hold tokens of this tile in token order; the groups of
-    // one warp have distinct adapters, so its lanes update distinct running
-    // starts.
+    // One warp hands every (warp, adapter) group its first position, in
+    // token order: the adapter's running start plus the tokens of that
+    // adapter in earlier warps of this tile; the running start then moves
+    // past this tile.  When every warp holds one group (long runs of one
+    // adapter, as in prefill batches of several tiles) lane w takes warp w's
+    // group and all bases come from one round of shuffles; otherwise the warps are walked
+    // one by one (the groups of one warp have distinct adapters, so its
+    // lanes update distinct running starts).
     if (warp == 0) {
-      const int nw = min(nthr, T - base + 31) >> 5;
-      for (int w = 0; w < nw; ++w) {
-        const int ng = ngrp[w];
-        if (lane < ng) {
-          const int k = grp_key[w][lane];
-          const int b = hist[k];
-          grp_base[w][lane] = b;
-          hist[k] = b + grp_cnt[w][lane];
+      const int nw = min(nthr, T - base + 31) >> 5;   // warps with tokens in this tile
+      const int ng_l = lane < nw ? ngrp[lane] : 0;
+      if (T > nthr && __all_sync(0xffffffffu, ng_l <= 1)) {   // batches of several tiles
+        const int k_l = ng_l ? grp_key[lane][0] : -1 - lane;   // empty warps match nothing
+        const int c_l = ng_l ? grp_cnt[lane][0] : 0;
+        int before = 0;
+        bool last_of_key = true;
+        for (int j = 0; j < 32; ++j) {
+          const int kj = __shfl_sync(0xffffffffu, k_l, j);
+          const int cj = __shfl_sync(0xffffffffu, c_l, j);
+          if (kj == k_l) {
+            if (j < lane) before += cj;
+            if (j > lane) last_of_key = false;
+          }
         }
+        const int b0 = ng_l ? hist[k_l] : 0;
         __syncwarp();
+        if (ng_l) {
+          grp_base[lane][0] = b0 + before;
+          if (last_of_key) hist[k_l] = b0 + before + c_l;
+        }
+      } else {
+        for (int w = 0; w < nw; ++w) {
+          const int ng = ngrp[w];
+          if (lane < ng) {
+            const int k = grp_key[w][lane];
+            const int b = hist[k];
+            grp_base[w][lane] = b;
+            hist[k] = b + grp_cnt[w][lane];
+          }
+          __syncwarp();
+        }
       }
     }
     __syncthreads();

@@ -750,9 +750,13 @@ int slora_lora_apply_multi(slora_pool* p, const slora_segments* seg, int32_t n, 
       t.vlo[i] = t.vhi[i] + half_elems;
       t.tc_ncol[i] = tc_col_tiles(P.h_out, p->H);
     }
-    t.tc_off = p->seg.tc_tile_long;
-    t.tc_total_idx = kTcTileLong;
-    {
+    if (mode == SLORA_MODE_PREFILL) {
+      // every segment on the tensor cores; no CUDA-core launch
+      t.tc_off = p->seg.tc_tile_all;
+      t.tc_total_idx = kTcTileAll;
+    } else {
+      t.tc_off = p->seg.tc_tile_long;
+      t.tc_total_idx = kTcTileLong;
       Timed tm(p, kTApplyCC, p->compute);
       CUDA_TRY(launch_apply_cc(d, p->dtype, p->grid_cc, p->compute));
       tm.done();
