@@ -278,12 +278,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_shrink_kernel(const __grid_c
           uint16_t hi[16], lo[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const bool in = c0 + i < u.r;
-            const float x = in ? v[i] : 0.f;
+            const float x = c0 + i < u.r ? v[i] : 0.f;
+            v[i] = x;
             hi[i] = Elem<E>::from(x);
             lo[i] = Elem<E>::from(x - Elem<E>::to(hi[i]));
-            if (in) vrow[c0 + i] = x;
           }
+          // fp32 v: 16-byte stores up to the row's last multiple of 4 columns
+          // (the v row stride is a multiple of 4 floats, past r only padding)
+#pragma unroll
+          for (int i = 0; i < 16; i += 4)
+            if (c0 + i < u.r) *reinterpret_cast<float4*>(vrow + c0 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
           uint4 h0, h1, l0, l1;
           memcpy(&h0, hi, 16);
           memcpy(&h1, hi + 8, 16);
@@ -313,7 +317,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_shrink_kernel(const __grid_c
 // Work unit = (segment in work order, projection, column tile of <= kTcNe
 // columns inside one page).  The adapter's B rows for the column tile are
 // gathered once per unit (all rank rows, N-major) and reused by every 128-token
-// tile of the segment; per token tile the producer loads the tile's v halves
+// tile of the segment.  Units of rank <= 128 alternate between the two halves
+// of the B area, so the next unit's rows load while this one computes; a unit
+// of larger rank takes the whole area.  Per token tile the producer loads the tile's v halves
 // (2-D boxes, rows consecutive in sorted order) and its y rows (2-D boxes when
 // the tile is a run of consecutive tokens, row gathers otherwise) into
 // double-buffered stages, so the epilogue reads y from shared memory and its
@@ -326,7 +332,7 @@ struct TcExpandSmem {
   uint8_t Vhi[2][kTcM * kRowBytes];                  // 128 tokens x 64 ranks (16 KB)
   uint8_t Vlo[2][kTcM * kRowBytes];
   uint8_t Y[2][kEAtoms][kTcM * kRowBytes];           // 128 tokens x 128 columns (32 KB)
-  uint64_t b_full, b_empty, v_full[2], v_empty[2], y_full[2], y_empty[2], tfull[2], tempty[2];
+  uint64_t b_full[2], b_empty[2], v_full[2], v_empty[2], y_full[2], y_empty[2], tfull[2], tempty[2];
   uint32_t tmem_slot;
 };
 
@@ -369,9 +375,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expand_kernel(const __grid_c
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == 1) tmem_alloc(&sm.tmem_slot, 2 * kTcNe);
   if (threadIdx.x == 0) {
-    mbar_init(&sm.b_full, 1);
-    mbar_init(&sm.b_empty, 1);
     for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.b_full[b], 1);
+      mbar_init(&sm.b_empty[b], 1);
       mbar_init(&sm.v_full[b], 1);
       mbar_init(&sm.v_empty[b], 1);
       mbar_init(&sm.y_full[b], 1);
@@ -400,7 +406,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expand_kernel(const __grid_c
   };
 
   if (warp == 0) {  // ------------------------------------------ producer
-    uint32_t nb_ = 0, nv = 0, ny = 0;  // B units, v stages, y tiles issued
+    uint32_t bu0 = 0, bu1 = 0, nv = 0, ny = 0;  // B uses per half, v stages, y tiles issued
+    int bsel = 0;
     for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x) {
       const TcEUnit u = tc_eunit(t, g, per_seg);
       if (u.ntm == 0) continue;
@@ -410,11 +417,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expand_kernel(const __grid_c
       const int natoms = (u.ncols + 63) >> 6;
       const int col0 = u.c * d.H + u.o;
       // B rows of this column tile, all rank blocks (rows >= r: row 0 again;
-      // the matching v columns are zero)
-      if (!wait_lane0(&sm.b_empty, (nb_ & 1) ^ 1)) { ok = false; break; }
-      ++nb_;
-      if (lane == 0) mbar_expect_tx(&sm.b_full, (uint32_t)(natoms * r16) * kRowBytes);
+      // the matching v columns are zero), into half bsel of the B area, or
+      // into the whole area for ranks above 128
+      const bool whole = nkb > kEKBlocks / 2;
+      const int hb = whole ? 0 : bsel;
+      if (!wait_lane0(&sm.b_empty[hb], ((hb ? bu1 : bu0) & 1) ^ 1)) { ok = false; break; }
+      if (hb) ++bu1; else ++bu0;
+      if (whole) {
+        if (!wait_lane0(&sm.b_empty[1], (bu1 & 1) ^ 1)) { ok = false; break; }
+        ++bu1;
+      } else {
+        bsel ^= 1;
+      }
+      if (lane == 0) {
+        mbar_expect_tx(&sm.b_full[hb], (uint32_t)(natoms * r16) * kRowBytes);
+        if (whole) mbar_arrive(&sm.b_full[1]);
+      }
       __syncwarp();
+      const int kb0 = hb * (kEKBlocks / 2);   // first rank block of this half
       const int32_t* ptB = d.page_table + (int64_t)u.a * d.pt_stride + (int64_t)u.r * (P.rows_before + P.ppi) + u.c;
       for (int k4 = lane; 4 * k4 < r16; k4 += 32) {
         int pg[4];
@@ -423,10 +443,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expand_kernel(const __grid_c
           const int row = 4 * k4 + i;
           pg[i] = __ldg(ptB + (int64_t)(row < u.r ? row : 0) * P.ppo);
         }
-        const int kb = (4 * k4) / kTcK, kr = (4 * k4) % kTcK;
+        const int kb = kb0 + (4 * k4) / kTcK, kr = (4 * k4) % kTcK;
         for (int nb = 0; nb < natoms; ++nb)
           tma_gather4(&sm.B[kb][nb][kr * kRowBytes], &t.pool_map, u.o + 64 * nb, pg[0], pg[1], pg[2], pg[3],
-                      &sm.b_full);
+                      &sm.b_full[hb]);
       }
       for (int mt = 0; mt < u.ntm && ok; ++mt) {
         const int j0 = u.start + mt * kTcM;
@@ -474,7 +494,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expand_kernel(const __grid_c
       }
     }
   } else if (warp == 1) {  // ----------------------------------- MMA issuer
-    uint32_t nb_ = 0, nv = 0, nt = 0;
+    uint32_t bu0 = 0, bu1 = 0, nv = 0, nt = 0;
+    int bsel = 0;
     for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x) {
       TcEUnit u;
       if (lane == 0) u = tc_eunit(t, g, per_seg);
@@ -485,8 +506,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expand_kernel(const __grid_c
       const int r16 = (r + 15) & ~15;
       const int nkb = (r16 + kTcK - 1) / kTcK;
       const uint32_t idesc = umma_idesc_f16(kTcM, (ncols + 15) & ~15, bf16, true);
-      if (!wait_lane0(&sm.b_full, nb_ & 1)) { ok = false; break; }
-      ++nb_;
+      const bool whole = nkb > kEKBlocks / 2;
+      const int hb = whole ? 0 : bsel;
+      if (!wait_lane0(&sm.b_full[hb], (hb ? bu1 : bu0) & 1)) { ok = false; break; }
+      if (hb) ++bu1; else ++bu0;
+      if (whole) {
+        if (!wait_lane0(&sm.b_full[1], bu1 & 1)) { ok = false; break; }
+        ++bu1;
+      } else {
+        bsel ^= 1;
+      }
+      const int kb0 = hb * (kEKBlocks / 2);
       tc_fence_after();
       for (int mt = 0; mt < ntm && ok; ++mt) {
         const int ab = nt & 1;
@@ -502,7 +532,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expand_kernel(const __grid_c
           if (lane == 0) {
             const int nk = min(kTcK, r16 - kb * kTcK);
             const uint32_t ha = smem_addr(sm.Vhi[vb]), la = smem_addr(sm.Vlo[vb]);
-            const uint32_t ba = smem_addr(sm.B[kb][0]);
+            const uint32_t ba = smem_addr(sm.B[kb0 + kb][0]);
             for (int ks = 0; ks < nk / 16; ++ks) {
               // B is N-major: 64-column atoms kTcK rows apart, 8-row groups 1 KB apart
               const uint64_t bdesc = umma_desc_sw128(ba + ks * 16 * kRowBytes, kTcK * kRowBytes, 1024);
@@ -518,7 +548,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expand_kernel(const __grid_c
         __syncwarp();
       }
       if (!ok) break;
-      if (lane == 0) umma_commit(&sm.b_empty);  // B free once this unit's MMAs are done
+      if (lane == 0) {  // B free once this unit's MMAs are done
+        umma_commit(&sm.b_empty[hb]);
+        if (whole) umma_commit(&sm.b_empty[1]);
+      }
       __syncwarp();
     }
   } else {  // ------------------------------------------------- epilogue (warps 2-5)

@@ -32,6 +32,11 @@ SMALL = {
         name="prefill_ragged", H=512, dtype="f16", projections=workloads._qkvo(512),
         num_adapters=11, rank_set=(8, 16, 128), kind="prefill", requests=9, prompt_len=(1, 300),
         pool_factor=1.3, s=-1.25, seed=5),
+    # ranks above 128 take the whole B area of the tensor-core expand kernel
+    "prefill_bigrank_f16": workloads.WorkloadSpec(
+        name="prefill_bigrank", H=256, dtype="f16", projections=workloads._qkvo(256),
+        num_adapters=5, rank_set=(129, 200, 256, 64), kind="prefill", requests=7, prompt_len=(1, 260),
+        pool_factor=1.2, s=0.75, seed=8),
     "many_tokens_f16": workloads.WorkloadSpec(
         name="many_tokens", H=128, dtype="f16", projections=(workloads.Projection("q", 128, 136),),
         num_adapters=300, rank_set=(2, 8, 24), kind="decode", tokens=3001, popularity="uniform",
