@@ -94,7 +94,18 @@ struct Elem<__nv_bfloat16> {
 };
 
 // ================================================================ tc_shrink
+// Warps: 0 loads x tiles (TMA), 1 issues the MMAs, 2-5 drain TMEM, 6-9 copy
+// the adapter's rows.  Adapter rows go through the load/store unit rather
+// than the TMA engine: a K block needs r rows of 128 bytes, and a TMA op per
+// four rows made the copy engine's op rate the limit.  Each loader thread
+// copies one 16-byte chunk column of every 16th row with cp.async, straight
+// to its 128-byte-swizzled place, then (once its copies have landed) fences
+// them for the tensor cores' async proxy and arrives on the stage.
 constexpr int kShrinkTcStages = 4;
+constexpr int kShrinkLoaderWarps = 4;
+constexpr int kShrinkLoaders = kShrinkLoaderWarps * 32;
+constexpr int kShrinkTcThreads = kTcThreads + kShrinkLoaders;
+constexpr int kRowsPerLoader = kMaxRank * (kRowBytes / 16) / kShrinkLoaders;   // rows one loader thread covers
 struct TcShrinkSmem {
   uint8_t X[kShrinkTcStages][kTcM * kRowBytes];     // 128 token rows x 64 K, swizzled (16 KB)
   uint8_t B[kShrinkTcStages][kMaxRank * kRowBytes]; // <= 256 adapter rows x 64 K (32 KB)
@@ -103,8 +114,12 @@ struct TcShrinkSmem {
   int32_t off[kSegSmem];
 };
 
+__device__ __forceinline__ void cp16_shared(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
 template <class E>
-__global__ void __launch_bounds__(kTcThreads, 1) tc_shrink_kernel(const __grid_constant__ TcDev t) {
+__global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __grid_constant__ TcDev t) {
   extern __shared__ uint8_t smem_raw[];
   TcShrinkSmem& sm = *reinterpret_cast<TcShrinkSmem*>(smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023));
   const ApplyDev& d = t.a;
@@ -112,7 +127,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_shrink_kernel(const __grid_c
   if (warp == 1) tmem_alloc(&sm.tmem_slot, 2 * kTcN);
   if (threadIdx.x == 0) {
     for (int s = 0; s < kShrinkTcStages; ++s) {
-      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.full[s], 1 + kShrinkLoaders);   // x bytes (warp 0) + every loader thread
       mbar_init(&sm.empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -160,29 +175,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_shrink_kernel(const __grid_c
       const int n16 = (u.len + 15) >> 4;  // 16-row boxes of a partial run tile
       const uint32_t x_bytes = run ? (u.len == kTcM ? (uint32_t)kTcM * kRowBytes : (uint32_t)n16 * 16 * kRowBytes)
                                    : (uint32_t)(4 * nx4) * kRowBytes;
-      const int32_t* pt = d.page_table + (int64_t)u.a * d.pt_stride + (int64_t)u.r * P.rows_before;
       const int nkb = (P.h_in + kTcK - 1) / kTcK;
-      int chunk = -1;
-      int pg[2][4];
+      (void)nb4;
       for (int kb = 0; kb < nkb; ++kb) {
-        const int k0 = kb * kTcK, c = k0 / d.H, o = k0 - c * d.H;
-        if (c != chunk) {  // page of each adapter row for this page chunk
-          chunk = c;
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int row = 128 * h + 4 * lane + i;
-              pg[h][i] = __ldg(pt + (int64_t)(row < u.r ? row : 0) * P.ppi + c);
-            }
-        }
+        const int k0 = kb * kTcK;
         bool got = true;
         if (lane == 0) got = mbar_wait(&sm.empty[stage], phase ^ 1);
         if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
           ok = false;
           break;
         }
-        if (lane == 0) mbar_expect_tx(&sm.full[stage], x_bytes + (uint32_t)(4 * nb4) * kRowBytes);
+        if (lane == 0) mbar_expect_tx(&sm.full[stage], x_bytes);
         __syncwarp();
         if (!run) {
           if (lane < nx4)
@@ -193,11 +196,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_shrink_kernel(const __grid_c
         } else if (lane < n16) {
           tma_load_2d(&sm.X[stage][16 * lane * kRowBytes], &t.x16_map[u.p], k0, t_first + 16 * lane, &sm.full[stage]);
         }
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          if (32 * h + lane < nb4)
-            tma_gather4(&sm.B[stage][(128 * h + 4 * lane) * kRowBytes], &t.pool_map, o, pg[h][0], pg[h][1],
-                        pg[h][2], pg[h][3], &sm.full[stage]);
         if (++stage == kShrinkTcStages) {
           stage = 0;
           phase ^= 1;
@@ -250,6 +248,62 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_shrink_kernel(const __grid_c
       if (!ok) break;
       if (lane == 0) umma_commit(&sm.tfull[ab]);
       __syncwarp();
+    }
+  } else if (warp >= 6) {  // ------------------------------------ adapter-row loaders
+    const int lt = threadIdx.x - 6 * 32;    // 0 .. kShrinkLoaders - 1
+    const int ch = lt & 7;                  // 16-byte chunk column of the 128-byte row
+    const int row0 = lt >> 3;               // rows row0, row0 + 16, ...
+    uint32_t stage = 0, phase = 0;
+    int pending = -1;                       // stage whose copies are committed, not yet announced
+    for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x) {
+      const int tile = (int)(g / d.nproj);
+      const TcUnit u = tc_tile(t, sm.off, off_smem, S, tile, (int)(g - (int64_t)tile * d.nproj));
+      const ProjDev& P = d.proj[u.p];
+      const int32_t* pt = d.page_table + (int64_t)u.a * d.pt_stride + (int64_t)u.r * P.rows_before;
+      const int nkb = (P.h_in + kTcK - 1) / kTcK;
+      const int nrow = (u.r - row0 + 15) >> 4;   // my rows below r (rows past r are never read back)
+      int chunk = -1;
+      int pg[kRowsPerLoader];
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int k0 = kb * kTcK, c = k0 / d.H, o = k0 - c * d.H;
+        if (c != chunk) {  // pages of my rows for this page chunk
+          chunk = c;
+#pragma unroll
+          for (int j = 0; j < kRowsPerLoader; ++j)
+            pg[j] = j < nrow ? __ldg(pt + (int64_t)(row0 + 16 * j) * P.ppi + c) : 0;
+        }
+        if (!mbar_wait(&sm.empty[stage], phase ^ 1)) {
+          ok = false;
+          break;
+        }
+        const uint32_t base = smem_addr(sm.B[stage]);
+#pragma unroll
+        for (int j = 0; j < kRowsPerLoader; ++j) {
+          if (j < nrow) {
+            const int row = row0 + 16 * j;
+            cp16_shared(base + row * kRowBytes + ((ch ^ (row & 7)) << 4),
+                        d.pool + (int64_t)pg[j] * d.H + o + ch * 8);
+          }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        if (pending >= 0) {
+          // the previous stage's copies have landed: make them visible to the
+          // tensor cores' async proxy, then announce them
+          asm volatile("cp.async.wait_group 1;" ::: "memory");
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          mbar_arrive(&sm.full[pending]);
+        }
+        pending = (int)stage;
+        if (++stage == kShrinkTcStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    if (pending >= 0 && ok) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(&sm.full[pending]);
     }
   } else {  // ------------------------------------------------- epilogue (warps 2-5)
     const int quarter = warp & 3;  // TMEM lanes this warp may read
@@ -612,10 +666,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expand_kernel(const __grid_c
 }
 
 template <typename Kern>
-cudaError_t launch_pdl_tc(Kern kernel, int grid, size_t smem, cudaStream_t st, const TcDev& a) {
+cudaError_t launch_pdl_tc(Kern kernel, int grid, int threads, size_t smem, cudaStream_t st, const TcDev& a) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kTcThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -647,13 +701,13 @@ cudaError_t prepare_tc_kernels() {
 }
 
 cudaError_t launch_tc_shrink(const TcDev& a, int dtype, int grid, cudaStream_t st) {
-  if (dtype == 0) return launch_pdl_tc(tc_shrink_kernel<__half>, grid, kShrinkTcSmem, st, a);
-  return launch_pdl_tc(tc_shrink_kernel<__nv_bfloat16>, grid, kShrinkTcSmem, st, a);
+  if (dtype == 0) return launch_pdl_tc(tc_shrink_kernel<__half>, grid, kShrinkTcThreads, kShrinkTcSmem, st, a);
+  return launch_pdl_tc(tc_shrink_kernel<__nv_bfloat16>, grid, kShrinkTcThreads, kShrinkTcSmem, st, a);
 }
 
 cudaError_t launch_tc_expand(const TcDev& a, int dtype, int grid, cudaStream_t st) {
-  if (dtype == 0) return launch_pdl_tc(tc_expand_kernel<__half>, grid, kExpandTcSmem, st, a);
-  return launch_pdl_tc(tc_expand_kernel<__nv_bfloat16>, grid, kExpandTcSmem, st, a);
+  if (dtype == 0) return launch_pdl_tc(tc_expand_kernel<__half>, grid, kTcThreads, kExpandTcSmem, st, a);
+  return launch_pdl_tc(tc_expand_kernel<__nv_bfloat16>, grid, kTcThreads, kExpandTcSmem, st, a);
 }
 
 int32_t tc_col_tiles(int32_t h_out, int32_t H) {
