@@ -325,14 +325,20 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
       float* vrow = d.proj[u.p].v + (int64_t)j * d.v_ld;
       uint16_t* hrow = t.vhi[u.p] + (int64_t)j * t.v16_ld;
       uint16_t* lrow = t.vlo[u.p] + (int64_t)j * t.v16_ld;
-      for (int c0 = 0; c0 < r16; c0 += 16) {
-        float v[16];
-        tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(ab * kTcN + c0), v);
-        if (m < u.len) {
+      // 32 accumulator columns per TMEM round trip
+      for (int c00 = 0; c00 < r16; c00 += 32) {
+        uint32_t raw[32];
+        tmem_ld32_nowait(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(ab * kTcN + c00), raw);
+        tmem_wait_ld(raw);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+        const int c0 = c00 + 16 * hh;
+        if (m < u.len && c0 < r16) {
+          float v[16];
           uint16_t hi[16], lo[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float x = c0 + i < u.r ? v[i] : 0.f;
+            const float x = c0 + i < u.r ? __uint_as_float(raw[16 * hh + i]) : 0.f;
             v[i] = x;
             hi[i] = Elem<E>::from(x);
             lo[i] = Elem<E>::from(x - Elem<E>::to(hi[i]));
@@ -351,6 +357,7 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
           *reinterpret_cast<uint4*>(hrow + c0 + 8) = h1;
           *reinterpret_cast<uint4*>(lrow + c0) = l0;
           *reinterpret_cast<uint4*>(lrow + c0 + 8) = l1;
+        }
         }
       }
       tc_fence_before();
@@ -381,12 +388,16 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
 constexpr int kTcNe = 128;                        // expand column tile
 constexpr int kEAtoms = kTcNe / 64;               // 64-column swizzle atoms per tile
 constexpr int kEKBlocks = kMaxRank / kTcK;        // B row blocks of 64 ranks
+constexpr int kEBufs = 3;                         // y tiles and TMEM accumulators in flight
+constexpr int kETmemCols = 512;                   // power of two >= kEBufs * kTcNe
+static_assert(kEBufs * kTcNe <= kETmemCols, "accumulators must fit the TMEM allocation");
 struct TcExpandSmem {
   uint8_t B[kEKBlocks][kEAtoms][kTcK * kRowBytes];   // <= 256 rank rows x 128 columns, N-major (64 KB)
   uint8_t Vhi[2][kTcM * kRowBytes];                  // 128 tokens x 64 ranks (16 KB)
   uint8_t Vlo[2][kTcM * kRowBytes];
-  uint8_t Y[2][kEAtoms][kTcM * kRowBytes];           // 128 tokens x 128 columns (32 KB)
-  uint64_t b_full[2], b_empty[2], v_full[2], v_empty[2], y_full[2], y_empty[2], tfull[2], tempty[2];
+  uint8_t Y[kEBufs][kEAtoms][kTcM * kRowBytes];      // 128 tokens x 128 columns (32 KB)
+  uint64_t b_full[2], b_empty[2], v_full[2], v_empty[2];
+  uint64_t y_full[kEBufs], y_empty[kEBufs], tfull[kEBufs], tempty[kEBufs], epi_done[kEBufs];
   uint32_t tmem_slot;
 };
 
@@ -427,15 +438,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expand_kernel(const __grid_c
   TcExpandSmem& sm = *reinterpret_cast<TcExpandSmem*>(smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023));
   const ApplyDev& d = t.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp == 1) tmem_alloc(&sm.tmem_slot, 2 * kTcNe);
+  if (warp == 1) tmem_alloc(&sm.tmem_slot, kETmemCols);
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.b_full[b], 1);
       mbar_init(&sm.b_empty[b], 1);
       mbar_init(&sm.v_full[b], 1);
       mbar_init(&sm.v_empty[b], 1);
+    }
+    for (int b = 0; b < kEBufs; ++b) {
       mbar_init(&sm.y_full[b], 1);
-      mbar_init(&sm.y_empty[b], 4);
+      mbar_init(&sm.y_empty[b], 1);   // epilogue warp 2 lane 0, after the four warps are done
+      mbar_init(&sm.epi_done[b], 4);  // each epilogue warp, done with the y tile
       mbar_init(&sm.tfull[b], 1);
       mbar_init(&sm.tempty[b], 4);
     }
@@ -515,8 +529,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expand_kernel(const __grid_c
         const bool run = __ldg(d.perm + j0 + len - 1) - t_first == len - 1;
         const int n16 = (len + 15) >> 4, nx4 = (len + 3) >> 2;
         // y tile
-        const int yb = ny & 1;
-        if (!wait_lane0(&sm.y_empty[yb], ((ny >> 1) & 1) ^ 1)) { ok = false; break; }
+        const int yb = (int)(ny % kEBufs);
+        if (!wait_lane0(&sm.y_empty[yb], ((ny / kEBufs) & 1) ^ 1)) { ok = false; break; }
         ++ny;
         const uint32_t ybytes = (uint32_t)natoms * (run ? (len == kTcM ? kTcM : 16 * n16) : 4 * nx4) * kRowBytes;
         if (lane == 0) mbar_expect_tx(&sm.y_full[yb], ybytes);
@@ -573,8 +587,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expand_kernel(const __grid_c
       const int kb0 = hb * (kEKBlocks / 2);
       tc_fence_after();
       for (int mt = 0; mt < ntm && ok; ++mt) {
-        const int ab = nt & 1;
-        if (!wait_lane0(&sm.tempty[ab], ((nt >> 1) & 1) ^ 1)) { ok = false; break; }
+        const int ab = (int)(nt % kEBufs);
+        if (!wait_lane0(&sm.tempty[ab], ((nt / kEBufs) & 1) ^ 1)) { ok = false; break; }
         ++nt;
         tc_fence_after();
         const uint32_t dtm = tmem + (uint32_t)(ab * kTcNe);
@@ -609,6 +623,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expand_kernel(const __grid_c
       __syncwarp();
     }
   } else {  // ------------------------------------------------- epilogue (warps 2-5)
+    // Per token tile: 64 accumulator columns per TMEM round trip; the TMEM
+    // buffer is released as soon as it has been read.  A tile of 128
+    // consecutive tokens and 128 columns (the common prefill case) is written
+    // back into its y tile in shared memory and stored by the TMA engine in
+    // whole 128-byte rows; other tiles store their 16-byte pieces directly.
     const int quarter = warp & 3;
     const int m = 32 * quarter + lane;
     uint32_t nt = 0;
@@ -617,51 +636,87 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expand_kernel(const __grid_c
       if (u.ntm == 0) continue;
       const ProjDev& P = d.proj[u.p];
       const int col0 = u.c * d.H + u.o;
+      const int natoms = (u.ncols + 63) >> 6;
       for (int mt = 0; mt < u.ntm && ok; ++mt) {
         const int j0 = u.start + mt * kTcM;
         const int len = min(kTcM, u.start + u.len - j0);
         const int token = m < len ? __ldg(d.perm + j0 + m) : 0;
-        const int ab = nt & 1;
-        if (!wait_lane0(&sm.tfull[ab], (nt >> 1) & 1) || !wait_lane0(&sm.y_full[ab], (nt >> 1) & 1)) {
+        const int t_first = __ldg(d.perm + j0);
+        const bool tma_out =
+            len == kTcM && u.ncols == kTcNe && __ldg(d.perm + j0 + kTcM - 1) - t_first == kTcM - 1;
+        const int ab = (int)(nt % kEBufs);
+        const uint32_t ph = (nt / kEBufs) & 1;
+        if (!wait_lane0(&sm.tfull[ab], ph) || !wait_lane0(&sm.y_full[ab], ph)) {
           ok = false;
           break;
         }
         ++nt;
         tc_fence_after();
         uint16_t* yrow = static_cast<uint16_t*>(P.y) + (int64_t)token * P.ldy + col0;
-        for (int c0 = 0; c0 < u.ncols; c0 += 16) {
-          float acc[16];
-          tmem_ld16(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(ab * kTcNe + c0), acc);
+        for (int at = 0; at < natoms; ++at) {
+          uint32_t r0[32], r1[32];
+          const uint32_t ta = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(ab * kTcNe + 64 * at);
+          tmem_ld32_nowait(ta, r0);
+          tmem_ld32_nowait(ta + 32, r1);
+          tmem_wait_ld(r0);
+          tmem_wait_ld(r1);
+          if (at == natoms - 1) {  // this warp is done with the TMEM buffer
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.tempty[ab]);
+          }
           if (m < len) {
-            const int nv8 = min(2, (u.ncols - c0) >> 3);
-            const uint8_t* ytile = sm.Y[ab][c0 >> 6] + m * kRowBytes;
-            for (int h = 0; h < nv8; ++h) {
-              const int chunk = ((c0 & 63) >> 3) + h;  // 16-byte chunk of the 128-byte row, swizzled
-              uint4 yv = *reinterpret_cast<const uint4*>(ytile + ((chunk ^ (m & 7)) << 4));
-              uint16_t e[8];
-              memcpy(e, &yv, 16);
+            uint8_t* ytile = sm.Y[ab][at] + m * kRowBytes;
+            const int nch = min(8, (u.ncols - 64 * at) >> 3);   // 8-column chunks in this atom
 #pragma unroll
-              for (int i = 0; i < 8; ++i) e[i] = Elem<E>::from(Elem<E>::to(e[i]) + d.s * acc[8 * h + i]);
-              memcpy(&yv, e, 16);
-              *reinterpret_cast<uint4*>(yrow + c0 + 8 * h) = yv;
+            for (int h = 0; h < 8; ++h) {
+              if (h < nch) {
+                uint8_t* py = ytile + ((h ^ (m & 7)) << 4);   // swizzled 16-byte chunk
+                uint4 yv = *reinterpret_cast<const uint4*>(py);
+                uint16_t e[8];
+                memcpy(e, &yv, 16);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const uint32_t bits = h < 4 ? r0[8 * h + i] : r1[8 * (h - 4) + i];
+                  e[i] = Elem<E>::from(Elem<E>::to(e[i]) + d.s * __uint_as_float(bits));
+                }
+                memcpy(&yv, e, 16);
+                if (tma_out) *reinterpret_cast<uint4*>(py) = yv;
+                else *reinterpret_cast<uint4*>(yrow + 64 * at + 8 * h) = yv;
+              }
             }
           }
         }
-        tc_fence_before();
+        if (tma_out) fence_async_shared();   // the tile's new values, for the TMA engine
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&sm.tempty[ab]);
-          mbar_arrive(&sm.y_empty[ab]);
+        if (lane == 0) mbar_arrive(&sm.epi_done[ab]);
+        if (warp == 2 && lane == 0) {
+          // once the four warps are done with the y tile: store it (TMA) or
+          // just hand it back to the producer
+          if (!mbar_wait(&sm.epi_done[ab], ph)) {
+            ok = false;
+          } else {
+            if (tma_out) {
+#pragma unroll
+              for (int at = 0; at < kEAtoms; ++at)
+                tma_store_2d(&t.y128_map[u.p], col0 + 64 * at, t_first, sm.Y[ab][at]);
+              bulk_commit();
+              bulk_wait_read();   // the y tile may be refilled once the stores have read it
+            }
+            mbar_arrive(&sm.y_empty[ab]);
+          }
         }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       }
     }
+    if (warp == 2 && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");   // stores complete
   }
   if (!ok && lane == 0) report_err(d.error, kErrTimeout);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 2 * kTcNe);
+    tmem_dealloc(tmem, kETmemCols);
   }
 }
 
