@@ -31,7 +31,8 @@ def lib():
             ctypes.c_int32, P, P, ctypes.c_int32,          # num_proj, proj_in, proj_out, p
             P, ctypes.c_int32, P, ctypes.c_int32,          # token_adapter, T, tokens, n_tokens
             P, ctypes.c_int64, P, ctypes.c_int64,          # x, ldx, y_in, ldy
-            ctypes.c_double, P, P, P, ctypes.c_int64,      # s, y_out, y_exact, v_out, v_ld
+            ctypes.c_double, P,                            # s, adapter_scale (fp64 per adapter id, or NULL)
+            P, P, P, ctypes.c_int64,                       # y_out, y_exact, v_out, v_ld
             ctypes.c_int32]                                # num_threads
         L.oracle_decode_array.argtypes = [P, P, ctypes.c_int64, ctypes.c_int32]
         L.oracle_encode_array.argtypes = [P, P, ctypes.c_int64, ctypes.c_int32]
@@ -70,8 +71,11 @@ def max_threads() -> int:
 
 def apply(store, pool, p: int, token_adapter: np.ndarray, x: np.ndarray, y_in: np.ndarray,
           s: float, dtype: str, tokens: Optional[Sequence[int]] = None, want_exact: bool = False,
-          want_v: bool = False, num_threads: int = 1):
-    """Oracle of y_out = round(y_in + s (x A) B) for projection p.
+          want_v: bool = False, num_threads: int = 1, adapter_scale: Optional[np.ndarray] = None):
+    """Oracle of y_out = round(y_in + s s_a (x A) B) for projection p.
+
+    adapter_scale: s_a per adapter id (float64, max_adapters entries), or None
+    for s_a = 1 everywhere.
 
     store: oracle.pool.OracleStore with the touched adapters' pages written.
     pool:  oracle.pool.OraclePool whose page tables address those pages.
@@ -94,13 +98,17 @@ def apply(store, pool, p: int, token_adapter: np.ndarray, x: np.ndarray, y_in: n
     proj_in = np.asarray([d.h_in for d in dims], dtype=np.int32)
     proj_out = np.asarray([d.h_out for d in dims], dtype=np.int32)
     rank = np.ascontiguousarray(pool.rank, dtype=np.int32)
+    sc = None
+    if adapter_scale is not None:
+        sc = np.ascontiguousarray(adapter_scale, dtype=np.float64)
+        assert sc.shape == (pool.max_adapters,)
     rc = lib().oracle_lora_apply(
         _ptr(store.data), _ptr(store.page_slot), pool.H, dtype_code(dtype),
         _ptr(pt), _ptr(pt_off), _ptr(rank), pool.max_adapters,
         len(dims), _ptr(proj_in), _ptr(proj_out), p,
         _ptr(ta), T, _ptr(tok), 0 if tok is None else tok.shape[0],
         _ptr(x), h_in, _ptr(y_in), h_out,
-        float(s), _ptr(y_out), _ptr(y_exact), _ptr(v), v_ld, int(num_threads))
+        float(s), _ptr(sc), _ptr(y_out), _ptr(y_exact), _ptr(v), v_ld, int(num_threads))
     if rc != 0:
         raise ValueError("oracle: a token names an adapter that is not resident")
     return y_out, y_exact, v

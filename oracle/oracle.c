@@ -11,9 +11,10 @@
  * and the adapter weights sit in non-contiguous pages of one pool shared with
  * the KV cache; dongaigc.com summary, section 2 "heterogeneous batching"):
  *
- *     y_out[i, n] = round( y_in[i, n] + s * sum_k ( sum_c x[i, c] A_a[c, k] ) B_a[k, n] )
+ *     y_out[i, n] = round( y_in[i, n] + s * s_a * sum_k ( sum_c x[i, c] A_a[c, k] ) B_a[k, n] )
  *
- * for every token i whose adapter a = a(i) is >= 0; tokens with a(i) = -1 are
+ * where s_a is adapter a's own scale (LoRA's alpha / r; 1 when no per-adapter
+ * scales are given), for every token i whose adapter a = a(i) is >= 0; tokens with a(i) = -1 are
  * copied unchanged.  All arithmetic is fp64 on the exact values of the 16-bit
  * inputs, and round() is one IEEE round-to-nearest-even into the storage
  * type.  A and B are never dense here: every element is fetched through the
@@ -145,7 +146,7 @@ int oracle_lora_apply(const uint16_t* pool, const int64_t* page_slot, int32_t H,
                       int32_t num_adapters, int32_t num_proj, const int32_t* proj_in,
                       const int32_t* proj_out, int32_t p, const int32_t* token_adapter, int32_t T,
                       const int32_t* tokens, int32_t n_tokens, const uint16_t* x, int64_t ldx,
-                      const uint16_t* y_in, int64_t ldy, double s, uint16_t* y_out,
+                      const uint16_t* y_in, int64_t ldy, double s, const double* adapter_scale, uint16_t* y_out,
                       double* y_exact, double* v_out, int64_t v_ld, int32_t num_threads) {
   int64_t rows_before = 0;               /* page chunks of one rank index in projections < p */
   for (int q = 0; q < p; q++) rows_before += ceil_div(proj_in[q], H) + ceil_div(proj_out[q], H);
@@ -189,7 +190,7 @@ int oracle_lora_apply(const uint16_t* pool, const int64_t* page_slot, int32_t H,
       double acc = 0.0;
       for (int64_t k = 0; k < r; k++)
         acc += v[k] * decode(*row_elem(pool, page_slot, H, page_table, b_base + k * ppo, c), dtype);
-      double y = decode(yi[c], dtype) + s * acc;
+      double y = decode(yi[c], dtype) + s * (adapter_scale ? adapter_scale[a] : 1.0) * acc;
       if (y_exact) y_exact[(int64_t)i * ldy + c] = y;
       yo[c] = encode(y, dtype);
     }

@@ -230,6 +230,38 @@ def test_linear_in_s():
     assert np.abs(d1).max() > 0.1
 
 
+def test_per_adapter_scale_against_dense_brute_force():
+    """y = y_in + s s_a (x A_a) B_a: each adapter's tokens against numpy's
+    dense product with that adapter's own factor; s_a = 1 everywhere gives
+    exactly the unscaled result, s_a = 0 leaves the adapter's tokens alone."""
+    sp = SMALL_SPECS[1]
+    wl = workloads.make(sp)
+    pool = H.oracle_pool_for(wl)
+    adapters = H.touched(wl.token_adapter)
+    store = H.oracle_store_for(wl, pool, adapters)
+    scale = np.ones(pool.max_adapters)
+    rng = np.random.default_rng(4)
+    scale[adapters] = rng.uniform(-2.0, 2.0, len(adapters))
+    scale[adapters[0]] = 0.0
+    for p in range(len(wl.projections)):
+        x, y = wl.x(p), wl.y_in(p)
+        X, Y = H.lib_values(x, sp.dtype), H.lib_values(y, sp.dtype)
+        dense = H.dense_weights(wl, adapters, p)
+        y_out, e, _ = olora.apply(store, pool, p, wl.token_adapter, x, y, sp.s, sp.dtype, want_exact=True,
+                                  adapter_scale=scale)
+        for a in adapters:
+            only_a = np.where(wl.token_adapter == a, a, -1).astype(np.int32)
+            want = ref.brute_force(only_a, X, Y, {a: dense[a]}, sp.s * scale[a])
+            rows = wl.token_adapter == a
+            assert np.allclose(e[rows], want[rows], rtol=1e-12, atol=1e-12)
+        rows0 = wl.token_adapter == adapters[0]
+        assert np.array_equal(y_out[rows0], y[rows0])
+        ones = olora.apply(store, pool, p, wl.token_adapter, x, y, sp.s, sp.dtype, want_exact=True,
+                           adapter_scale=np.ones(pool.max_adapters))[1]
+        plain = olora.apply(store, pool, p, wl.token_adapter, x, y, sp.s, sp.dtype, want_exact=True)[1]
+        assert np.array_equal(ones, plain)
+
+
 def test_base_only_tokens_unchanged():
     wl, pool = _tiny_state()
     store = H.oracle_store_for(wl, pool, range(4))
