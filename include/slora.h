@@ -177,6 +177,17 @@ int slora_adapter_load(slora_pool* pool, int32_t adapter_id, int32_t rank,
  */
 int slora_adapter_evict(slora_pool* pool, int32_t adapter_id);
 
+/*
+ * Per-adapter scale s_a (LoRA's alpha / r): applies compute
+ *     y += s * s_a * (x A_a) B_a
+ * for tokens of adapter a.  A load sets s_a = 1; this call changes it for
+ * applies queued on the compute stream after it (it waits for the adapter's
+ * own pending load first).  Errors: SLORA_ERR_NOT_RESIDENT for an adapter
+ * that is not loaded, SLORA_ERR_INVALID for a scale that is not finite, and
+ * for a planning pool (no device state).
+ */
+int slora_adapter_set_scale(slora_pool* pool, int32_t adapter_id, float scale);
+
 /* Host copy of an adapter's page table (page-table order above); *n = entries. */
 int slora_adapter_pages(const slora_pool* pool, int32_t adapter_id, int32_t* out_pages,
                         int64_t capacity, int64_t* n);

@@ -114,6 +114,7 @@ struct ApplyDev {
   float s;
   int32_t* error;                // first device error (0 = none)
   const int4* seg_desc;          // per work-order position: {adapter, rank, start, end}
+  const float* scale;            // per adapter id: s_a, applied to v (NULL: 1 for every adapter)
   // The grid barrier between the apply kernel's shrink and expand phases:
   // [kSyncCount] CTAs arrived (back to 0 when the last arrives; the segment
   // kernel also zeroes it), [kSyncGen] generation (incremented when the
@@ -174,6 +175,8 @@ cudaError_t launch_build_segments(const SegBuildArgs& a, cudaStream_t st);
 // every CTA resident at once.
 cudaError_t launch_apply_cc(const ApplyDev& a, int dtype, int grid, cudaStream_t st);
 cudaError_t launch_scatter(const ScatterDev& a, cudaStream_t st);
+// *p = v, ordered on the stream (one thread).
+cudaError_t launch_set_f32(float* p, float v, cudaStream_t st);
 cudaError_t prepare_kernels(int device);   // opt-in shared memory sizes
 // Tensor-core kernels (tc_kernels.cu); the page size must be a multiple of kTcK.
 cudaError_t prepare_tc_kernels();

@@ -564,6 +564,7 @@ enum : int { kKindShrink = 0, kKindExpand = 1 };
 struct __align__(16) StageMeta {
   int kind, ntok, p, len, last;
   int j0, k0, nrows;                // shrink
+  float sa;                         // shrink: the adapter's scale, applied to v
   int col0, nk, buf, vph;           // expand (k0 = first B row of the stage)
   int rows[kTT];
 };
@@ -801,6 +802,7 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
       const int64_t gl = snake_unit(i0 + lane);   // lane l resolves this CTA's unit i0 + l
       const int nb = (int)min((int64_t)32, ns - i0);
       int m_p = 0, m_j0 = 0, m_ntok = 0, m_k0 = 0, m_nrows = 0, m_r = 0, m_a = 0;
+      float m_sa = 1.f;
       int pg[kShrinkRows], xt[kTT];
 #pragma unroll
       for (int i = 0; i < kShrinkRows; ++i) pg[i] = 0;
@@ -814,6 +816,7 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
         const int4 sd = __ldg(d.seg_desc + q);   // adapter, rank, start, end
         m_a = sd.x;
         m_r = sd.y;
+        if (d.scale) m_sa = __ldg(d.scale + m_a);
         const int nrc = (m_r + kShrinkRows - 1) / kShrinkRows;
         const int tt = local / nrc, rc = local - tt * nrc;
         m_j0 = sd.z + tt * kTT;
@@ -838,6 +841,7 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
         const int nrows = __shfl_sync(0xffffffffu, m_nrows, l);
         const int r = __shfl_sync(0xffffffffu, m_r, l);
         const int a = __shfl_sync(0xffffffffu, m_a, l);
+        const float sa = __shfl_sync(0xffffffffu, m_sa, l);
         // lane i < nrows holds A row k0 + i's page, lane 8 + t token t of the tile
         int my = 0;
 #pragma unroll
@@ -876,6 +880,7 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
               m.j0 = j0;
               m.k0 = k0;
               m.nrows = nrows;
+              m.sa = sa;
               mbar_expect_tx(&sm.full[stage], (uint32_t)(nrows + ntok) * (uint32_t)len * 2u);
             }
             __syncwarp();
@@ -1036,6 +1041,7 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
         const StageMeta& ms = sm.meta[stage];
         const int ntok = ms.ntok, len = ms.len, nrows = ms.nrows, last = ms.last;
         const int p = ms.p, j0 = ms.j0, k0 = ms.k0;
+        const float sa = ms.sa;
         if (warp < nrows) {
           float accs[kTT];
 #pragma unroll
@@ -1071,7 +1077,7 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
               float* vrow = d.proj[p].v + (int64_t)j0 * d.v_ld + k0 + warp;
 #pragma unroll
               for (int t = 0; t < kTT; ++t)
-                if (t < ntok) vrow[(int64_t)t * d.v_ld] = tot[t];
+                if (t < ntok) vrow[(int64_t)t * d.v_ld] = sa * tot[t];
             }
           }
           break;
@@ -1154,6 +1160,9 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
     if (!ok && lane == 0) report(d.error, kErrTimeout);
   }
 }
+
+// ---- per-adapter scale: one value, ordered on a stream -------------------------
+__global__ void set_f32_kernel(float* p, float v) { *p = v; }
 
 // ---- adapter load: staging -> pages ---------------------------------------------
 // One CTA per page-table entry: copies that row chunk (<= H elements) from the
@@ -1248,6 +1257,11 @@ cudaError_t launch_build_segments(const SegBuildArgs& in, cudaStream_t st) {
 cudaError_t launch_apply_cc(const ApplyDev& a, int dtype, int grid, cudaStream_t st) {
   if (dtype == 0) return launch_pdl(apply_cc_kernel<F16>, grid, kCcThreads, sizeof(ApplySmem), st, a, true);
   return launch_pdl(apply_cc_kernel<BF16>, grid, kCcThreads, sizeof(ApplySmem), st, a, true);
+}
+
+cudaError_t launch_set_f32(float* p, float v, cudaStream_t st) {
+  set_f32_kernel<<<1, 1, 0, st>>>(p, v);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_scatter(const ScatterDev& a, cudaStream_t st) {

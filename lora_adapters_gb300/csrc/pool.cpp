@@ -16,6 +16,7 @@
 
 #include <algorithm>
 #include <climits>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -90,6 +91,7 @@ struct slora_pool {
   int device = 0;
   int32_t* d_pt = nullptr;
   int32_t* d_rank = nullptr;
+  float* d_scale = nullptr;              // per adapter: s_a (1 after a load)
   int32_t* d_error = nullptr;
   int32_t* d_seg_mem = nullptr;
   SegDev seg{};
@@ -279,6 +281,7 @@ void free_device(slora_pool* p) {
   if (p->order_event) cudaEventDestroy(p->order_event);
   cudaFree(p->d_pt);
   cudaFree(p->d_rank);
+  cudaFree(p->d_scale);
   cudaFree(p->d_error);
   cudaFree(p->d_seg_mem);
   cudaFree(p->d_v);
@@ -383,6 +386,11 @@ int slora_pool_create(slora_pool** out, void* d_pool, int64_t num_pages, int32_t
     std::fill(p->rank_pin, p->rank_pin + max_adapters, 0);
     CUDA_TRY(cudaMalloc(&p->d_pt, sizeof(int32_t) * (size_t)pt_entries));
     CUDA_TRY(cudaMalloc(&p->d_rank, sizeof(int32_t) * (size_t)max_adapters));
+    CUDA_TRY(cudaMalloc(&p->d_scale, sizeof(float) * (size_t)max_adapters));
+    {
+      const std::vector<float> ones((size_t)max_adapters, 1.0f);
+      CUDA_TRY(cudaMemcpy(p->d_scale, ones.data(), sizeof(float) * (size_t)max_adapters, cudaMemcpyHostToDevice));
+    }
     CUDA_TRY(cudaMalloc(&p->d_error, sizeof(int32_t)));
     // segment arrays: per-position descriptors (16-byte aligned, first),
     // counts, perm, seg_start, seg_adapter, seg_rank, seg_order, 6 prefix arrays
@@ -583,6 +591,7 @@ int slora_adapter_load(slora_pool* p, int32_t a, int32_t rank, const void* const
       CUDA_TRY(launch_scatter(sd, p->copy));
       tm.done();
     }
+    CUDA_TRY(launch_set_f32(p->d_scale + a, 1.0f, p->copy));   // a fresh adapter: s_a = 1
     CUDA_TRY(cudaMemcpyAsync(p->d_rank + a, p->rank_pin + a, sizeof(int32_t), cudaMemcpyHostToDevice,
                              p->copy));
     CUDA_TRY(cudaEventRecord(p->load_event[a], p->copy));
@@ -612,6 +621,17 @@ int slora_adapter_evict(slora_pool* p, int32_t a) {
   // Segment handles carry the ranks seen when they were built; a reload of
   // this id with another rank would make them index the wrong entries.
   p->seg_generation++;
+  return SLORA_OK;
+}
+
+int slora_adapter_set_scale(slora_pool* p, int32_t a, float scale) {
+  if (int rc = check_device_pool(p)) return rc;
+  if (a < 0 || a >= p->max_adapters || p->rank_h[a] == 0)
+    return fail(SLORA_ERR_NOT_RESIDENT, "adapter %d is not resident", a);
+  if (!std::isfinite(scale)) return fail(SLORA_ERR_INVALID, "scale of adapter %d is not finite", a);
+  // after the adapter's own load (which sets s_a = 1), before later applies
+  if (p->load_pending[a]) CUDA_TRY(cudaStreamWaitEvent(p->compute, p->load_event[a], 0));
+  CUDA_TRY(launch_set_f32(p->d_scale + a, scale, p->compute));
   return SLORA_OK;
 }
 
@@ -686,6 +706,7 @@ int slora_lora_apply_multi(slora_pool* p, const slora_segments* seg, int32_t n, 
   d.error = p->d_error;
   d.grid_sync = p->d_grid_sync;
   d.seg_desc = p->seg.seg_desc;
+  d.scale = p->d_scale;
   d.off_n = std::min<int32_t>(kSegSmem, std::max(1, std::min(p->seg_T, p->max_adapters)) + 1);
   d.s = s;
   for (int i = 0; i < n; ++i) {

@@ -322,6 +322,7 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
       }
       tc_fence_after();
       const int j = u.j0 + m;
+      const float sa = d.scale ? __ldg(d.scale + u.a) : 1.f;   // the adapter's scale, applied to v
       float* vrow = d.proj[u.p].v + (int64_t)j * d.v_ld;
       uint16_t* hrow = t.vhi[u.p] + (int64_t)j * t.v16_ld;
       uint16_t* lrow = t.vlo[u.p] + (int64_t)j * t.v16_ld;
@@ -338,7 +339,7 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
           uint16_t hi[16], lo[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float x = c0 + i < u.r ? __uint_as_float(raw[16 * hh + i]) : 0.f;
+            const float x = c0 + i < u.r ? sa * __uint_as_float(raw[16 * hh + i]) : 0.f;
             v[i] = x;
             hi[i] = Elem<E>::from(x);
             lo[i] = Elem<E>::from(x - Elem<E>::to(hi[i]));

@@ -36,7 +36,7 @@ EXPORTED = (
     "slora_pool_info", "slora_adapter_load", "slora_adapter_evict", "slora_adapter_pages",
     "slora_build_segments", "slora_lora_apply", "slora_lora_apply_multi", "slora_device_status",
     "slora_pool_snapshot", "slora_timing_enable", "slora_timing_read", "slora_set_tc_threshold",
-    "slora_last_error_string", "slora_lora_apply_noalloc",
+    "slora_last_error_string", "slora_lora_apply_noalloc", "slora_adapter_set_scale",
 )
 
 
@@ -64,6 +64,7 @@ _SIGS = {
     "slora_pool_info": [P, P, P, P, P],
     "slora_adapter_load": [P, I32, I32, P, P, ctypes.POINTER(P)],
     "slora_adapter_evict": [P, I32],
+    "slora_adapter_set_scale": [P, I32, ctypes.c_float],
     "slora_adapter_pages": [P, I32, P, I64, P],
     "slora_build_segments": [P, P, I32, ctypes.POINTER(slora_segments)],
     "slora_lora_apply": [P, ctypes.POINTER(slora_segments), I32, P, I64, P, I64, ctypes.c_float, I32],
@@ -158,6 +159,10 @@ def slora_adapter_load(pool: int, adapter_id: int, rank: int, h_A: Optional[Sequ
 
 def slora_adapter_evict(pool: int, adapter_id: int) -> None:
     _check(lib().slora_adapter_evict(pool, adapter_id), "slora_adapter_evict")
+
+
+def slora_adapter_set_scale(pool: int, adapter_id: int, scale: float) -> None:
+    _check(lib().slora_adapter_set_scale(pool, adapter_id, float(scale)), "slora_adapter_set_scale")
 
 
 def slora_adapter_pages(pool: int, adapter_id: int) -> np.ndarray:
@@ -310,6 +315,9 @@ class Pool:
             addrs.append(base + off)
             self._arena_off = off + a.nbytes
         return slora_adapter_load(self.handle, adapter_id, rank, addrs[0::2], addrs[1::2])
+
+    def set_scale(self, adapter_id: int, scale: float) -> None:
+        slora_adapter_set_scale(self.handle, adapter_id, scale)
 
     def sync_loads(self):
         if self.buffer is not None:

@@ -76,15 +76,16 @@ def build_case(wl: workloads.Workload, weights: str = "all", max_tokens: Optiona
     return GpuCase(wl, pool, ta, xs, ys, opool_, touched)
 
 
-def oracle_outputs(case: GpuCase, tokens=None, threads=None) -> Dict[int, np.ndarray]:
-    """Oracle y_out (16-bit patterns) per projection, for `tokens` (all if None)."""
+def oracle_outputs(case: GpuCase, tokens=None, threads=None, adapter_scale=None) -> Dict[int, np.ndarray]:
+    """Oracle y_out (16-bit patterns) per projection, for `tokens` (all if None);
+    adapter_scale: s_a per adapter id (float64) or None."""
     wl = case.wl
     store = H.oracle_store_for(wl, case.oracle_pool, case.touched)
     out = {}
     for p in range(len(wl.projections)):
         y_out, _, _ = olora.apply(store, case.oracle_pool, p, wl.token_adapter, wl.x(p), wl.y_in(p),
                                   wl.spec.s, wl.spec.dtype, tokens=tokens,
-                                  num_threads=threads or olora.default_threads())
+                                  num_threads=threads or olora.default_threads(), adapter_scale=adapter_scale)
         out[p] = y_out
     return out
 

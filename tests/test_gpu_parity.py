@@ -213,6 +213,42 @@ def test_evict_and_reload_into_other_pages_gives_identical_y():
     case.pool.close()
 
 
+@pytest.mark.parametrize("name", ["tiny", "mlp_ragged_bf16", "prefill_ragged_f16"])
+def test_per_adapter_scale(name):
+    """y += s s_a (x A_a) B_a with a scale per adapter, on both kernel paths;
+    a reload starts from s_a = 1 again."""
+    wl = workloads.make(SMALL[name])
+    case = G.build_case(wl)
+    rng = np.random.default_rng(17)
+    scale = np.ones(case.oracle_pool.max_adapters)
+    for a in case.touched:
+        scale[a] = float(np.float32(rng.uniform(-1.5, 2.5)))
+        case.pool.set_scale(a, scale[a])
+    scale[case.touched[0]] = 0.0
+    case.pool.set_scale(case.touched[0], 0.0)
+    want = G.oracle_outputs(case, adapter_scale=scale)
+    for mode in MODES:
+        _run_and_check(case, mode, want)
+    slora.slora_set_tc_threshold(case.pool.handle, 0)
+    _run_and_check(case, slora.MODE_AUTO, want)
+    # evict + reload: the adapter's scale is 1 again (page placement does not
+    # change the result)
+    a = case.touched[-1]
+    slora.slora_adapter_evict(case.pool.handle, a)
+    case.pool.load(a, int(wl.ranks[a]), wl.adapter(a))
+    case.pool.sync_loads()
+    scale[a] = 1.0
+    _run_and_check(case, slora.MODE_DECODE, G.oracle_outputs(case, adapter_scale=scale))
+    # errors: not resident, not finite
+    with pytest.raises(slora.SloraError) as e:
+        case.pool.set_scale(-1, 1.0)
+    assert e.value.code == slora.ERR_NOT_RESIDENT
+    with pytest.raises(slora.SloraError) as e:
+        case.pool.set_scale(case.touched[0], float("nan"))
+    assert e.value.code == slora.ERR_INVALID
+    case.pool.close()
+
+
 def test_timing_hooks_count_launches():
     wl = workloads.make("tiny")
     case = G.build_case(wl)
