@@ -1,0 +1,60 @@
+"""CPU tests of the serving-trace driver on a planning pool (no GPU work).
+
+The driver's log of pool calls is replayed by the oracle's own allocator:
+page ownership, ranks and page tables must match the library's pool bit for
+bit after hundreds of steps of KV growth, request completions, adapter loads
+and least-recently-used evictions.
+"""
+import dataclasses
+
+import numpy as np
+
+from lora_adapters_gb300 import slora, trace, workloads
+from oracle import pool as opool
+
+
+def small_spec(**kw):
+    base = dict(H=256, projections=workloads._qkvo(256), num_adapters=60, pool_bytes=256 * 2 * 3000,
+                token_budget=128, max_running=24, arrivals_per_step=1.5, prompt_len=(4, 60),
+                output_len=(4, 40), steps=300, max_loads_per_step=4)
+    base.update(kw)
+    return dataclasses.replace(trace.TraceSpec(), **base)
+
+
+def test_trace_pool_state_replays_on_the_oracle_allocator():
+    sp = small_spec()
+    tr = trace.Trace(sp)
+    res = tr.run()
+    assert res.loads > 0 and res.evictions > 0 and res.finished > 0      # the trace exercised all of it
+    op = opool.OraclePool(sp.pool_pages, sp.H, [(p.h_in, p.h_out) for p in sp.projections], sp.num_adapters,
+                          max(sp.rank_set))
+    op.replay(res.ops, res.ranks)
+    snap = slora.slora_pool_snapshot(tr.pool.handle)
+    assert np.array_equal(snap["owner"], op.owner)
+    assert np.array_equal(snap["rank"], op.rank)
+    assert snap["free_pages"] == op.free_count
+    for a, tab in op.tables.items():
+        assert np.array_equal(snap["page_table"][a, :tab.shape[0]], tab)
+    # every running request's adapter is resident; its KV pages match its tokens
+    for rq in tr.running:
+        assert op.rank[rq.adapter] > 0
+        kv = sum(tr.kv[h].shape[0] for h in rq.kv_handles)
+        assert kv == (rq.prompt + rq.output) * sp.kv_pages_per_token
+    # pages: free + KV + adapters = all
+    kv_pages = sum(p.shape[0] for p in tr.kv.values())
+    ad_pages = sum(int(op.rank[a]) * op.chunks_per_rank() for a in op.tables)
+    assert op.free_count + kv_pages + ad_pages == sp.pool_pages
+    tr.close()
+
+
+def test_trace_is_deterministic():
+    a = trace.Trace(small_spec(steps=120)).run()
+    b = trace.Trace(small_spec(steps=120)).run()
+    assert len(a.ops) == len(b.ops)
+    for x, y in zip(a.ops, b.ops):
+        assert x[0] == y[0] and x[1] == y[1]
+        if x[0] == "kv_free":
+            assert np.array_equal(x[2], y[2])
+        elif x[0] == "kv_alloc":
+            assert x[2] == y[2]
+    assert a.tokens == b.tokens and a.finished == b.finished
