@@ -149,6 +149,12 @@ struct TcDev {
   uint16_t* vhi[kMaxProj];
   uint16_t* vlo[kMaxProj];
   int32_t v16_ld;                    // multiple of kTcK
+  // tc_shrink splits each (tile, projection) in two K halves: their partial
+  // sums (fp32, rows like v) and, per (tile, projection, 32-row quarter), a
+  // count of halves done (zero between calls)
+  float* vpart;                      // [2][kMaxProj][rows][v_ld]
+  int64_t vpart_half, vpart_proj;    // strides in floats
+  int32_t* combine;                  // [max_tc_tiles][kMaxProj][4]
   int32_t tc_ncol[kMaxProj];         // expand column tiles per projection (tc_col_tiles)
   const int32_t* tc_off;             // prefix array of the tensor-core tile list
   int32_t tc_total_idx;

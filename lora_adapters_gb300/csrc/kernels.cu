@@ -377,32 +377,47 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
     // One warp hands every (warp, adapter) group its first position, in
     // token order: the adapter's running start plus the tokens of that
     // adapter in earlier warps of this tile; the running start then moves
-    // past this tile.  When every warp holds one group (long runs of one
-    // adapter, as in prefill batches of several tiles) lane w takes warp w's
-    // group and all bases come from one round of shuffles; otherwise the warps are walked
+    // past this tile.  When every warp holds at most two groups (long runs of
+    // one adapter, as in prefill batches of several tiles) lane w takes warp
+    // w's groups and all bases come from one round of shuffles; otherwise the warps are walked
     // one by one (the groups of one warp have distinct adapters, so its
     // lanes update distinct running starts).
     if (warp == 0) {
       const int nw = min(nthr, T - base + 31) >> 5;   // warps with tokens in this tile
       const int ng_l = lane < nw ? ngrp[lane] : 0;
-      if (T > nthr && __all_sync(0xffffffffu, ng_l <= 1)) {   // batches of several tiles
-        const int k_l = ng_l ? grp_key[lane][0] : -1 - lane;   // empty warps match nothing
-        const int c_l = ng_l ? grp_cnt[lane][0] : 0;
-        int before = 0;
-        bool last_of_key = true;
+      if (T > nthr && __all_sync(0xffffffffu, ng_l <= 2)) {   // batches of several tiles
+        // lane w holds warp w's (at most two) groups; empty slots match nothing
+        const int k0 = ng_l > 0 ? grp_key[lane][0] : -1 - 2 * lane;
+        const int c0 = ng_l > 0 ? grp_cnt[lane][0] : 0;
+        const int k1 = ng_l > 1 ? grp_key[lane][1] : -2 - 2 * lane;
+        const int c1 = ng_l > 1 ? grp_cnt[lane][1] : 0;
+        int before0 = 0, before1 = 0;
+        bool last0 = true, last1 = true;
         for (int j = 0; j < 32; ++j) {
-          const int kj = __shfl_sync(0xffffffffu, k_l, j);
-          const int cj = __shfl_sync(0xffffffffu, c_l, j);
-          if (kj == k_l) {
-            if (j < lane) before += cj;
-            if (j > lane) last_of_key = false;
+          const int kj0 = __shfl_sync(0xffffffffu, k0, j), cj0 = __shfl_sync(0xffffffffu, c0, j);
+          const int kj1 = __shfl_sync(0xffffffffu, k1, j), cj1 = __shfl_sync(0xffffffffu, c1, j);
+          // the two groups of one warp have distinct adapters
+          const int m0 = (kj0 == k0 ? cj0 : 0) + (kj1 == k0 ? cj1 : 0);
+          const int m1 = (kj0 == k1 ? cj0 : 0) + (kj1 == k1 ? cj1 : 0);
+          if (j < lane) {
+            before0 += m0;
+            before1 += m1;
+          }
+          if (j > lane) {
+            last0 = last0 && m0 == 0;
+            last1 = last1 && m1 == 0;
           }
         }
-        const int b0 = ng_l ? hist[k_l] : 0;
+        const int b0 = ng_l > 0 ? hist[k0] : 0;
+        const int b1 = ng_l > 1 ? hist[k1] : 0;
         __syncwarp();
-        if (ng_l) {
-          grp_base[lane][0] = b0 + before;
-          if (last_of_key) hist[k_l] = b0 + before + c_l;
+        if (ng_l > 0) {
+          grp_base[lane][0] = b0 + before0;
+          if (last0) hist[k0] = b0 + before0 + c0;
+        }
+        if (ng_l > 1) {
+          grp_base[lane][1] = b1 + before1;
+          if (last1) hist[k1] = b1 + before1 + c1;
         }
       } else {
         for (int w = 0; w < nw; ++w) {

@@ -118,6 +118,30 @@ __device__ __forceinline__ void cp16_shared(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
+// Shrink unit g: the K range of (tile, projection) is split in two halves
+// (units 2u and 2u+1), so that the short list of 128-token tiles spreads over
+// twice as many units.  A projection with fewer than two K blocks is not
+// split (its second half is skipped).
+struct ShUnit {
+  int tile, p, kb_lo, kb_hi;
+  bool split, skip;
+  int half;
+};
+__device__ __forceinline__ ShUnit sh_unit(const ApplyDev& d, int64_t g) {
+  ShUnit s;
+  s.half = (int)(g & 1);
+  const int64_t tp = g >> 1;
+  s.tile = (int)(tp / d.nproj);
+  s.p = (int)(tp - (int64_t)s.tile * d.nproj);
+  const int nkb = (d.proj[s.p].h_in + kTcK - 1) / kTcK;
+  s.split = nkb >= 2;
+  s.skip = !s.split && s.half == 1;
+  const int mid = nkb / 2;
+  s.kb_lo = s.split && s.half ? mid : 0;
+  s.kb_hi = s.split && !s.half ? mid : nkb;
+  return s;
+}
+
 template <class E>
 __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __grid_constant__ TcDev t) {
   extern __shared__ uint8_t smem_raw[];
@@ -147,16 +171,16 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
   tc_fence_after();
   pdl_trigger();
   const uint32_t tmem = sm.tmem_slot;
-  const int64_t G = (int64_t)tiles * d.nproj;
+  const int64_t G = (int64_t)tiles * d.nproj * 2;   // K halves
   constexpr bool bf16 = std::is_same<E, __nv_bfloat16>::value;
   bool ok = true;
 
   if (warp == 0) {  // ------------------------------------------ producer
     uint32_t stage = 0, phase = 0;
     for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x) {
-      const int tile = (int)(g / d.nproj);
-      const TcUnit u = tc_tile(t, sm.off, off_smem, S, tile, (int)(g - (int64_t)tile * d.nproj));
-      const ProjDev& P = d.proj[u.p];
+      const ShUnit su = sh_unit(d, g);
+      if (su.skip) continue;
+      const TcUnit u = tc_tile(t, sm.off, off_smem, S, su.tile, su.p);
       const int r16 = (u.r + 15) & ~15;
       const int nx4 = (u.len + 3) >> 2;  // gather4 ops for the token rows
       const int nb4 = r16 >> 2;          // gather4 ops for the adapter rows
@@ -175,9 +199,8 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
       const int n16 = (u.len + 15) >> 4;  // 16-row boxes of a partial run tile
       const uint32_t x_bytes = run ? (u.len == kTcM ? (uint32_t)kTcM * kRowBytes : (uint32_t)n16 * 16 * kRowBytes)
                                    : (uint32_t)(4 * nx4) * kRowBytes;
-      const int nkb = (P.h_in + kTcK - 1) / kTcK;
       (void)nb4;
-      for (int kb = 0; kb < nkb; ++kb) {
+      for (int kb = su.kb_lo; kb < su.kb_hi; ++kb) {
         const int k0 = kb * kTcK;
         bool got = true;
         if (lane == 0) got = mbar_wait(&sm.empty[stage], phase ^ 1);
@@ -205,16 +228,15 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
   } else if (warp == 1) {  // ----------------------------------- MMA issuer
     uint32_t stage = 0, phase = 0;
     int n = 0;
-    for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x, ++n) {
-      const int tile = (int)(g / d.nproj);
-      const int p = (int)(g - (int64_t)tile * d.nproj);
+    for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x) {
+      const ShUnit su = sh_unit(d, g);
+      if (su.skip) continue;
+      const int tile = su.tile, p = su.p;
       int r = 0;
       if (lane == 0) r = tc_tile(t, sm.off, off_smem, S, tile, p).r;
       r = __shfl_sync(0xffffffffu, r, 0);
       const int r16 = (r + 15) & ~15;
       const int ab = n & 1;
-      const ProjDev& P = d.proj[p];
-      const int nkb = (P.h_in + kTcK - 1) / kTcK;
       bool got = true;
       if (lane == 0) got = mbar_wait(&sm.tempty[ab], ((n >> 1) & 1) ^ 1);
       if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
@@ -224,7 +246,7 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
       tc_fence_after();
       const uint32_t idesc = umma_idesc_f16(kTcM, r16, bf16, false);
       const uint32_t dtm = tmem + (uint32_t)(ab * kTcN);
-      for (int kb = 0; kb < nkb; ++kb) {
+      for (int kb = su.kb_lo; kb < su.kb_hi; ++kb) {
         if (lane == 0) got = mbar_wait(&sm.full[stage], phase);
         if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
           ok = false;
@@ -236,7 +258,7 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
 #pragma unroll
           for (int ks = 0; ks < kTcK / 16; ++ks)
             umma_f16(dtm, umma_desc_sw128(xa + ks * 32, 16, 1024), umma_desc_sw128(ba + ks * 32, 16, 1024), idesc,
-                     (kb | ks) ? 1u : 0u);
+                     (kb != su.kb_lo || ks) ? 1u : 0u);
           umma_commit(&sm.empty[stage]);  // the stage is free once these MMAs have read it
         }
         __syncwarp();
@@ -248,6 +270,7 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
       if (!ok) break;
       if (lane == 0) umma_commit(&sm.tfull[ab]);
       __syncwarp();
+      ++n;
     }
   } else if (warp >= 6) {  // ------------------------------------ adapter-row loaders
     const int lt = threadIdx.x - 6 * 32;    // 0 .. kShrinkLoaders - 1
@@ -256,15 +279,15 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
     uint32_t stage = 0, phase = 0;
     int pending = -1;                       // stage whose copies are committed, not yet announced
     for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x) {
-      const int tile = (int)(g / d.nproj);
-      const TcUnit u = tc_tile(t, sm.off, off_smem, S, tile, (int)(g - (int64_t)tile * d.nproj));
+      const ShUnit su = sh_unit(d, g);
+      if (su.skip) continue;
+      const TcUnit u = tc_tile(t, sm.off, off_smem, S, su.tile, su.p);
       const ProjDev& P = d.proj[u.p];
       const int32_t* pt = d.page_table + (int64_t)u.a * d.pt_stride + (int64_t)u.r * P.rows_before;
-      const int nkb = (P.h_in + kTcK - 1) / kTcK;
       const int nrow = (u.r - row0 + 15) >> 4;   // my rows below r (rows past r are never read back)
       int chunk = -1;
       int pg[kRowsPerLoader];
-      for (int kb = 0; kb < nkb; ++kb) {
+      for (int kb = su.kb_lo; kb < su.kb_hi; ++kb) {
         const int k0 = kb * kTcK, c = k0 / d.H, o = k0 - c * d.H;
         if (c != chunk) {  // pages of my rows for this page chunk
           chunk = c;
@@ -306,12 +329,17 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
       mbar_arrive(&sm.full[pending]);
     }
   } else {  // ------------------------------------------------- epilogue (warps 2-5)
+    // A split unit writes its partial sums (fp32) to its half's scratch
+    // rows; the half that finishes second (per warp: per 32 rows) adds the
+    // other half's rows to its own accumulator and writes s_a v and its
+    // 16-bit halves.  Neither half waits for the other.
     const int quarter = warp & 3;  // TMEM lanes this warp may read
     const int m = 32 * quarter + lane;
     int n = 0;
-    for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x, ++n) {
-      const int tile = (int)(g / d.nproj);
-      const TcUnit u = tc_tile(t, sm.off, off_smem, S, tile, (int)(g - (int64_t)tile * d.nproj));
+    for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x) {
+      const ShUnit su = sh_unit(d, g);
+      if (su.skip) continue;
+      const TcUnit u = tc_tile(t, sm.off, off_smem, S, su.tile, su.p);
       const int r16 = (u.r + 15) & ~15;
       const int ab = n & 1;
       bool got = true;
@@ -320,45 +348,94 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
         ok = false;
         break;
       }
+      ++n;
       tc_fence_after();
       const int j = u.j0 + m;
-      const float sa = d.scale ? __ldg(d.scale + u.a) : 1.f;   // the adapter's scale, applied to v
-      float* vrow = d.proj[u.p].v + (int64_t)j * d.v_ld;
-      uint16_t* hrow = t.vhi[u.p] + (int64_t)j * t.v16_ld;
-      uint16_t* lrow = t.vlo[u.p] + (int64_t)j * t.v16_ld;
-      // 32 accumulator columns per TMEM round trip
-      for (int c00 = 0; c00 < r16; c00 += 32) {
-        uint32_t raw[32];
-        tmem_ld32_nowait(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(ab * kTcN + c00), raw);
-        tmem_wait_ld(raw);
+      const uint32_t tacc = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(ab * kTcN);
+      bool finish = true;            // this warp writes the final v rows
+      const float* other = nullptr;  // the other half's partial row
+      if (su.split) {
+        float* mine = t.vpart + (int64_t)su.half * t.vpart_half + (int64_t)u.p * t.vpart_proj + (int64_t)j * d.v_ld;
+        for (int c00 = 0; c00 < r16; c00 += 32) {
+          uint32_t raw[32];
+          tmem_ld32_nowait(tacc + (uint32_t)c00, raw);
+          tmem_wait_ld(raw);
+          if (m < u.len) {
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-        const int c0 = c00 + 16 * hh;
-        if (m < u.len && c0 < r16) {
-          float v[16];
-          uint16_t hi[16], lo[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float x = c0 + i < u.r ? sa * __uint_as_float(raw[16 * hh + i]) : 0.f;
-            v[i] = x;
-            hi[i] = Elem<E>::from(x);
-            lo[i] = Elem<E>::from(x - Elem<E>::to(hi[i]));
+            for (int i = 0; i < 32; i += 4)
+              if (c00 + i < u.r)
+                *reinterpret_cast<float4*>(mine + c00 + i) =
+                    make_float4(__uint_as_float(raw[i]), __uint_as_float(raw[i + 1]), __uint_as_float(raw[i + 2]),
+                                __uint_as_float(raw[i + 3]));
           }
-          // fp32 v: 16-byte stores up to the row's last multiple of 4 columns
-          // (the v row stride is a multiple of 4 floats, past r only padding)
-#pragma unroll
-          for (int i = 0; i < 16; i += 4)
-            if (c0 + i < u.r) *reinterpret_cast<float4*>(vrow + c0 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-          uint4 h0, h1, l0, l1;
-          memcpy(&h0, hi, 16);
-          memcpy(&h1, hi + 8, 16);
-          memcpy(&l0, lo, 16);
-          memcpy(&l1, lo + 8, 16);
-          *reinterpret_cast<uint4*>(hrow + c0) = h0;
-          *reinterpret_cast<uint4*>(hrow + c0 + 8) = h1;
-          *reinterpret_cast<uint4*>(lrow + c0) = l0;
-          *reinterpret_cast<uint4*>(lrow + c0 + 8) = l1;
         }
+        __threadfence();   // my partial rows, before the count says they are there
+        __syncwarp();
+        int old = 0;
+        int32_t* cnt = t.combine + ((int64_t)su.tile * d.nproj + u.p) * 4 + quarter;
+        if (lane == 0) old = atomicAdd(cnt, 1);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        finish = old == 1;
+        if (finish) {
+          __threadfence();   // the other half's partial rows are visible now
+          other = t.vpart + (int64_t)(1 - su.half) * t.vpart_half + (int64_t)u.p * t.vpart_proj + (int64_t)j * d.v_ld;
+          if (lane == 0) *cnt = 0;   // both halves are in: ready for the next call
+        }
+      }
+      if (finish) {
+        const float sa = d.scale ? __ldg(d.scale + u.a) : 1.f;   // the adapter's scale, applied to v
+        float* vrow = d.proj[u.p].v + (int64_t)j * d.v_ld;
+        uint16_t* hrow = t.vhi[u.p] + (int64_t)j * t.v16_ld;
+        uint16_t* lrow = t.vlo[u.p] + (int64_t)j * t.v16_ld;
+        // 32 accumulator columns per TMEM round trip
+        for (int c00 = 0; c00 < r16; c00 += 32) {
+          uint32_t raw[32];
+          tmem_ld32_nowait(tacc + (uint32_t)c00, raw);
+          tmem_wait_ld(raw);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int c0 = c00 + 16 * hh;
+            if (m < u.len && c0 < r16) {
+              float v[16];
+              uint16_t hi[16], lo[16];
+              if (other) {
+#pragma unroll
+                for (int i = 0; i < 16; i += 4) {
+                  const float4 o4 = c0 + i < u.r ? *reinterpret_cast<const float4*>(other + c0 + i)
+                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                  v[i] = o4.x;
+                  v[i + 1] = o4.y;
+                  v[i + 2] = o4.z;
+                  v[i + 3] = o4.w;
+                }
+              } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = 0.f;
+              }
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float x = c0 + i < u.r ? sa * (__uint_as_float(raw[16 * hh + i]) + v[i]) : 0.f;
+                v[i] = x;
+                hi[i] = Elem<E>::from(x);
+                lo[i] = Elem<E>::from(x - Elem<E>::to(hi[i]));
+              }
+              // fp32 v: 16-byte stores up to the row's last multiple of 4 columns
+              // (the v row stride is a multiple of 4 floats, past r only padding)
+#pragma unroll
+              for (int i = 0; i < 16; i += 4)
+                if (c0 + i < u.r)
+                  *reinterpret_cast<float4*>(vrow + c0 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+              uint4 h0, h1, l0, l1;
+              memcpy(&h0, hi, 16);
+              memcpy(&h1, hi + 8, 16);
+              memcpy(&l0, lo, 16);
+              memcpy(&l1, lo + 8, 16);
+              *reinterpret_cast<uint4*>(hrow + c0) = h0;
+              *reinterpret_cast<uint4*>(hrow + c0 + 8) = h1;
+              *reinterpret_cast<uint4*>(lrow + c0) = l0;
+              *reinterpret_cast<uint4*>(lrow + c0 + 8) = l1;
+            }
+          }
         }
       }
       tc_fence_before();
