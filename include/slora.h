@@ -79,8 +79,10 @@ typedef struct slora_pool slora_pool; /* opaque, owned by the library */
  * matrix-vector products, SGMV: cmlonder.com newsletter, section "Iddia ve
  * Gerceklik").  Tokens are stably sorted by adapter id, ascending; tokens
  * with id -1 carry no adapter and are left out, as are tokens that name an
- * adapter that is not resident (those are counted in counts[2] and raise
- * the device status SLORA_ERR_NOT_RESIDENT).  All arrays are DEVICE memory
+ * adapter that is not resident or an id outside [-1, max_adapters) (those
+ * are counted in counts[2] and raise the device status
+ * SLORA_ERR_NOT_RESIDENT or SLORA_ERR_INVALID; the first such token seen
+ * decides which).  All arrays are DEVICE memory
  * owned by the pool; they stay valid until the next slora_build_segments on
  * the same pool (or the next evict), which invalidates every earlier handle
  * (generation check).

@@ -239,15 +239,16 @@ def build_segments(token_adapter, rank) -> Segments:
     """Group the batch's tokens by adapter (stable, ascending id; see module doc).
 
     Tokens with id -1 are skipped.  Tokens naming an id that is out of range
-    or not resident (rank 0) are skipped too and counted in ``bad_tokens``.
+    (below -1 or past the last adapter) or not resident (rank 0) are skipped
+    too and counted in ``bad_tokens``.
     """
     ta = [int(v) for v in np.asarray(token_adapter)]
     rank = np.asarray(rank)
     keep, bad = [], 0
     for i, a in enumerate(ta):
-        if a < 0:
+        if a == -1:
             continue
-        if a >= rank.shape[0] or rank[a] <= 0:
+        if a < 0 or a >= rank.shape[0] or rank[a] <= 0:
             bad += 1
             continue
         keep.append(i)

@@ -109,6 +109,16 @@ def test_golden_segments(golden_dir):
     assert seg.bad_tokens == g["expected_bad_tokens"]
 
 
+def test_segments_out_of_range_ids_by_hand():
+    """Only -1 means "no adapter": ids below it and past the last adapter are
+    left out and counted, like an adapter that is not resident."""
+    seg = opool.build_segments(np.asarray([1, -2, 0, -1, 5, 1, 2, 0]), np.asarray([4, 8, 0]))
+    assert seg.perm.tolist() == [2, 7, 0, 5]
+    assert seg.seg_start.tolist() == [0, 2, 4]
+    assert seg.seg_adapter.tolist() == [0, 1]
+    assert seg.bad_tokens == 3          # -2, 5 (out of range), 2 (rank 0)
+
+
 @pytest.mark.parametrize("T,N,frac_none", [(0, 5, 0.0), (1, 5, 0.0), (300, 7, 0.2), (5000, 1000, 0.05),
                                            (64, 3, 1.0)])
 def test_segment_properties(T, N, frac_none):
