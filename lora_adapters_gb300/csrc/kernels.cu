@@ -188,8 +188,13 @@ __device__ __forceinline__ int pick(const int (&a)[N], int i) {
 //      into shared memory first when it fits;
 //  (2) one block scan over the histogram (each thread owns a run of adapter
 //      ids) -> one segment per adapter present, in ascending id;
-//  (3) stable scatter of token indices: tokens are visited in order, 1024 at
-//      a time; each warp groups its tokens by adapter (match_any), one warp
+//  (3) stable scatter of token indices.  A batch of several tiles whose
+//      tokens come in few runs of one adapter (prefill: a run per request) is
+//      placed run by run: the runs are listed with one block scan, one warp
+//      gives each run its first position (the adapter's running start plus
+//      the earlier runs of that adapter), and every thread places its own
+//      contiguous tokens.  Otherwise tokens are visited in order, 1024 at a
+//      time; each warp groups its tokens by adapter (match_any), one warp
 //      then gives every (warp, adapter) group its first position by walking
 //      the warps in order, and a token's position is its group's first
 //      position + its rank inside the group;
@@ -348,9 +353,71 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
   }
   __syncthreads();
 
-  // (3) stable scatter, one tile of 1024 tokens at a time, in token order
+  // (3a) stable scatter by runs: thread t owns tokens [lo, hi); a run starts
+  // wherever the key changes (runs of invalid tokens are listed too and
+  // placed nowhere)
+  bool scattered = false;
+  if (keys_smem && T > nthr) {
+    const int m = (T + nthr - 1) / nthr;
+    const int lo = min(T, tid * m), hi = min(T, lo + m);
+    auto starts_run = [&](int i) -> bool { return i == 0 || skeys[i - 1] != skeys[i]; };
+    int v[1] = {0}, tot[1];
+    for (int i = lo; i < hi; ++i) v[0] += starts_run(i) ? 1 : 0;
+    block_scan_excl<1>(v, tot, scan_sh);
+    const int R = tot[0];
+    // worth it only for few, long runs; the run list lives in the group arrays
+    if (R < 32 * 32 && 8 * R <= T) {
+      int* run_start = &grp_cnt[0][0];   // [R + 1]
+      int* run_key = &grp_key[0][0];     // [R]
+      int* run_base = &grp_base[0][0];   // [R]
+      int q = v[0];
+      for (int i = lo; i < hi; ++i)
+        if (starts_run(i)) {
+          run_start[q] = i;
+          run_key[q] = skeys[i];
+          ++q;
+        }
+      if (tid == 0) run_start[R] = T;
+      __syncthreads();
+      if (warp == 0) {
+        // 32 runs at a time, in token order: a run's first position is its
+        // adapter's running start plus the earlier runs of that adapter in
+        // this chunk; the last of them moves the running start on
+        for (int c0 = 0; c0 < R; c0 += 32) {
+          const int qr = c0 + lane;
+          const int k = qr < R ? run_key[qr] : -1;
+          const int kk = k >= 0 ? k : -1 - lane;   // invalid runs match nothing
+          const int len = k >= 0 ? run_start[qr + 1] - run_start[qr] : 0;
+          int before = 0;
+          bool last = true;
+          for (int j = 0; j < 32; ++j) {
+            const int kj = __shfl_sync(0xffffffffu, kk, j), lj = __shfl_sync(0xffffffffu, len, j);
+            if (kj == kk) {
+              if (j < lane) before += lj;
+              if (j > lane) last = false;
+            }
+          }
+          const int b = k >= 0 ? hist[k] : 0;
+          __syncwarp();
+          if (k >= 0) {
+            run_base[qr] = b + before;
+            if (last) hist[k] = b + before + len;
+          }
+          __syncwarp();
+        }
+      }
+      __syncthreads();
+      int cur = v[0] - 1;   // the run holding token lo (token 0 always starts one)
+      for (int i = lo; i < hi; ++i) {
+        if (starts_run(i)) ++cur;
+        if (skeys[i] >= 0) sd.perm[run_base[cur] + (i - run_start[cur])] = i;
+      }
+      scattered = true;
+    }
+  }
+  // (3b) stable scatter, one tile of 1024 tokens at a time, in token order
   const unsigned lt = (1u << lane) - 1u;
-  for (int c = 0, base = 0; base < T; ++c, base += nthr) {
+  for (int c = 0, base = 0; base < T && !scattered; ++c, base += nthr) {
     const int i = base + tid;
     int key = -1;
     if (keys_smem) {

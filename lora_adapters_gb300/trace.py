@@ -56,7 +56,7 @@ class TraceSpec:
     max_running: int = 256                   # requests in the batch at once
     arrivals_per_step: float = 4.0
     prompt_len: Tuple[int, int] = (8, 512)
-    output_len: Tuple[int, int] = (8, 512)
+    output_len: Tuple[int, int] = (8, 128)   # with the 256-request cap, the 1024-token budget fills
     max_loads_per_step: int = 32
     prefetch_window: int = 64                # misses loaded only for the first waiting requests
     steps: int = 1000

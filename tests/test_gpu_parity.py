@@ -191,6 +191,49 @@ def test_edge_cases():
     pool.close()
 
 
+def test_segment_build_token_orders():
+    """The segment kernel on token orders of every kind, bit for bit: long runs
+    of one adapter (placed run by run), short runs and random orders (placed
+    tile by tile), the boundary between the two, a single tile plus one
+    token, invalid and non-resident ids."""
+    wl = workloads.make("tiny")
+    case = G.build_case(wl, max_tokens=20000)
+    pool = case.pool
+    slora.slora_adapter_evict(pool.handle, 3)
+    rank = case.oracle_pool.rank.copy()
+    rank[3] = 0
+    rng = np.random.default_rng(5)
+
+    def runs(n, lo, hi, ids, cap=20000):
+        keys = rng.choice(ids, n)
+        return np.repeat(keys, rng.integers(lo, hi + 1, n)).astype(np.int32)[:cap]
+
+    orders = {
+        "prefill runs": (runs(40, 50, 400, [0, 1, 2, -1]), False),
+        "runs of 8": (np.repeat(np.arange(400) % 3, 8).astype(np.int32), False),
+        "runs of 7": (np.repeat(np.arange(400) % 3, 7).astype(np.int32), False),
+        "short runs": (runs(2000, 1, 6, [0, 1, 2, -1]), False),
+        "random": (rng.choice([0, 1, 2, -1], 5000).astype(np.int32), False),
+        "one tile + 1": (runs(8, 200, 300, [0, 1, 2])[:1025], False),
+        "20000 tokens": (runs(80, 200, 500, [0, 1, 2]), False),
+        "bad ids in runs": (runs(30, 50, 300, [0, 1, 2, 3, 7, -1, -3]), True),
+        "bad ids scattered": (rng.choice([0, 1, 2, 3, 9, -1], 3000).astype(np.int32), True),
+    }
+    for name, (ta, bad) in orders.items():
+        seg = pool.build_segments(torch.from_numpy(ta).to("cuda"))
+        torch.cuda.synchronize()
+        want = opool.build_segments(ta, rank)
+        perm, start, adapter, counts = G.seg_arrays(seg)
+        assert counts[0] == want.num_segs and counts[1] == want.perm.shape[0], name
+        assert counts[2] == want.bad_tokens, name
+        assert np.array_equal(perm, want.perm), name
+        assert np.array_equal(start, want.seg_start), name
+        assert np.array_equal(adapter, want.seg_adapter), name
+        status = pool.status()   # reading clears it
+        assert (status != slora.OK) == bad, (name, status)
+    pool.close()
+
+
 def test_evict_and_reload_into_other_pages_gives_identical_y():
     wl = workloads.make("tiny")
     case = G.build_case(wl)
