@@ -27,6 +27,7 @@ constexpr int kSegThreads = 1024;
 constexpr int kTcM = 128;
 constexpr int kTcK = 64;
 constexpr int kTcN = 256;
+constexpr int kTcShrinkParts = 2;        // K parts of one tc_shrink (tile, projection)
 
 // Indices into SegDev::counts.
 enum CountIdx {
@@ -152,9 +153,8 @@ struct TcDev {
   // tc_shrink splits each (tile, projection) in two K halves: their partial
   // sums (fp32, rows like v) and, per (tile, projection, 32-row quarter), a
   // count of halves done (zero between calls)
-  float* vpart;                      // [2][kMaxProj][rows][v_ld]
-  int64_t vpart_half, vpart_proj;    // strides in floats
-  int32_t* combine;                  // [max_tc_tiles][kMaxProj][4]
+  float* vpart;                      // tc_shrink's partial sums, [kTcShrinkParts][kMaxProj][rows][v_ld] (by call position)
+  int64_t vpart_part, vpart_proj;    // strides in floats
   int32_t tc_ncol[kMaxProj];         // expand column tiles per projection (tc_col_tiles)
   const int32_t* tc_off;             // prefix array of the tensor-core tile list
   int32_t tc_total_idx;

@@ -110,9 +110,7 @@ struct slora_pool {
   bool tc_ok = false;
   int32_t v16_ld = 0;            // row stride of the 16-bit v halves
   uint16_t* d_v16 = nullptr;     // v_hi then v_lo, [kMaxProj][max_tokens][v16_ld] each
-  float* d_vpart = nullptr;      // tc_shrink's K-half partial sums, [2][kMaxProj][rows][v_ld]
-  int32_t* d_combine = nullptr;  // tc_shrink's halves-done counts, [max_tc_tiles][kMaxProj][4]
-  int64_t combine_ints = 0;
+  float* d_vpart = nullptr;      // tc_shrink's K-part partial sums, [kTcShrinkParts][kMaxProj][rows][v_ld]
   CUtensorMap pool_map{};
   CUtensorMap vhi_map[kMaxProj]{}, vlo_map[kMaxProj]{};
 
@@ -291,7 +289,6 @@ void free_device(slora_pool* p) {
   cudaFree(p->d_grid_sync);
   cudaFree(p->d_v16);
   cudaFree(p->d_vpart);
-  cudaFree(p->d_combine);
   cudaFree(p->d_staging);
   if (p->pt_h) cudaFreeHost(p->pt_h);
   if (p->rank_pin) cudaFreeHost(p->rank_pin);
@@ -437,11 +434,7 @@ int slora_pool_create(slora_pool** out, void* d_pool, int64_t num_pages, int32_t
       const size_t half_elems = (size_t)kMaxProj * rows * p->v16_ld;
       CUDA_TRY(cudaMalloc(&p->d_v16, sizeof(uint16_t) * 2 * half_elems));
       CUDA_TRY(cudaMemsetAsync(p->d_v16, 0, sizeof(uint16_t) * 2 * half_elems, p->compute));
-      CUDA_TRY(cudaMalloc(&p->d_vpart, sizeof(float) * 2 * (size_t)kMaxProj * rows * v_ld(p)));
-      const int64_t max_tc_tiles = (std::max(max_tokens, 1) + kTcM - 1) / kTcM + p->max_segs;
-      p->combine_ints = max_tc_tiles * kMaxProj * 4;
-      CUDA_TRY(cudaMalloc(&p->d_combine, sizeof(int32_t) * (size_t)p->combine_ints));
-      CUDA_TRY(cudaMemsetAsync(p->d_combine, 0, sizeof(int32_t) * (size_t)p->combine_ints, p->compute));
+      CUDA_TRY(cudaMalloc(&p->d_vpart, sizeof(float) * kTcShrinkParts * (size_t)kMaxProj * rows * v_ld(p)));
       if (int rc = encode_2d(&p->pool_map, p->d_pool, dtype, (uint64_t)page_elems, (uint64_t)num_pages,
                              (uint64_t)page_elems * 2, kTcK, 1))
         return rc;
@@ -783,9 +776,8 @@ int slora_lora_apply_multi(slora_pool* p, const slora_segments* seg, int32_t n, 
     }
     t.vpart = p->d_vpart;
     t.vpart_proj = rows * v_ld(p);
-    t.vpart_half = (int64_t)kMaxProj * rows * v_ld(p);
-    t.combine = p->d_combine;
-    if (!t.vpart || !t.combine) return fail(SLORA_ERR_INVALID, "tensor-core scratch is missing");
+    t.vpart_part = (int64_t)kMaxProj * rows * v_ld(p);
+    if (!t.vpart) return fail(SLORA_ERR_INVALID, "tensor-core scratch is missing");
     if (mode == SLORA_MODE_PREFILL) {
       // every segment on the tensor cores; no CUDA-core launch
       t.tc_off = p->seg.tc_tile_all;
@@ -830,12 +822,9 @@ int slora_device_status(slora_pool* p, int32_t* status) {
   CUDA_TRY(cudaMemsetAsync(p->d_error, 0, sizeof(int32_t), p->compute));
   CUDA_TRY(cudaStreamSynchronize(p->compute));
   if (v == SLORA_ERR_TIMEOUT) {
-    // A call that gave up may have left the apply kernel's grid barrier or
-    // tc_shrink's halves-done counts part-way; clear them so that the next
-    // call starts clean.
+    // A call that gave up may have left the apply kernel's grid barrier
+    // part-way; clear it so that the next call starts clean.
     CUDA_TRY(cudaMemsetAsync(p->d_grid_sync, 0, kGridSyncInts * sizeof(int32_t), p->compute));
-    if (p->d_combine)
-      CUDA_TRY(cudaMemsetAsync(p->d_combine, 0, sizeof(int32_t) * (size_t)p->combine_ints, p->compute));
     CUDA_TRY(cudaStreamSynchronize(p->compute));
   }
   *status = v;

@@ -94,51 +94,78 @@ struct Elem<__nv_bfloat16> {
 };
 
 // ================================================================ tc_shrink
-// Warps: 0 loads x tiles (TMA), 1 issues the MMAs, 2-5 drain TMEM, 6-9 copy
-// the adapter's rows.  Adapter rows go through the load/store unit rather
-// than the TMA engine: a K block needs r rows of 128 bytes, and a TMA op per
-// four rows made the copy engine's op rate the limit.  Each loader thread
-// copies one 16-byte chunk column of every 16th row with cp.async, straight
-// to its 128-byte-swizzled place, then (once its copies have landed) fences
-// them for the tensor cores' async proxy and arrives on the stage.
+// v^T = A_a x^T, one unit per (token tile, projection, K part).  The
+// adapter's A rows are the MMA's M side (128 rows, the rank padded) and the
+// tile's tokens its N side (up to 256).  A tcgen05 MMA of 128 x N x 16 costs
+// the same for every N up to 256, so this way round each MMA covers up to 256
+// tokens instead of the rank's 8..128 columns.  Ranks above 128 take two M
+// blocks (two accumulators) and tiles of 128 tokens.
+//
+// Warps: 1 issues the MMAs, 2-5 drain TMEM, 6-13 copy each stage's token
+// rows (x) and adapter rows (A); warp 0 has no role.  Rows go through the
+// load/store unit: each loader thread copies one 16-byte chunk column of every
+// 32nd row with cp.async, straight to its 128-byte-swizzled place, and (once
+// its copies have landed) fences them for the tensor cores' async proxy and
+// arrives on the stage.
+//
+// The K range of (tile, projection) is split into up to kShParts parts (units
+// of their own, so that a short list of tiles still spreads over the CTAs).
+// Each part writes its fp32 partial sums; tc_combine then adds the parts in
+// order and writes s_a v as its 16-bit hi and lo halves.
 constexpr int kShrinkTcStages = 4;
-constexpr int kShrinkLoaderWarps = 4;
+constexpr int kShrinkLoaderWarps = 8;
 constexpr int kShrinkLoaders = kShrinkLoaderWarps * 32;
 constexpr int kShrinkTcThreads = kTcThreads + kShrinkLoaders;
-constexpr int kRowsPerLoader = kMaxRank * (kRowBytes / 16) / kShrinkLoaders;   // rows one loader thread covers
+constexpr int kLoaderRowStep = kShrinkLoaders / (kRowBytes / 16);   // 32 rows between one thread's rows
+constexpr int kShTokWide = 256;                                     // tokens per unit when r <= 128
+constexpr int kShTokNarrow = 128;                                   // tokens per unit when r > 128
+constexpr int kShStageBytes = (kShTokWide + kTcM) * kRowBytes;      // 48 KB: x rows, then A rows
+static_assert((kShTokNarrow + 2 * kTcM) * kRowBytes == kShStageBytes, "both stage layouts fill a stage");
+constexpr int kShParts = kTcShrinkParts;
+constexpr int kShTmemCols = 2 * kShTokWide;                          // two accumulator buffers
+constexpr int kShMaxRows = kShTokWide / kLoaderRowStep;              // x or A rows one loader thread covers
 struct TcShrinkSmem {
-  uint8_t X[kShrinkTcStages][kTcM * kRowBytes];     // 128 token rows x 64 K, swizzled (16 KB)
-  uint8_t B[kShrinkTcStages][kMaxRank * kRowBytes]; // <= 256 adapter rows x 64 K (32 KB)
+  uint8_t st[kShrinkTcStages][kShStageBytes];
   uint64_t full[kShrinkTcStages], empty[kShrinkTcStages], tfull[2], tempty[2];
   uint32_t tmem_slot;
-  int32_t off[kSegSmem];
+  int32_t off[kSegSmem];    // tensor-core 128-token tile list (prefix per work-order position)
+  int32_t uoff[kSegSmem];   // unit tiles per position (256 tokens when r <= 128, else 128)
 };
 
 __device__ __forceinline__ void cp16_shared(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
+// The first `bytes` (0..16) of the chunk from global memory, the rest zeros.
+__device__ __forceinline__ void cp16_shared_zfill(uint32_t dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
 
-// Shrink unit g: the K range of (tile, projection) is split in two halves
-// (units 2u and 2u+1), so that the short list of 128-token tiles spreads over
-// twice as many units.  A projection with fewer than two K blocks is not
-// split (its second half is skipped).
+// Shrink unit g: part fastest, then projection, then unit tile.
 struct ShUnit {
-  int tile, p, kb_lo, kb_hi;
-  bool split, skip;
-  int half;
+  int tile, p, part, nparts, kb_lo, kb_hi;
+  int j0, ntok, tok, r, a;   // tok: the tile's token capacity (kShTokWide or kShTokNarrow)
+  bool skip;
 };
-__device__ __forceinline__ ShUnit sh_unit(const ApplyDev& d, int64_t g) {
+__device__ __forceinline__ ShUnit sh_unit(const TcDev& t, const int32_t* uoff, bool wide_ok, int S, int64_t g) {
+  const ApplyDev& d = t.a;
   ShUnit s;
-  s.half = (int)(g & 1);
-  const int64_t tp = g >> 1;
+  s.part = (int)(g % kShParts);
+  const int64_t tp = g / kShParts;
   s.tile = (int)(tp / d.nproj);
   s.p = (int)(tp - (int64_t)s.tile * d.nproj);
   const int nkb = (d.proj[s.p].h_in + kTcK - 1) / kTcK;
-  s.split = nkb >= 2;
-  s.skip = !s.split && s.half == 1;
-  const int mid = nkb / 2;
-  s.kb_lo = s.split && s.half ? mid : 0;
-  s.kb_hi = s.split && !s.half ? mid : nkb;
+  s.nparts = min(kShParts, nkb);
+  s.skip = s.part >= s.nparts;
+  s.kb_lo = nkb * s.part / s.nparts;
+  s.kb_hi = nkb * (s.part + 1) / s.nparts;
+  const int q = find_pos_tc(uoff, t.tc_off, wide_ok, S, s.tile);
+  const int mt = s.tile - (wide_ok ? uoff[q] : __ldg(t.tc_off + q));
+  const int4 sd = __ldg(d.seg_desc + q);   // adapter, rank, start, end
+  s.a = sd.x;
+  s.r = sd.y;
+  s.tok = wide_ok && s.r <= kTcM ? kShTokWide : kShTokNarrow;
+  s.j0 = sd.z + mt * s.tok;
+  s.ntok = min(s.tok, sd.w - s.j0);
   return s;
 }
 
@@ -148,10 +175,10 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
   TcShrinkSmem& sm = *reinterpret_cast<TcShrinkSmem*>(smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023));
   const ApplyDev& d = t.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp == 1) tmem_alloc(&sm.tmem_slot, 2 * kTcN);
+  if (warp == 1) tmem_alloc(&sm.tmem_slot, kShTmemCols);
   if (threadIdx.x == 0) {
     for (int s = 0; s < kShrinkTcStages; ++s) {
-      mbar_init(&sm.full[s], 1 + kShrinkLoaders);   // x bytes (warp 0) + every loader thread
+      mbar_init(&sm.full[s], kShrinkLoaders);   // every loader thread
       mbar_init(&sm.empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -163,79 +190,52 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
   pdl_wait();
   const int tiles = d.counts[t.tc_total_idx];
   const int S = d.counts[kNumSegs];
-  const bool off_smem = S + 1 <= kSegSmem;
-  if (off_smem)
+  // Wide unit tiles need the per-position list of unit tiles, built here in
+  // shared memory when it fits; otherwise every unit tile is a 128-token tile.
+  const bool wide_ok = S + 1 <= kSegSmem;
+  if (wide_ok)
     for (int i = threadIdx.x; i <= S; i += blockDim.x) sm.off[i] = t.tc_off[i];
+  __syncthreads();
+  if (wide_ok && warp == 0) {
+    const int per = (S + 31) >> 5;   // positions per lane
+    const int lo = min(S, lane * per), hi = min(S, lo + per);
+    auto units = [&](int q) -> int {
+      const int n = sm.off[q + 1] - sm.off[q];
+      return __ldg(d.seg_desc + q).y <= kTcM ? (n + 1) >> 1 : n;
+    };
+    int sum = 0;
+    for (int q = lo; q < hi; ++q) sum += units(q);
+    int inc = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += v;
+    }
+    int run = inc - sum;
+    for (int q = lo; q < hi; ++q) {
+      sm.uoff[q] = run;
+      run += units(q);
+    }
+    if (lane == 31) sm.uoff[S] = inc;
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   pdl_trigger();
   const uint32_t tmem = sm.tmem_slot;
-  const int64_t G = (int64_t)tiles * d.nproj * 2;   // K halves
+  const int utiles = wide_ok ? sm.uoff[S] : tiles;
+  const int64_t G = (int64_t)utiles * d.nproj * kShParts;
   constexpr bool bf16 = std::is_same<E, __nv_bfloat16>::value;
   bool ok = true;
 
-  if (warp == 0) {  // ------------------------------------------ producer
-    uint32_t stage = 0, phase = 0;
-    for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x) {
-      const ShUnit su = sh_unit(d, g);
-      if (su.skip) continue;
-      const TcUnit u = tc_tile(t, sm.off, off_smem, S, su.tile, su.p);
-      const int r16 = (u.r + 15) & ~15;
-      const int nx4 = (u.len + 3) >> 2;  // gather4 ops for the token rows
-      const int nb4 = r16 >> 2;          // gather4 ops for the adapter rows
-      int tok[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int m = 4 * lane + i;
-        tok[i] = __ldg(d.perm + u.j0 + (m < u.len ? m : 0));
-      }
-      // Tokens of a segment are in increasing order, so the tile is one run
-      // of consecutive rows of x exactly when its last token is first + len - 1
-      // (prefill requests): then 2-D boxes replace the row gathers.
-      const int t_first = __shfl_sync(0xffffffffu, tok[0], 0);
-      const int t_last = __ldg(d.perm + u.j0 + u.len - 1);
-      const bool run = t_last - t_first == u.len - 1;
-      const int n16 = (u.len + 15) >> 4;  // 16-row boxes of a partial run tile
-      const uint32_t x_bytes = run ? (u.len == kTcM ? (uint32_t)kTcM * kRowBytes : (uint32_t)n16 * 16 * kRowBytes)
-                                   : (uint32_t)(4 * nx4) * kRowBytes;
-      (void)nb4;
-      for (int kb = su.kb_lo; kb < su.kb_hi; ++kb) {
-        const int k0 = kb * kTcK;
-        bool got = true;
-        if (lane == 0) got = mbar_wait(&sm.empty[stage], phase ^ 1);
-        if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) mbar_expect_tx(&sm.full[stage], x_bytes);
-        __syncwarp();
-        if (!run) {
-          if (lane < nx4)
-            tma_gather4(&sm.X[stage][4 * lane * kRowBytes], &t.x_map[u.p], k0, tok[0], tok[1], tok[2], tok[3],
-                        &sm.full[stage]);
-        } else if (u.len == kTcM) {
-          if (lane == 0) tma_load_2d(sm.X[stage], &t.x128_map[u.p], k0, t_first, &sm.full[stage]);
-        } else if (lane < n16) {
-          tma_load_2d(&sm.X[stage][16 * lane * kRowBytes], &t.x16_map[u.p], k0, t_first + 16 * lane, &sm.full[stage]);
-        }
-        if (++stage == kShrinkTcStages) {
-          stage = 0;
-          phase ^= 1;
-        }
-      }
-    }
+  if (warp == 0) {
+    // no role
   } else if (warp == 1) {  // ----------------------------------- MMA issuer
     uint32_t stage = 0, phase = 0;
     int n = 0;
     for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x) {
-      const ShUnit su = sh_unit(d, g);
+      const ShUnit su = sh_unit(t, sm.uoff, wide_ok, S, g);
       if (su.skip) continue;
-      const int tile = su.tile, p = su.p;
-      int r = 0;
-      if (lane == 0) r = tc_tile(t, sm.off, off_smem, S, tile, p).r;
-      r = __shfl_sync(0xffffffffu, r, 0);
-      const int r16 = (r + 15) & ~15;
       const int ab = n & 1;
       bool got = true;
       if (lane == 0) got = mbar_wait(&sm.tempty[ab], ((n >> 1) & 1) ^ 1);
@@ -244,8 +244,9 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
         break;
       }
       tc_fence_after();
-      const uint32_t idesc = umma_idesc_f16(kTcM, r16, bf16, false);
-      const uint32_t dtm = tmem + (uint32_t)(ab * kTcN);
+      const int nmb = su.r > kTcM ? 2 : 1;   // M blocks of 128 rank rows
+      const uint32_t idesc = umma_idesc_f16(kTcM, (su.ntok + 15) & ~15, bf16, false);
+      const uint32_t dtm = tmem + (uint32_t)(ab * kShTokWide);
       for (int kb = su.kb_lo; kb < su.kb_hi; ++kb) {
         if (lane == 0) got = mbar_wait(&sm.full[stage], phase);
         if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
@@ -254,11 +255,12 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
         }
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t xa = smem_addr(sm.X[stage]), ba = smem_addr(sm.B[stage]);
+          const uint32_t xa = smem_addr(sm.st[stage]), aa = xa + (uint32_t)su.tok * kRowBytes;
 #pragma unroll
           for (int ks = 0; ks < kTcK / 16; ++ks)
-            umma_f16(dtm, umma_desc_sw128(xa + ks * 32, 16, 1024), umma_desc_sw128(ba + ks * 32, 16, 1024), idesc,
-                     (kb != su.kb_lo || ks) ? 1u : 0u);
+            for (int mb = 0; mb < nmb; ++mb)
+              umma_f16(dtm + (uint32_t)(mb * kShTokNarrow), umma_desc_sw128(aa + mb * kTcM * kRowBytes + ks * 32, 16, 1024),
+                       umma_desc_sw128(xa + ks * 32, 16, 1024), idesc, (kb != su.kb_lo || ks) ? 1u : 0u);
           umma_commit(&sm.empty[stage]);  // the stage is free once these MMAs have read it
         }
         __syncwarp();
@@ -272,51 +274,73 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
       __syncwarp();
       ++n;
     }
-  } else if (warp >= 6) {  // ------------------------------------ adapter-row loaders
+  } else if (warp >= 6) {  // ------------------------------------ x-row and A-row loaders
     const int lt = threadIdx.x - 6 * 32;    // 0 .. kShrinkLoaders - 1
     const int ch = lt & 7;                  // 16-byte chunk column of the 128-byte row
-    const int row0 = lt >> 3;               // rows row0, row0 + 16, ...
+    const int row0 = lt >> 3;               // rows row0, row0 + kLoaderRowStep, ...
     uint32_t stage = 0, phase = 0;
-    int pending = -1;                       // stage whose copies are committed, not yet announced
+    // Stages whose copies are committed but not yet announced: the last
+    // npend stages before `stage`.  Up to kLoaderLag of them stay in flight.
+    constexpr int kLoaderLag = kShrinkTcStages - 1;
+    int npend = 0;
     for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x) {
-      const ShUnit su = sh_unit(d, g);
+      const ShUnit su = sh_unit(t, sm.uoff, wide_ok, S, g);
       if (su.skip) continue;
-      const TcUnit u = tc_tile(t, sm.off, off_smem, S, su.tile, su.p);
-      const ProjDev& P = d.proj[u.p];
-      const int32_t* pt = d.page_table + (int64_t)u.a * d.pt_stride + (int64_t)u.r * P.rows_before;
-      const int nrow = (u.r - row0 + 15) >> 4;   // my rows below r (rows past r are never read back)
+      const ProjDev& P = d.proj[su.p];
+      const int32_t* pt = d.page_table + (int64_t)su.a * d.pt_stride + (int64_t)su.r * P.rows_before;
+      const int nrow = (su.r - row0 + kLoaderRowStep - 1) / kLoaderRowStep;    // my A rows below r
+      const int nxr = (su.ntok - row0 + kLoaderRowStep - 1) / kLoaderRowStep;  // my x rows below ntok
+      // my x rows (rows past the tile's end are not loaded: those
+      // accumulator columns are never read)
+      const uint16_t* xrow[kShMaxRows];
+#pragma unroll
+      for (int j = 0; j < kShMaxRows; ++j)
+        xrow[j] = j < nxr ? static_cast<const uint16_t*>(P.x) +
+                                (int64_t)__ldg(d.perm + su.j0 + row0 + kLoaderRowStep * j) * P.ldx
+                          : nullptr;
       int chunk = -1;
-      int pg[kRowsPerLoader];
+      int pg[kShMaxRows];
       for (int kb = su.kb_lo; kb < su.kb_hi; ++kb) {
         const int k0 = kb * kTcK, c = k0 / d.H, o = k0 - c * d.H;
         if (c != chunk) {  // pages of my rows for this page chunk
           chunk = c;
 #pragma unroll
-          for (int j = 0; j < kRowsPerLoader; ++j)
-            pg[j] = j < nrow ? __ldg(pt + (int64_t)(row0 + 16 * j) * P.ppi + c) : 0;
+          for (int j = 0; j < kShMaxRows; ++j)
+            pg[j] = j < nrow ? __ldg(pt + (int64_t)(row0 + kLoaderRowStep * j) * P.ppi + c) : 0;
         }
         if (!mbar_wait(&sm.empty[stage], phase ^ 1)) {
           ok = false;
           break;
         }
-        const uint32_t base = smem_addr(sm.B[stage]);
+        const uint32_t xbase = smem_addr(sm.st[stage]), abase = xbase + (uint32_t)su.tok * kRowBytes;
 #pragma unroll
-        for (int j = 0; j < kRowsPerLoader; ++j) {
+        for (int j = 0; j < kShMaxRows; ++j) {
           if (j < nrow) {
-            const int row = row0 + 16 * j;
-            cp16_shared(base + row * kRowBytes + ((ch ^ (row & 7)) << 4),
-                        d.pool + (int64_t)pg[j] * d.H + o + ch * 8);
+            const int row = row0 + kLoaderRowStep * j;
+            cp16_shared(abase + row * kRowBytes + ((ch ^ (row & 7)) << 4), d.pool + (int64_t)pg[j] * d.H + o + ch * 8);
+          }
+        }
+        // x: columns past h_in are zero-filled (A's are zero in its pages)
+        const int e = k0 + ch * 8;
+        const uint32_t xbytes = (uint32_t)min(16, max(0, 2 * (P.h_in - e)));
+#pragma unroll
+        for (int j = 0; j < kShMaxRows; ++j) {
+          if (j < nxr) {
+            const int m = row0 + kLoaderRowStep * j;
+            cp16_shared_zfill(xbase + m * kRowBytes + ((ch ^ (m & 7)) << 4), xrow[j] + (xbytes ? e : 0), xbytes);
           }
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
-        if (pending >= 0) {
-          // the previous stage's copies have landed: make them visible to the
-          // tensor cores' async proxy, then announce them
-          asm volatile("cp.async.wait_group 1;" ::: "memory");
+        if (npend == kLoaderLag) {
+          // the oldest pending stage's copies have landed (no more than
+          // kLoaderLag newer groups are outstanding): make them visible to
+          // the tensor cores' async proxy, then announce them
+          asm volatile("cp.async.wait_group %0;" ::"n"(kLoaderLag) : "memory");
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          mbar_arrive(&sm.full[pending]);
+          mbar_arrive(&sm.full[(stage + kShrinkTcStages - kLoaderLag) % kShrinkTcStages]);
+          --npend;
         }
-        pending = (int)stage;
+        ++npend;
         if (++stage == kShrinkTcStages) {
           stage = 0;
           phase ^= 1;
@@ -324,23 +348,20 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
-    if (pending >= 0 && ok) {
+    if (ok) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(&sm.full[pending]);
+      for (int i = npend; i > 0; --i) mbar_arrive(&sm.full[(stage + kShrinkTcStages - i) % kShrinkTcStages]);
     }
   } else {  // ------------------------------------------------- epilogue (warps 2-5)
-    // A split unit writes its partial sums (fp32) to its half's scratch
-    // rows; the half that finishes second (per warp: per 32 rows) adds the
-    // other half's rows to its own accumulator and writes s_a v and its
-    // 16-bit halves.  Neither half waits for the other.
-    const int quarter = warp & 3;  // TMEM lanes this warp may read
-    const int m = 32 * quarter + lane;
+    // Warp w owns TMEM lanes 32 (w % 4) .. +31: rank rows k (and k + 128 in
+    // the second M block); accumulator columns are the tile's tokens.  For
+    // each token the warp's 32 lanes write 32 consecutive ranks of its
+    // part's partial row.
+    const int quarter = warp & 3;
     int n = 0;
     for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x) {
-      const ShUnit su = sh_unit(d, g);
+      const ShUnit su = sh_unit(t, sm.uoff, wide_ok, S, g);
       if (su.skip) continue;
-      const TcUnit u = tc_tile(t, sm.off, off_smem, S, su.tile, su.p);
-      const int r16 = (u.r + 15) & ~15;
       const int ab = n & 1;
       bool got = true;
       if (lane == 0) got = mbar_wait(&sm.tfull[ab], (n >> 1) & 1);
@@ -350,90 +371,22 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
       }
       ++n;
       tc_fence_after();
-      const int j = u.j0 + m;
-      const uint32_t tacc = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(ab * kTcN);
-      bool finish = true;            // this warp writes the final v rows
-      const float* other = nullptr;  // the other half's partial row
-      if (su.split) {
-        float* mine = t.vpart + (int64_t)su.half * t.vpart_half + (int64_t)u.p * t.vpart_proj + (int64_t)j * d.v_ld;
-        for (int c00 = 0; c00 < r16; c00 += 32) {
-          uint32_t raw[32];
-          tmem_ld32_nowait(tacc + (uint32_t)c00, raw);
-          tmem_wait_ld(raw);
-          if (m < u.len) {
+      const int nmb = su.r > kTcM ? 2 : 1;
+      const uint32_t tacc = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(ab * kShTokWide);
+      // this warp's partial rows (rank rows below r)
+      if (32 * quarter < su.r || nmb == 2) {
+        float* part = t.vpart + (int64_t)su.part * t.vpart_part + (int64_t)su.p * t.vpart_proj;
+        for (int mb = 0; mb < nmb; ++mb) {
+          const int k = mb * kTcM + 32 * quarter + lane;
+          for (int c00 = 0; c00 < su.ntok; c00 += 32) {
+            uint32_t raw[32];
+            tmem_ld32_nowait(tacc + (uint32_t)(mb * kShTokNarrow + c00), raw);
+            tmem_wait_ld(raw);
+            if (k < su.r) {
+              float* dst = part + (int64_t)(su.j0 + c00) * d.v_ld + k;
 #pragma unroll
-            for (int i = 0; i < 32; i += 4)
-              if (c00 + i < u.r)
-                *reinterpret_cast<float4*>(mine + c00 + i) =
-                    make_float4(__uint_as_float(raw[i]), __uint_as_float(raw[i + 1]), __uint_as_float(raw[i + 2]),
-                                __uint_as_float(raw[i + 3]));
-          }
-        }
-        __threadfence();   // my partial rows, before the count says they are there
-        __syncwarp();
-        int old = 0;
-        int32_t* cnt = t.combine + ((int64_t)su.tile * d.nproj + u.p) * 4 + quarter;
-        if (lane == 0) old = atomicAdd(cnt, 1);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        finish = old == 1;
-        if (finish) {
-          __threadfence();   // the other half's partial rows are visible now
-          other = t.vpart + (int64_t)(1 - su.half) * t.vpart_half + (int64_t)u.p * t.vpart_proj + (int64_t)j * d.v_ld;
-          if (lane == 0) *cnt = 0;   // both halves are in: ready for the next call
-        }
-      }
-      if (finish) {
-        const float sa = d.scale ? __ldg(d.scale + u.a) : 1.f;   // the adapter's scale, applied to v
-        float* vrow = d.proj[u.p].v + (int64_t)j * d.v_ld;
-        uint16_t* hrow = t.vhi[u.p] + (int64_t)j * t.v16_ld;
-        uint16_t* lrow = t.vlo[u.p] + (int64_t)j * t.v16_ld;
-        // 32 accumulator columns per TMEM round trip
-        for (int c00 = 0; c00 < r16; c00 += 32) {
-          uint32_t raw[32];
-          tmem_ld32_nowait(tacc + (uint32_t)c00, raw);
-          tmem_wait_ld(raw);
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int c0 = c00 + 16 * hh;
-            if (m < u.len && c0 < r16) {
-              float v[16];
-              uint16_t hi[16], lo[16];
-              if (other) {
-#pragma unroll
-                for (int i = 0; i < 16; i += 4) {
-                  const float4 o4 = c0 + i < u.r ? *reinterpret_cast<const float4*>(other + c0 + i)
-                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-                  v[i] = o4.x;
-                  v[i + 1] = o4.y;
-                  v[i + 2] = o4.z;
-                  v[i + 3] = o4.w;
-                }
-              } else {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = 0.f;
-              }
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const float x = c0 + i < u.r ? sa * (__uint_as_float(raw[16 * hh + i]) + v[i]) : 0.f;
-                v[i] = x;
-                hi[i] = Elem<E>::from(x);
-                lo[i] = Elem<E>::from(x - Elem<E>::to(hi[i]));
-              }
-              // fp32 v: 16-byte stores up to the row's last multiple of 4 columns
-              // (the v row stride is a multiple of 4 floats, past r only padding)
-#pragma unroll
-              for (int i = 0; i < 16; i += 4)
-                if (c0 + i < u.r)
-                  *reinterpret_cast<float4*>(vrow + c0 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-              uint4 h0, h1, l0, l1;
-              memcpy(&h0, hi, 16);
-              memcpy(&h1, hi + 8, 16);
-              memcpy(&l0, lo, 16);
-              memcpy(&l1, lo + 8, 16);
-              *reinterpret_cast<uint4*>(hrow + c0) = h0;
-              *reinterpret_cast<uint4*>(hrow + c0 + 8) = h1;
-              *reinterpret_cast<uint4*>(lrow + c0) = l0;
-              *reinterpret_cast<uint4*>(lrow + c0 + 8) = l1;
+              for (int i = 0; i < 32; ++i)
+                if (c00 + i < su.ntok) dst[(int64_t)i * d.v_ld] = __uint_as_float(raw[i]);
             }
           }
         }
@@ -448,7 +401,72 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 2 * kTcN);
+    tmem_dealloc(tmem, kShTmemCols);
+  }
+}
+
+// ================================================================ tc_combine
+// v of the tensor-core tiles from tc_shrink's K parts: their fp32 partial rows
+// added in part order, times s_a, written as 16-bit hi and lo halves (zeros
+// from r up to the next multiple of 16, which tc_expand reads as K padding).
+// Block = 32 tokens of a 128-token tile and one projection; consecutive
+// threads take consecutive ranks of a token row, and each thread loads
+// kCombineUnroll elements' partial sums before it adds any of them.
+constexpr int kCombineThreads = 256;
+constexpr int kCombineTokens = 32;
+constexpr int kCombineUnroll = 4;
+template <class E>
+__global__ void __launch_bounds__(kCombineThreads) tc_combine_kernel(const __grid_constant__ TcDev t) {
+  const ApplyDev& d = t.a;
+  pdl_wait();
+  const int tiles = d.counts[t.tc_total_idx];
+  const int S = d.counts[kNumSegs];
+  pdl_trigger();
+  constexpr int kGroups = kTcM / kCombineTokens;
+  const int64_t nblk = (int64_t)tiles * d.nproj * kGroups;
+  for (int64_t b = blockIdx.x; b < nblk; b += gridDim.x) {
+    const int tile = (int)(b / (d.nproj * kGroups));
+    const int rem = (int)(b - (int64_t)tile * d.nproj * kGroups);
+    const int p = rem / kGroups, grp = rem - p * kGroups;
+    const int q = find_pos_tc(nullptr, t.tc_off, false, S, tile);
+    const int4 sd = __ldg(d.seg_desc + q);   // adapter, rank, start, end
+    const int j0 = sd.z + (tile - __ldg(t.tc_off + q)) * kTcM + grp * kCombineTokens;
+    const int ntok = min(kCombineTokens, sd.w - j0);
+    if (ntok <= 0) continue;
+    const int r = sd.y, r16 = (r + 15) & ~15;
+    const int nparts = min(kTcShrinkParts, (d.proj[p].h_in + kTcK - 1) / kTcK);
+    const float sa = d.scale ? __ldg(d.scale + sd.x) : 1.f;
+    const float* part0 = t.vpart + (int64_t)p * t.vpart_proj;
+    uint16_t* hbase = t.vhi[p];
+    uint16_t* lbase = t.vlo[p];
+    const int total = ntok * r16;
+    for (int base = threadIdx.x; base < total; base += kCombineUnroll * kCombineThreads) {
+      float acc[kCombineUnroll][kTcShrinkParts];
+#pragma unroll
+      for (int u = 0; u < kCombineUnroll; ++u) {
+        const int idx = base + u * kCombineThreads;
+        const int m = idx / r16, k = idx - m * r16;
+        const bool live = idx < total && k < r;
+#pragma unroll
+        for (int o = 0; o < kTcShrinkParts; ++o)
+          acc[u][o] = live && o < nparts ? part0[(int64_t)o * t.vpart_part + (int64_t)(j0 + m) * d.v_ld + k] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kCombineUnroll; ++u) {
+        const int idx = base + u * kCombineThreads;
+        if (idx < total) {
+          const int m = idx / r16, k = idx - m * r16;
+          float x = 0.f;
+#pragma unroll
+          for (int o = 0; o < kTcShrinkParts; ++o) x += acc[u][o];
+          x *= sa;
+          const int64_t j = j0 + m;
+          const uint16_t hi = Elem<E>::from(x);
+          hbase[j * t.v16_ld + k] = hi;
+          lbase[j * t.v16_ld + k] = Elem<E>::from(x - Elem<E>::to(hi));
+        }
+      }
+    }
   }
 }
 
@@ -834,8 +852,12 @@ cudaError_t prepare_tc_kernels() {
 }
 
 cudaError_t launch_tc_shrink(const TcDev& a, int dtype, int grid, cudaStream_t st) {
-  if (dtype == 0) return launch_pdl_tc(tc_shrink_kernel<__half>, grid, kShrinkTcThreads, kShrinkTcSmem, st, a);
-  return launch_pdl_tc(tc_shrink_kernel<__nv_bfloat16>, grid, kShrinkTcThreads, kShrinkTcSmem, st, a);
+  cudaError_t e = dtype == 0 ? launch_pdl_tc(tc_shrink_kernel<__half>, grid, kShrinkTcThreads, kShrinkTcSmem, st, a)
+                             : launch_pdl_tc(tc_shrink_kernel<__nv_bfloat16>, grid, kShrinkTcThreads, kShrinkTcSmem, st, a);
+  if (e != cudaSuccess) return e;
+  // the K parts' sums: eight small blocks per SM
+  return dtype == 0 ? launch_pdl_tc(tc_combine_kernel<__half>, 8 * grid, kCombineThreads, 0, st, a)
+                    : launch_pdl_tc(tc_combine_kernel<__nv_bfloat16>, 8 * grid, kCombineThreads, 0, st, a);
 }
 
 cudaError_t launch_tc_expand(const TcDev& a, int dtype, int grid, cudaStream_t st) {
