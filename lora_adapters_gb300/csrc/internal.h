@@ -139,9 +139,6 @@ inline int32_t expand_col_tiles(int32_t h_out, int32_t H) {
 struct TcDev {
   ApplyDev a;                        // projections, segments, v (fp32), error word
   CUtensorMap pool_map;              // pool as [num_pages x H], box {64, 1} (gather4 rows)
-  CUtensorMap x_map[kMaxProj];       // x of each projection as [T x h_in], box {64, 1}
-  CUtensorMap x128_map[kMaxProj];    // the same, box {64, 128} (tiles of consecutive tokens)
-  CUtensorMap x16_map[kMaxProj];     // the same, box {64, 16}
   CUtensorMap y_map[kMaxProj];       // y of each projection as [T x h_out], box {64, 1}
   CUtensorMap y128_map[kMaxProj];    // box {64, 128}
   CUtensorMap y16_map[kMaxProj];     // box {64, 16}

@@ -757,13 +757,9 @@ int slora_lora_apply_multi(slora_pool* p, const slora_segments* seg, int32_t n, 
     const size_t half_elems = (size_t)kMaxProj * rows * p->v16_ld;
     for (int i = 0; i < n; ++i) {
       const ProjDev& P = d.proj[i];
-      for (int b = 0; b < 3; ++b) {
+      for (int b = 0; b < 3; ++b) {   // y maps of tc_expand (x rows are copied with cp.async)
         const uint32_t box_rows = b == 0 ? 1 : b == 1 ? kTcM : 16;
-        CUtensorMap* mx = b == 0 ? &t.x_map[i] : b == 1 ? &t.x128_map[i] : &t.x16_map[i];
         CUtensorMap* my = b == 0 ? &t.y_map[i] : b == 1 ? &t.y128_map[i] : &t.y16_map[i];
-        if (int rc = encode_2d(mx, P.x, p->dtype, (uint64_t)P.h_in, (uint64_t)p->seg_T, (uint64_t)P.ldx * 2, kTcK,
-                               box_rows))
-          return rc;
         if (int rc = encode_2d(my, P.y, p->dtype, (uint64_t)P.h_out, (uint64_t)p->seg_T, (uint64_t)P.ldy * 2, kTcK,
                                box_rows))
           return rc;
