@@ -86,7 +86,9 @@ class TraceResult:
     tokens: int
     decode_tokens: int
     prefill_tokens: int
-    gpu_ms: float
+    gpu_ms: float                # kernel time of the path (segments + apply), from the pool's timing hooks
+    step_event_ms: float         # the steps bracketed by events; includes the GPU's waits for the host
+    load_kernel_ms: float        # the adapter loads' scatter kernels (copy stream, overlapping the steps)
     loads: int
     load_bytes: int
     evictions: int
@@ -102,7 +104,7 @@ class TraceResult:
     def summary(self) -> dict:
         d = {k: v for k, v in dataclasses.asdict(self).items() if k not in ("ops", "ranks")}
         d["tokens_per_s_per_layer"] = self.tokens / (self.gpu_ms * 1e-3) if self.gpu_ms > 0 else None
-        d["load_gbs"] = self.load_bytes / (self.gpu_ms * 1e-3) / 1e9 if self.gpu_ms > 0 else None
+        d["load_gbs_over_gpu_time"] = self.load_bytes / (self.gpu_ms * 1e-3) / 1e9 if self.gpu_ms > 0 else None
         d["adapter_hit_rate"] = self.adapter_hits / max(1, self.adapter_hits + self.adapter_misses)
         return d
 
@@ -256,8 +258,14 @@ class Trace:
         tokens = dec_tokens = pre_tokens = 0
         running_sum = 0
         peak_kv = 0
-        gpu_ms = 0.0
+        gpu_ms = step_ms = load_ms = 0.0
         events = []
+        if self.device is not None:
+            # per-kernel events around every launch: the GPU time of the path
+            # itself, which the step events overstate whenever the GPU waits
+            # for the host between launches
+            slora.slora_timing_enable(self.pool.handle, True)
+            slora.slora_timing_read(self.pool.handle)   # (reading also resets the counters)
         t0 = time.perf_counter()
         for step in range(steps):
             # arrivals
@@ -366,11 +374,15 @@ class Trace:
             import torch
 
             torch.cuda.synchronize()
-            gpu_ms = sum(a.elapsed_time(b) for a, b in events)
+            step_ms = sum(a.elapsed_time(b) for a, b in events)
+            tm = slora.slora_timing_read(self.pool.handle)
+            slora.slora_timing_enable(self.pool.handle, False)
+            gpu_ms = sum(ms for k, (ms, _) in tm.items() if k != "scatter")
+            load_ms = tm.get("scatter", (0.0, 0))[0]
             st = self.pool.status()
             if st != slora.OK:
                 raise RuntimeError(f"device status {st} after the trace")
-        return TraceResult(steps, tokens, dec_tokens, pre_tokens, gpu_ms, self.loads, self.load_bytes,
+        return TraceResult(steps, tokens, dec_tokens, pre_tokens, gpu_ms, step_ms, load_ms, self.loads, self.load_bytes,
                            self.evictions, hits, misses, finished, running_sum / max(1, steps), peak_kv,
                            list(self.ops), self.ranks.copy(), time.perf_counter() - t0)
 
