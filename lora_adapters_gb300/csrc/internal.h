@@ -22,11 +22,11 @@ constexpr int kExpandCols = kCcConsumerWarps * 32 * 8;  // 8 output columns (16 
 constexpr int kSegSmem = 1536;         // work-list prefix entries searched in shared memory
 constexpr int kSegThreads = 1024;
 
-// Tensor-core (tcgen05) kernels: M tile of tokens, K block (one 128-byte
-// swizzle row of 16-bit elements), expand N tile of output columns.
+// Tensor-core (tcgen05) kernels: 128-token tiles of the work lists (the M
+// side of tc_expand, half a tc_shrink tile), K block (one 128-byte swizzle row
+// of 16-bit elements).
 constexpr int kTcM = 128;
 constexpr int kTcK = 64;
-constexpr int kTcN = 256;
 constexpr int kTcShrinkParts = 2;        // K parts of one tc_shrink (tile, projection)
 
 // Indices into SegDev::counts.

@@ -58,28 +58,6 @@ __device__ __forceinline__ int find_pos_tc(const int32_t* s_off, const int32_t* 
   return lo;
 }
 
-struct TcUnit {
-  int p, j0, len, r, a, seg;
-};
-
-// Tile `tile` of the long-segment list: segment (in work order) and row range.
-__device__ __forceinline__ TcUnit tc_tile(const TcDev& t, const int32_t* s_off, bool in_smem, int S, int tile,
-                                          int p) {
-  const ApplyDev& d = t.a;
-  TcUnit u;
-  const int q = find_pos_tc(s_off, t.tc_off, in_smem, S, tile);
-  const int mt = tile - (in_smem ? s_off[q] : __ldg(t.tc_off + q));
-  const int s = __ldg(d.seg_order + q);
-  const int start = __ldg(d.seg_start + s), end = __ldg(d.seg_start + s + 1);
-  u.p = p;
-  u.j0 = start + mt * kTcM;
-  u.len = min(kTcM, end - u.j0);
-  u.r = __ldg(d.seg_rank + s);
-  u.a = __ldg(d.seg_adapter + s);
-  u.seg = s;
-  return u;
-}
-
 template <class T>
 struct Elem;
 template <>
@@ -417,20 +395,25 @@ constexpr int kCombineTokens = 32;
 constexpr int kCombineUnroll = 4;
 template <class E>
 __global__ void __launch_bounds__(kCombineThreads) tc_combine_kernel(const __grid_constant__ TcDev t) {
+  __shared__ int32_t s_off[kSegSmem];   // the tile list's prefix, searched here when it fits
   const ApplyDev& d = t.a;
   pdl_wait();
   const int tiles = d.counts[t.tc_total_idx];
   const int S = d.counts[kNumSegs];
   pdl_trigger();
+  const bool off_smem = S + 1 <= kSegSmem;
+  if (off_smem)
+    for (int i = threadIdx.x; i <= S; i += kCombineThreads) s_off[i] = __ldg(t.tc_off + i);
+  __syncthreads();
   constexpr int kGroups = kTcM / kCombineTokens;
   const int64_t nblk = (int64_t)tiles * d.nproj * kGroups;
   for (int64_t b = blockIdx.x; b < nblk; b += gridDim.x) {
     const int tile = (int)(b / (d.nproj * kGroups));
     const int rem = (int)(b - (int64_t)tile * d.nproj * kGroups);
     const int p = rem / kGroups, grp = rem - p * kGroups;
-    const int q = find_pos_tc(nullptr, t.tc_off, false, S, tile);
+    const int q = find_pos_tc(s_off, t.tc_off, off_smem, S, tile);
     const int4 sd = __ldg(d.seg_desc + q);   // adapter, rank, start, end
-    const int j0 = sd.z + (tile - __ldg(t.tc_off + q)) * kTcM + grp * kCombineTokens;
+    const int j0 = sd.z + (tile - (off_smem ? s_off[q] : __ldg(t.tc_off + q))) * kTcM + grp * kCombineTokens;
     const int ntok = min(kCombineTokens, sd.w - j0);
     if (ntok <= 0) continue;
     const int r = sd.y, r16 = (r + 15) & ~15;
@@ -510,11 +493,11 @@ __device__ __forceinline__ TcEUnit tc_eunit(const TcDev& t, int64_t g, int per_s
   u.p = 0;
   while (nt >= t.tc_ncol[u.p]) nt -= t.tc_ncol[u.p++];
   u.ntm = __ldg(t.tc_off + q + 1) - __ldg(t.tc_off + q);
-  const int s = __ldg(d.seg_order + q);
-  u.start = __ldg(d.seg_start + s);
-  u.len = __ldg(d.seg_start + s + 1) - u.start;
-  u.r = __ldg(d.seg_rank + s);
-  u.a = __ldg(d.seg_adapter + s);
+  const int4 sd = __ldg(d.seg_desc + q);   // adapter, rank, start, end
+  u.start = sd.z;
+  u.len = sd.w - sd.z;
+  u.r = sd.y;
+  u.a = sd.x;
   for (u.c = 0;; ++u.c) {  // column tile within one page chunk
     const int lenc = min(d.H, d.proj[u.p].h_out - u.c * d.H);
     const int n = (lenc + kTcNe - 1) / kTcNe;
