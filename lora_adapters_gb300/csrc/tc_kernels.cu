@@ -3,26 +3,27 @@
 // A segment of many tokens on one adapter turns the per-token products into
 // dense contractions ("S-LoRA: Serving Thousands of Concurrent LoRA
 // Adapters": heterogeneous batching runs custom kernels directly on the
-// non-contiguous pool; the pages give no kernel internals).  Per work unit a
-// 128-token tile of one segment is multiplied on the 5th-generation tensor
-// cores, fp16/bf16 operands from shared memory, fp32 accumulators in TMEM:
+// non-contiguous pool; the pages give no kernel internals).  Tiles of one
+// segment are multiplied on the 5th-generation tensor cores, fp16/bf16
+// operands from shared memory, fp32 accumulators in TMEM:
 //
-//   tc_shrink:  V[128 x r] = X[128 x H_in] . A^T   (A rows = pages, K-major)
-//   tc_expand:  Y[128 x 256] += s * (V_hi + V_lo)[128 x r] . B[r x 256]
+//   tc_shrink:  V^T[r x 256] = A[r x H_in] . X^T   (A rows = pages; rank on M, tokens on N)
+//   tc_combine: V = s_a (part 0 + part 1), written as V_hi and V_lo
+//   tc_expand:  Y[128 x 128] += s * (V_hi + V_lo)[128 x r] . B[r x 128]
 //
-// Operands are gathered by the TMA engine straight from where they live:
-// token rows of x by `tile::gather4` through the segment's sorted token list,
-// adapter rows by `gather4` over the page pool viewed as a [pages x H] matrix,
-// v rows (consecutive in sorted order) by 2-D tiles; all land in shared
-// memory in the 128-byte-swizzled layout the MMA reads.  V is carried as two
-// 16-bit halves, V_hi = round(v) and V_lo = round(v - V_hi), so the expand
-// multiplies with ~fp32 accuracy on 16-bit tensor cores.
+// tc_shrink copies token rows of x and adapter rows of A with cp.async into
+// the 128-byte-swizzled layout the MMA reads; tc_expand gathers B rows with
+// the TMA engine (`tile::gather4` over the page pool viewed as a [pages x H]
+// matrix) and loads v and y tiles as 2-D boxes or row gathers.  V is carried
+// as two 16-bit halves, V_hi = round(v) and V_lo = round(v - V_hi), so the
+// expand multiplies with ~fp32 accuracy on 16-bit tensor cores.
 //
-// Each kernel is persistent (one CTA per SM) and warp-specialised: warp 0
-// issues copies into a ring of shared-memory stages, warp 1 owns TMEM and
-// issues the MMAs (one thread), warps 2-5 drain a TMEM accumulator (two of
-// them, so the epilogue of one unit overlaps the MMAs of the next) and write
-// v or y.  Every wait is bounded (SLORA_ERR_TIMEOUT on give-up).
+// tc_shrink and tc_expand are persistent (one CTA per SM) and warp-
+// specialised: copy warps fill a ring of shared-memory stages, warp 1 owns
+// TMEM and issues the MMAs (one thread), the epilogue warps drain TMEM
+// accumulators (more than one, so the epilogue of one tile overlaps the MMAs
+// of the next) and write partial sums of v or y.  Every wait is bounded
+// (SLORA_ERR_TIMEOUT on give-up).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
