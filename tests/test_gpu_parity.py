@@ -37,6 +37,14 @@ SMALL = {
         name="prefill_bigrank", H=256, dtype="f16", projections=workloads._qkvo(256),
         num_adapters=5, rank_set=(129, 200, 256, 64), kind="prefill", requests=7, prompt_len=(1, 260),
         pool_factor=1.2, s=0.75, seed=8),
+    # one K block in the first projection (no K split in tc_shrink, x columns
+    # past h_in zero-filled), ranks on both sides of 128, runs longer than a
+    # 256-token tile
+    "short_k_f16": workloads.WorkloadSpec(
+        name="short_k", H=64, dtype="f16",
+        projections=(workloads.Projection("a", 48, 200), workloads.Projection("b", 200, 48)),
+        num_adapters=6, rank_set=(3, 40, 130, 17), kind="prefill", requests=6, prompt_len=(1, 600),
+        pool_factor=1.3, s=0.9, seed=14),
     "many_tokens_f16": workloads.WorkloadSpec(
         name="many_tokens", H=128, dtype="f16", projections=(workloads.Projection("q", 128, 136),),
         num_adapters=300, rank_set=(2, 8, 24), kind="decode", tokens=3001, popularity="uniform",
