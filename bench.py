@@ -241,6 +241,50 @@ def run_reference(args, wl, cfg):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- replicas
+class Replicas:
+    """N independent replicas of the path, one process per GPU (the path has
+    no exchange step, so no collective touches the data): rank and world from
+    the launcher's environment, a barrier around each timed region, the
+    maximum over ranks of a time, and the whole-job rate (units of all ranks
+    divided by that time)."""
+
+    def __init__(self, backend: str, device=None):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.device = device
+        self.dist = None
+        if self.world > 1:
+            import torch.distributed as dist
+
+            if backend == "nccl":
+                dist.init_process_group("nccl", device_id=device)
+            else:
+                dist.init_process_group(backend)
+            self.dist = dist
+
+    def barrier(self) -> None:
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def max(self, v: float) -> float:
+        if self.dist is None:
+            return v
+        import torch
+
+        t = torch.tensor([v], dtype=torch.float64, device=self.device)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def rate(self, units_per_rank: float, seconds: float) -> float:
+        return self.world * units_per_rank / seconds
+
+    def close(self) -> None:
+        if self.dist is not None:
+            self.dist.destroy_process_group()
+            self.dist = None
+
+
 # ---------------------------------------------------------------- GPU arm
 def main():
     ap = argparse.ArgumentParser()
@@ -281,10 +325,7 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("nccl", device_id=device)
+    rep = Replicas("nccl", device)
     mode = {"auto": slora.MODE_AUTO, "decode": slora.MODE_DECODE, "prefill": slora.MODE_PREFILL}[args.mode]
 
     pool, ta, xs, ys, y0 = setup_device(wl, device)
@@ -311,8 +352,7 @@ def main():
     # ---- device-timed steps (inputs resident in HBM; per-kernel hooks off)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
+    rep.barrier()
     torch.cuda.synchronize()
     clocks = ClockSampler(_gpu_id(torch))
     wall0 = time.perf_counter()
@@ -325,15 +365,10 @@ def main():
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
     clk = clocks.stop()
-    if world > 1:
-        torch.distributed.barrier()
+    rep.barrier()
     ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
-    ms_step = ms / args.steps
-    if world > 1:
-        t = torch.tensor([ms_step], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
-    value = world * wl.T / (ms_step * 1e-3)
+    ms_step = rep.max(ms / args.steps)
+    value = rep.rate(wl.T, ms_step * 1e-3)
 
 
     # ---- per-kernel durations: the same steps again, each kernel bracketed by
@@ -426,6 +461,7 @@ def main():
     for k in range(args.warmup):
         e2e_step(k)
     torch.cuda.synchronize()
+    rep.barrier()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
@@ -443,11 +479,9 @@ def main():
         for a_, b_ in zip(out_y[0], out_y[1]):
             if not torch.equal(a_, b_):
                 raise RuntimeError("pipelined end-to-end steps disagree")
-    if world > 1:
-        t = torch.tensor([e_ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e_ms = float(t.item())
-    e2e = {"value": world * wl.T / (e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+    rep.barrier()
+    e_ms = rep.max(e_ms)
+    e2e = {"value": rep.rate(wl.T, e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
            "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms,
            "pipelining": "inputs of step k+1 in and step k-1's y out while step k computes", "l2": "not flushed"}
 
@@ -476,8 +510,7 @@ def main():
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
                 "gpu_launches": launches, "wall_s_timed_region": wall}
         print(json.dumps(line), flush=True)
-    if world > 1:
-        torch.distributed.destroy_process_group()
+    rep.close()
 
 
 if __name__ == "__main__":
