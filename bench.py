@@ -291,7 +291,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference", "bmm"],
+                    help="bmm: the padded batched-matmul comparator through slora_lora_apply_bmm")
     ap.add_argument("--workload", default="llama7b_decode")
     ap.add_argument("--mode", default="decode", choices=["auto", "decode", "prefill"])
     ap.add_argument("--ref-tokens", type=int, default=24)
@@ -343,7 +344,11 @@ def main():
 
     def step():
         seg = pool.build_segments(ta)
-        pool.apply_multi(seg, projs, xs, ys, sp.s, mode)
+        if args.impl == "bmm":
+            for p_ in projs:
+                pool.apply_bmm(seg, p_, xs[p_], ys[p_], sp.s)
+        else:
+            pool.apply_multi(seg, projs, xs, ys, sp.s, mode)
 
     for _ in range(args.warmup):
         step()
@@ -370,6 +375,25 @@ def main():
     ms_step = rep.max(ms / args.steps)
     value = rep.rate(wl.T, ms_step * 1e-3)
 
+
+    if args.impl == "bmm":
+        # the comparator: step time and the same algorithmic bytes only
+        ab = algorithmic_bytes(wl, None)
+        hbm_peak = _peaks()[0]
+        rep.close()
+        if rank == 0:
+            print(json.dumps({
+                "impl": "bmm", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": sp.dtype, "data": "synthetic", "config": cfg,
+                "comparator": "every token's rows gathered and padded to the pool's max rank, two cuBLAS "
+                              "strided-batched GEMMs, one rounding",
+                "scratch_bytes": slora.slora_bmm_scratch_bytes(pool.handle),
+                "step_algorithmic_bytes": ab["step"],
+                "step_frac_of_hbm": ab["step"] / (ms_step * 1e-3) / 1e9 / hbm_peak,
+                "clocks": clk, "gpu_launches": (1 + 3 * n) * args.steps}), flush=True)
+        pool.close()
+        return
 
     # ---- per-kernel durations: the same steps again, each kernel bracketed by
     # events on the compute stream (this serialises the launches a little, so

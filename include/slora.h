@@ -220,6 +220,27 @@ int slora_lora_apply_multi(slora_pool* pool, const slora_segments* seg, int32_t 
                            void* const* d_y, const int64_t* ldy, float s, int32_t mode);
 
 /*
+ * Comparator: the same delta by the "traditional batched matmul" variant
+ * that the pages compare S-LoRA with (dongaigc.com summary, section
+ * "S-LoRA的性能评估": S-LoRA against its own variants, one without unified
+ * memory, one with traditional batched matrix multiplication).  Every token's
+ * adapter rows are gathered out of the pool into dense tensors padded to the
+ * pool's max_rank (zeros past the adapter's rank), two cuBLAS strided-batched
+ * GEMMs give (x_t A) B per token (fp32 accumulation, v kept in fp32), and
+ * y_t += s * s_a * delta_t is rounded once.  Arguments and errors as
+ * slora_lora_apply (one projection; no mode).  Scratch: on the first call
+ * the pool allocates max_tokens * max_rank * (2 * max h_in + 4 * max h_out)
+ * bytes and a little more (slora_bmm_scratch_bytes reports it), freed with
+ * the pool; SLORA_ERR_OOM if it cannot.  cuBLAS is opened on the first call
+ * (SLORA_ERR_CUDA when it is not installed); nothing else in the library
+ * needs it.  For measurement and comparison, not for serving.
+ */
+int slora_lora_apply_bmm(slora_pool* pool, const slora_segments* seg, int32_t proj, const void* d_x,
+                         int64_t ldx, void* d_y, int64_t ldy, float s);
+/* Bytes of comparator scratch the pool holds (0 before the first call). */
+int slora_bmm_scratch_bytes(const slora_pool* pool, size_t* bytes);
+
+/*
  * Synchronises the compute stream, returns in *status the first error a
  * kernel reported since the last call (SLORA_OK, SLORA_ERR_NOT_RESIDENT for a
  * token naming an adapter that is not loaded, SLORA_ERR_INVALID for an id

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJ_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libslora.so")
-SOURCES = ["pool.cpp", "kernels.cu", "tc_kernels.cu", "noalloc.cu"]
+SOURCES = ["pool.cpp", "kernels.cu", "tc_kernels.cu", "noalloc.cu", "bmm.cu"]
 HEADERS = [os.path.join(CSRC, "internal.h"), os.path.join(ROOT, "include", "slora.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
@@ -60,7 +60,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
                 print(res.stderr, file=sys.stderr)
     if force or jobs or _stale(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
+        cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static", "-ldl"]
         res = run(cmd)
         if res.returncode != 0:
             raise RuntimeError(f"link failed: {' '.join(cmd)}\n{res.stdout}\n{res.stderr}")

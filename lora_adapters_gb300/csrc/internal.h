@@ -172,6 +172,32 @@ struct ScatterDev {
   int32_t entry_base[kMaxProj];  // first page-table entry of projection q
 };
 
+// The padded batched-matmul comparator (bmm.cu): one projection.
+struct BmmDev {
+  const uint16_t* pool;
+  const int32_t* page_table;
+  int64_t pt_stride;
+  int32_t H;
+  const int32_t* perm;
+  const int32_t* seg_start;
+  const int32_t* seg_adapter;
+  const int32_t* seg_rank;
+  const int32_t* counts;
+  const float* scale;            // per adapter id: s_a (NULL: 1)
+  int32_t T;                     // tokens of the batch
+  int32_t r_pad;                 // every adapter padded to this rank
+  int32_t h_in, h_out, ppi, ppo, rows_before;
+  int32_t* tok_seg;              // [T] segment of each token, -1: none
+  uint16_t* a_pad;               // [T][r_pad][h_in], as stored
+  float* b_pad;                  // [T][r_pad][h_out]
+  float* delta;                  // [T][h_out] = (x A) B per token (cuBLAS)
+  void* y;
+  int64_t ldy;
+  float s;
+};
+cudaError_t launch_bmm_gather(const BmmDev& d, int dtype, int grid, cudaStream_t st);
+cudaError_t launch_bmm_epilogue(const BmmDev& d, int dtype, int grid, cudaStream_t st);
+
 // Launchers (kernels.cu).  dtype: 0 = fp16, 1 = bf16.
 cudaError_t launch_build_segments(const SegBuildArgs& a, cudaStream_t st);
 // The CUDA-core apply (shrink units, grid barrier, expand units); grid = SMs,

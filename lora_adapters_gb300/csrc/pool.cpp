@@ -10,9 +10,11 @@
 // abstract): one cudaMemcpyAsync per weight block into a device staging
 // buffer on the copy stream, then a scatter kernel that writes each row chunk
 // to its page; the compute stream waits on the load's event before using it.
+#include <cublas_v2.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
+#include <dlfcn.h>
 
 #include <algorithm>
 #include <climits>
@@ -21,6 +23,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <string>
 #include <vector>
@@ -108,6 +111,10 @@ struct slora_pool {
   int grid_cc = 0;
   // tensor-core path (page size a multiple of kTcK)
   bool tc_ok = false;
+  // padded batched-matmul comparator: cuBLAS handle and scratch, made on first use
+  cublasHandle_t cublas = nullptr;
+  void* d_bmm = nullptr;
+  size_t bmm_bytes = 0;
   int32_t v16_ld = 0;            // row stride of the 16-bit v halves
   uint16_t* d_v16 = nullptr;     // v_hi then v_lo, [kMaxProj][max_tokens][v16_ld] each
   float* d_vpart = nullptr;      // tc_shrink's K-part partial sums, [kTcShrinkParts][kMaxProj][rows][v_ld]
@@ -266,6 +273,37 @@ int wait_pending_loads(slora_pool* p) {
   return SLORA_OK;
 }
 
+// cuBLAS, opened on first use of the comparator only: the library itself
+// does not depend on it.
+struct CublasApi {
+  bool ok = false;
+  cublasStatus_t (*create)(cublasHandle_t*) = nullptr;
+  cublasStatus_t (*destroy)(cublasHandle_t) = nullptr;
+  cublasStatus_t (*set_stream)(cublasHandle_t, cudaStream_t) = nullptr;
+  cublasStatus_t (*gemm_sb)(cublasHandle_t, cublasOperation_t, cublasOperation_t, int, int, int, const void*,
+                            const void*, cudaDataType, int, long long, const void*, cudaDataType, int, long long,
+                            const void*, void*, cudaDataType, int, long long, int, cublasComputeType_t,
+                            cublasGemmAlgo_t) = nullptr;
+};
+const CublasApi& cublas_api() {
+  static CublasApi api;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    const char* names[] = {"libcublas.so.13", "libcublas.so", "/usr/local/cuda/lib64/libcublas.so.13",
+                           "/usr/local/cuda/lib64/libcublas.so"};
+    void* h = nullptr;
+    for (const char* n : names)
+      if ((h = dlopen(n, RTLD_NOW | RTLD_GLOBAL)) != nullptr) break;
+    if (!h) return;
+    api.create = reinterpret_cast<decltype(api.create)>(dlsym(h, "cublasCreate_v2"));
+    api.destroy = reinterpret_cast<decltype(api.destroy)>(dlsym(h, "cublasDestroy_v2"));
+    api.set_stream = reinterpret_cast<decltype(api.set_stream)>(dlsym(h, "cublasSetStream_v2"));
+    api.gemm_sb = reinterpret_cast<decltype(api.gemm_sb)>(dlsym(h, "cublasGemmStridedBatchedEx"));
+    api.ok = api.create && api.destroy && api.set_stream && api.gemm_sb;
+  });
+  return api;
+}
+
 void free_device(slora_pool* p) {
   if (p->planning) {
     std::free(p->pt_h);
@@ -290,6 +328,8 @@ void free_device(slora_pool* p) {
   cudaFree(p->d_v16);
   cudaFree(p->d_vpart);
   cudaFree(p->d_staging);
+  cudaFree(p->d_bmm);
+  if (p->cublas) cublas_api().destroy(p->cublas);
   if (p->pt_h) cudaFreeHost(p->pt_h);
   if (p->rank_pin) cudaFreeHost(p->rank_pin);
 }
@@ -808,6 +848,95 @@ int slora_lora_apply(slora_pool* p, const slora_segments* seg, int32_t proj, con
   const void* xs[1] = {d_x};
   void* ys[1] = {d_y};
   return slora_lora_apply_multi(p, seg, 1, &proj, xs, &ldx, ys, &ldy, s, mode);
+}
+
+int slora_lora_apply_bmm(slora_pool* p, const slora_segments* seg, int32_t proj, const void* d_x, int64_t ldx,
+                         void* d_y, int64_t ldy, float s) {
+  if (int rc = check_device_pool(p)) return rc;
+  if (!seg || seg->generation != p->seg_generation || seg->generation == 0)
+    return fail(SLORA_ERR_INVALID, "segments are missing or stale (rebuild them after every build call)");
+  if (proj < 0 || proj >= p->num_proj) return fail(SLORA_ERR_INVALID, "projection %d out of range", proj);
+  if (p->seg_T > 0 && (!d_x || !d_y)) return fail(SLORA_ERR_INVALID, "NULL x or y");
+  if ((reinterpret_cast<uintptr_t>(d_x) | reinterpret_cast<uintptr_t>(d_y)) & 15)
+    return fail(SLORA_ERR_INVALID, "x and y must be 16-byte aligned");
+  if (ldx < p->proj_in[proj] || ldx % 8 || ldy < p->proj_out[proj] || ldy % 8)
+    return fail(SLORA_ERR_INVALID, "row strides must be multiples of 8 and cover the row");
+  if (p->seg_T == 0) return SLORA_OK;
+  const CublasApi& cb = cublas_api();
+  if (!cb.ok) return fail(SLORA_ERR_CUDA, "cuBLAS could not be opened");
+  const int T = p->seg_T, r_pad = p->max_rank;
+  const int h_in = p->proj_in[proj], h_out = p->proj_out[proj];
+  if (!p->d_bmm) {   // sized for the largest batch and projection of the pool
+    int32_t mi = 0, mo = 0;
+    for (int q = 0; q < p->num_proj; ++q) {
+      mi = std::max(mi, p->proj_in[q]);
+      mo = std::max(mo, p->proj_out[q]);
+    }
+    const size_t Tm = (size_t)std::max(p->max_tokens, 1);
+    const size_t bytes = Tm * r_pad * mi * 2 + Tm * r_pad * mo * 4 + Tm * r_pad * 4 + Tm * mo * 4 + Tm * 4 + 64;
+    if (cudaMalloc(&p->d_bmm, bytes) != cudaSuccess) {
+      p->d_bmm = nullptr;
+      cudaGetLastError();
+      return fail(SLORA_ERR_OOM, "comparator scratch of %zu bytes", bytes);
+    }
+    p->bmm_bytes = bytes;
+  }
+  if (!p->cublas) {
+    if (cb.create(&p->cublas) != CUBLAS_STATUS_SUCCESS) {
+      p->cublas = nullptr;
+      return fail(SLORA_ERR_CUDA, "cublasCreate failed");
+    }
+  }
+  if (cb.set_stream(p->cublas, p->compute) != CUBLAS_STATUS_SUCCESS) return fail(SLORA_ERR_CUDA, "cublasSetStream failed");
+  BmmDev d{};
+  d.pool = p->d_pool;
+  d.page_table = p->d_pt;
+  d.pt_stride = p->pt_stride;
+  d.H = p->H;
+  d.perm = p->seg.perm;
+  d.seg_start = p->seg.seg_start;
+  d.seg_adapter = p->seg.seg_adapter;
+  d.seg_rank = p->seg.seg_rank;
+  d.counts = p->seg.counts;
+  d.scale = p->d_scale;
+  d.T = T;
+  d.r_pad = r_pad;
+  d.h_in = h_in;
+  d.h_out = h_out;
+  d.ppi = p->ppi[proj];
+  d.ppo = p->ppo[proj];
+  d.rows_before = p->rows_before[proj];
+  char* q = static_cast<char*>(p->d_bmm);
+  d.a_pad = reinterpret_cast<uint16_t*>(q); q += (size_t)T * r_pad * h_in * 2;
+  d.b_pad = reinterpret_cast<float*>(q); q += (size_t)T * r_pad * h_out * 4;
+  float* v = reinterpret_cast<float*>(q); q += (size_t)T * r_pad * 4;
+  d.delta = reinterpret_cast<float*>(q); q += (size_t)T * h_out * 4;
+  d.tok_seg = reinterpret_cast<int32_t*>(q);
+  d.y = d_y;
+  d.ldy = ldy;
+  d.s = s;
+  CUDA_TRY(launch_bmm_gather(d, p->dtype, p->grid_cc, p->compute));
+  const cudaDataType t16 = p->dtype == SLORA_F16 ? CUDA_R_16F : CUDA_R_16BF;
+  const float one = 1.f, zero = 0.f;
+  // v_t[r_pad] = A_t (x_t): a_pad[t] is [r_pad][h_in] row-major, i.e. h_in x r_pad column-major
+  if (cb.gemm_sb(p->cublas, CUBLAS_OP_T, CUBLAS_OP_N, r_pad, 1, h_in, &one, d.a_pad, t16, h_in,
+                 (long long)r_pad * h_in, d_x, t16, (int)ldx, (long long)ldx, &zero, v, CUDA_R_32F, r_pad,
+                 (long long)r_pad, T, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
+    return fail(SLORA_ERR_CUDA, "batched GEMM (x A) failed");
+  // delta_t[h_out] = B_t^T v_t: b_pad[t] is [r_pad][h_out] row-major, i.e. h_out x r_pad column-major
+  if (cb.gemm_sb(p->cublas, CUBLAS_OP_N, CUBLAS_OP_N, h_out, 1, r_pad, &one, d.b_pad, CUDA_R_32F, h_out,
+                 (long long)r_pad * h_out, v, CUDA_R_32F, r_pad, (long long)r_pad, &zero, d.delta, CUDA_R_32F,
+                 h_out, (long long)h_out, T, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT) != CUBLAS_STATUS_SUCCESS)
+    return fail(SLORA_ERR_CUDA, "batched GEMM (v B) failed");
+  CUDA_TRY(launch_bmm_epilogue(d, p->dtype, p->grid_cc, p->compute));
+  return SLORA_OK;
+}
+
+int slora_bmm_scratch_bytes(const slora_pool* p, size_t* bytes) {
+  if (int rc = check_pool(p)) return rc;
+  if (!bytes) return fail(SLORA_ERR_INVALID, "bytes is NULL");
+  *bytes = p->bmm_bytes;
+  return SLORA_OK;
 }
 
 int slora_device_status(slora_pool* p, int32_t* status) {

@@ -37,6 +37,7 @@ EXPORTED = (
     "slora_build_segments", "slora_lora_apply", "slora_lora_apply_multi", "slora_device_status",
     "slora_pool_snapshot", "slora_timing_enable", "slora_timing_read", "slora_set_tc_threshold",
     "slora_last_error_string", "slora_lora_apply_noalloc", "slora_adapter_set_scale",
+    "slora_lora_apply_bmm", "slora_bmm_scratch_bytes",
 )
 
 
@@ -69,6 +70,8 @@ _SIGS = {
     "slora_build_segments": [P, P, I32, ctypes.POINTER(slora_segments)],
     "slora_lora_apply": [P, ctypes.POINTER(slora_segments), I32, P, I64, P, I64, ctypes.c_float, I32],
     "slora_lora_apply_multi": [P, ctypes.POINTER(slora_segments), I32, P, P, P, P, P, ctypes.c_float, I32],
+    "slora_lora_apply_bmm": [P, ctypes.POINTER(slora_segments), I32, P, I64, P, I64, ctypes.c_float],
+    "slora_bmm_scratch_bytes": [P, ctypes.POINTER(ctypes.c_size_t)],
     "slora_device_status": [P, P],
     "slora_pool_snapshot": [P, P, ctypes.POINTER(ctypes.c_size_t)],
     "slora_timing_enable": [P, I32],
@@ -185,6 +188,17 @@ def slora_lora_apply(pool: int, seg: slora_segments, proj: int, d_x: int, ldx: i
                      s: float, mode: int = MODE_AUTO) -> None:
     _check(lib().slora_lora_apply(pool, ctypes.byref(seg), proj, d_x, ldx, d_y, ldy, s, mode),
            "slora_lora_apply")
+
+
+def slora_lora_apply_bmm(pool: int, seg: slora_segments, proj: int, d_x: int, ldx: int, d_y: int, ldy: int,
+                         s: float) -> None:
+    _check(lib().slora_lora_apply_bmm(pool, ctypes.byref(seg), proj, d_x, ldx, d_y, ldy, s), "slora_lora_apply_bmm")
+
+
+def slora_bmm_scratch_bytes(pool: int) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().slora_bmm_scratch_bytes(pool, ctypes.byref(n)), "slora_bmm_scratch_bytes")
+    return n.value
 
 
 def slora_lora_apply_multi(pool: int, seg: slora_segments, projs: Sequence[int], d_x: Sequence[int],
@@ -349,6 +363,10 @@ class Pool:
 
     def apply(self, seg, proj: int, x, y, s: float, mode: int = MODE_AUTO) -> None:
         slora_lora_apply(self.handle, seg, proj, x.data_ptr(), x.stride(0), y.data_ptr(), y.stride(0), s, mode)
+
+    def apply_bmm(self, seg, proj: int, x, y, s: float) -> None:
+        """The padded batched-matmul comparator (slora_lora_apply_bmm)."""
+        slora_lora_apply_bmm(self.handle, seg, proj, x.data_ptr(), x.stride(0), y.data_ptr(), y.stride(0), s)
 
     def apply_multi(self, seg, projs, xs, ys, s: float, mode: int = MODE_AUTO) -> None:
         slora_lora_apply_multi(self.handle, seg, list(projs), [x.data_ptr() for x in xs],

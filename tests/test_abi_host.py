@@ -157,6 +157,11 @@ def test_argument_validation(S):
     with pytest.raises(S.SloraError) as e:
         S.slora_build_segments(h, 0, 0)                                      # planning pool: no GPU work
     assert e.value.code == S.ERR_INVALID
+    seg = S.slora_segments()
+    with pytest.raises(S.SloraError) as e:
+        S.slora_lora_apply_bmm(h, seg, 0, 0, 256, 0, 256, 1.0)             # the comparator: GPU only
+    assert e.value.code == S.ERR_INVALID
+    assert S.slora_bmm_scratch_bytes(h) == 0
     with pytest.raises(S.SloraError) as e:
         S.slora_adapter_load(h, 4, 2, None, None)
     assert e.value.code == S.ERR_INVALID
