@@ -78,6 +78,8 @@ class Request:
     generated: int = 0
     kv_handles: List[str] = dataclasses.field(default_factory=list)
     admitted_step: int = -1
+    arrived_step: int = 0
+    missed: bool = False         # its adapter was not resident (or still loading) when it arrived
 
 
 @dataclasses.dataclass
@@ -92,8 +94,11 @@ class TraceResult:
     loads: int
     load_bytes: int
     evictions: int
-    adapter_hits: int
-    adapter_misses: int
+    admitted: int                # requests admitted into the batch
+    arrival_misses: int          # arrivals whose adapter was not resident yet
+    arrivals: int
+    wait_steps_hit: float        # mean steps from arrival to admission, adapter resident on arrival
+    wait_steps_miss: float       # the same for arrivals that had to wait for a load (the stall)
     finished: int
     mean_running: float
     peak_kv_pages: int
@@ -105,7 +110,7 @@ class TraceResult:
         d = {k: v for k, v in dataclasses.asdict(self).items() if k not in ("ops", "ranks")}
         d["tokens_per_s_per_layer"] = self.tokens / (self.gpu_ms * 1e-3) if self.gpu_ms > 0 else None
         d["load_gbs_over_gpu_time"] = self.load_bytes / (self.gpu_ms * 1e-3) / 1e9 if self.gpu_ms > 0 else None
-        d["adapter_hit_rate"] = self.adapter_hits / max(1, self.adapter_hits + self.adapter_misses)
+        d["adapter_hit_rate"] = 1.0 - self.arrival_misses / max(1, self.arrivals)
         return d
 
 
@@ -254,7 +259,10 @@ class Trace:
         sp = self.spec
         steps = sp.steps if steps is None else steps
         self.loads = self.load_bytes = self.evictions = 0
-        hits = misses = finished = 0
+        finished = 0
+        waits_hit: List[int] = []
+        waits_miss: List[int] = []
+        arrivals = arrival_misses = 0
         tokens = dec_tokens = pre_tokens = 0
         running_sum = 0
         peak_kv = 0
@@ -271,8 +279,13 @@ class Trace:
             # arrivals
             for _ in range(self.rng.poisson(sp.arrivals_per_step)):
                 a = int(self.rng.choice(sp.num_adapters, p=self.zipf))
-                self.waiting.append(Request(self.next_rid, a, int(self.rng.integers(sp.prompt_len[0], sp.prompt_len[1] + 1)),
-                                            int(self.rng.integers(sp.output_len[0], sp.output_len[1] + 1))))
+                rq = Request(self.next_rid, a, int(self.rng.integers(sp.prompt_len[0], sp.prompt_len[1] + 1)),
+                             int(self.rng.integers(sp.output_len[0], sp.output_len[1] + 1)))
+                rq.arrived_step = step
+                rq.missed = not (a in self.resident and self.resident[a] < step)
+                arrivals += 1
+                arrival_misses += rq.missed
+                self.waiting.append(rq)
                 self.next_rid += 1
             # admission: adapters loaded in an earlier step; start loads for misses
             loads_now = 0
@@ -292,13 +305,12 @@ class Trace:
                             rq.kv_handles.append(h)
                             rq.admitted_step = step
                             self.running.append(rq)
-                            hits += 1
+                            (waits_miss if rq.missed else waits_hit).append(step - rq.arrived_step)
                             continue
                         self.refs[rq.adapter] -= 1
                 elif (pos <= sp.prefetch_window and loads_now < sp.max_loads_per_step
                       and self._load(rq.adapter, step)):
                     loads_now += 1
-                    misses += 1
                 still.append(rq)
             self.waiting = still
             # the step's batch: decode tokens first, then prompt chunks
@@ -383,7 +395,10 @@ class Trace:
             if st != slora.OK:
                 raise RuntimeError(f"device status {st} after the trace")
         return TraceResult(steps, tokens, dec_tokens, pre_tokens, gpu_ms, step_ms, load_ms, self.loads, self.load_bytes,
-                           self.evictions, hits, misses, finished, running_sum / max(1, steps), peak_kv,
+                           self.evictions, len(waits_hit) + len(waits_miss), arrival_misses, arrivals,
+                           float(np.mean(waits_hit)) if waits_hit else 0.0,
+                           float(np.mean(waits_miss)) if waits_miss else 0.0,
+                           finished, running_sum / max(1, steps), peak_kv,
                            list(self.ops), self.ranks.copy(), time.perf_counter() - t0)
 
     def close(self):

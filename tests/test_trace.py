@@ -58,3 +58,22 @@ def test_trace_is_deterministic():
         elif x[0] == "kv_alloc":
             assert x[2] == y[2]
     assert a.tokens == b.tokens and a.finished == b.finished
+
+
+def test_trace_accounts_for_every_request_and_the_load_stall():
+    sp = small_spec(steps=250)
+    tr = trace.Trace(sp)
+    res = tr.run()
+    # every arrival is admitted or still waiting; every admitted request is
+    # running or finished
+    assert res.arrivals == res.admitted + len(tr.waiting)
+    assert res.admitted == res.finished + len(tr.running)
+    assert 0 < res.arrival_misses < res.arrivals
+    # a miss waits at least one step for its load (an adapter loaded in step
+    # k serves from step k + 1); queueing adds to both kinds of wait
+    assert res.wait_steps_miss >= 1.0
+    assert res.wait_steps_hit >= 0.0
+    s = res.summary()
+    assert s["adapter_hit_rate"] == 1.0 - res.arrival_misses / res.arrivals
+    tr.close()
+
