@@ -178,3 +178,13 @@ def test_argument_validation(S):
     assert e.value.code == S.ERR_EXISTS
     assert S.slora_pool_info(h)["free_pages"] == 2
     S.slora_pool_destroy(h)
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    """No fallback: with the shared library absent every call raises."""
+    from lora_adapters_gb300 import slora
+
+    monkeypatch.setattr(slora, "_lib", None)
+    monkeypatch.setattr(slora, "LIB_PATH", str(tmp_path / "libslora.so"))
+    with pytest.raises(ImportError):
+        slora.slora_pool_create(0, 64, 256, slora.F16, 4, 16, 16, [256], [256])
