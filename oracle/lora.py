@@ -71,7 +71,8 @@ def max_threads() -> int:
 
 def apply(store, pool, p: int, token_adapter: np.ndarray, x: np.ndarray, y_in: np.ndarray,
           s: float, dtype: str, tokens: Optional[Sequence[int]] = None, want_exact: bool = False,
-          want_v: bool = False, num_threads: int = 1, adapter_scale: Optional[np.ndarray] = None):
+          want_v: bool = False, num_threads: int = 1, adapter_scale: Optional[np.ndarray] = None,
+          on_bad: str = "raise"):
     """Oracle of y_out = round(y_in + s s_a (x A) B) for projection p.
 
     adapter_scale: s_a per adapter id (float64, max_adapters entries), or None
@@ -81,6 +82,10 @@ def apply(store, pool, p: int, token_adapter: np.ndarray, x: np.ndarray, y_in: n
     pool:  oracle.pool.OraclePool whose page tables address those pages.
     Returns (y_out, y_exact or None, v or None); rows of tokens not listed in
     ``tokens`` are left as zeros in every output.
+
+    on_bad: what a token naming an id other than -1 outside [0, max_adapters)
+    or a non-resident adapter does: "raise" (ValueError) or "keep" (its row
+    is returned unchanged, like a base-only token's).
     """
     T = int(token_adapter.shape[0])
     dims = pool.proj
@@ -109,8 +114,8 @@ def apply(store, pool, p: int, token_adapter: np.ndarray, x: np.ndarray, y_in: n
         _ptr(ta), T, _ptr(tok), 0 if tok is None else tok.shape[0],
         _ptr(x), h_in, _ptr(y_in), h_out,
         float(s), _ptr(sc), _ptr(y_out), _ptr(y_exact), _ptr(v), v_ld, int(num_threads))
-    if rc != 0:
-        raise ValueError("oracle: a token names an adapter that is not resident")
+    if rc != 0 and on_bad == "raise":
+        raise ValueError("oracle: a token names an adapter that is not resident or an id out of range")
     return y_out, y_exact, v
 
 

@@ -15,7 +15,9 @@
  *
  * where s_a is adapter a's own scale (LoRA's alpha / r; 1 when no per-adapter
  * scales are given), for every token i whose adapter a = a(i) is >= 0; tokens with a(i) = -1 are
- * copied unchanged.  All arithmetic is fp64 on the exact values of the 16-bit
+ * copied unchanged.  Only -1 means "no adapter": a token naming any other id
+ * outside [0, num_adapters), or an adapter of rank 0, is copied unchanged too
+ * and makes the call return -1.  All arithmetic is fp64 on the exact values of the 16-bit
  * inputs, and round() is one IEEE round-to-nearest-even into the storage
  * type.  A and B are never dense here: every element is fetched through the
  * adapter's page table, exactly as the pages describe the non-contiguous
@@ -139,7 +141,8 @@ static const uint16_t* row_elem(const uint16_t* pool, const int64_t* page_slot, 
  *   y_out       receives round(y_in + s * delta) in the same layout
  *   y_exact     optional: the unrounded fp64 value y_in + s * delta
  *   v_out       optional: the fp64 shrink result, row stride v_ld
- * Returns 0, or -1 for a token whose adapter is out of range or has rank 0.
+ * Returns 0, or -1 when a token names an id other than -1 outside
+ * [0, num_adapters) or an adapter of rank 0 (its row is copied unchanged).
  */
 int oracle_lora_apply(const uint16_t* pool, const int64_t* page_slot, int32_t H, int32_t dtype,
                       const int32_t* page_table, const int64_t* pt_off, const int32_t* rank,
@@ -163,19 +166,22 @@ int oracle_lora_apply(const uint16_t* pool, const int64_t* page_slot, int32_t H,
     const int32_t a = token_adapter[i];
     const uint16_t* yi = y_in + (int64_t)i * ldy;
     uint16_t* yo = y_out + (int64_t)i * ldy;
-    if (a < 0) {                                   /* base model only: unchanged */
+    /* Only -1 means "base model only".  Any other id outside
+     * [0, num_adapters), or an adapter of rank 0 (not resident), is an error:
+     * the token is flagged and, like a base-only token, left unchanged. */
+    const int is_bad = a != -1 && (a < 0 || a >= num_adapters || rank[a] <= 0 || rank[a] > 1024);
+    if (a == -1 || is_bad) {
       for (int64_t c = 0; c < hout; c++) {
         yo[c] = yi[c];
         if (y_exact) y_exact[(int64_t)i * ldy + c] = decode(yi[c], dtype);
       }
+      if (is_bad) bad = 1;
       continue;
     }
-    if (a >= num_adapters || rank[a] <= 0) { bad = 1; continue; }
     const int64_t r = rank[a];
     const int64_t a_base = pt_off[a] + r * rows_before;     /* A rows of projection p */
     const int64_t b_base = a_base + r * ppi;                /* B rows follow the A rows */
-    double v[1024];                                         /* r <= 1024 */
-    if (r > 1024) { bad = 1; continue; }
+    double v[1024];                                         /* r <= 1024 (checked above) */
     for (int64_t k = 0; k < r; k++) {                       /* shrink: v = x A */
       double acc = 0.0;
       for (int64_t c = 0; c < hin; c++) {

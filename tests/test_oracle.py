@@ -273,6 +273,29 @@ def test_base_only_tokens_unchanged():
     assert not np.array_equal(y_out[1::3], y[1::3])
 
 
+def test_out_of_range_ids_are_errors_and_left_unchanged():
+    """Only -1 means "no adapter": -2, an id past the last adapter and an
+    evicted adapter are errors (ValueError by default); with on_bad="keep"
+    their rows come back unchanged and every other row is what it is when
+    those tokens carry no adapter at all."""
+    wl, pool = _tiny_state()
+    store = H.oracle_store_for(wl, pool, range(4))
+    x, y = wl.x(0), wl.y_in(0)
+    pool.evict(2)
+    for bad_id in (-2, -7, 4, 1000, 2):
+        ta = wl.token_adapter.copy()
+        ta[ta == 2] = 1                     # no token on the evicted adapter except the planted ones
+        ta[[1, 6]] = bad_id
+        with pytest.raises(ValueError):
+            olora.apply(store, pool, 0, ta, x, y, 1.0, "f16")
+        got, _, _ = olora.apply(store, pool, 0, ta, x, y, 1.0, "f16", on_bad="keep")
+        base = ta.copy()
+        base[[1, 6]] = -1
+        want, _, _ = olora.apply(store, pool, 0, base, x, y, 1.0, "f16")
+        assert np.array_equal(got, want), bad_id
+        assert np.array_equal(got[[1, 6]], y[[1, 6]]), bad_id
+
+
 def test_single_adapter_batch_equals_dense_gemm_chain():
     wl, pool = _tiny_state()
     store = H.oracle_store_for(wl, pool, range(4))
