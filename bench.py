@@ -1,17 +1,26 @@
-"""Benchmark of the heterogeneous-batch paged LoRA delta on one layer.
+"""Benchmark of the heterogeneous-batch paged LoRA delta, one layer per step.
 
 One step = the whole hot path over one batch: group the batch's tokens by
-adapter (build_segments), then y += s (x A_a) B_a for the layer's q, k, v, o
-projections (one multi-projection apply).  The workload is the Llama-7B-shaped
-decode batch: H = 4096, 256 tokens (one per request), 1000 adapters of ranks
-{8, 16, 32, 64} resident in a pre-fragmented pool, token -> adapter Zipf(1),
-fp16.  L2 is flushed before every timed step (a 256 MiB device write, then a
-256 MiB device read, so that the write's dirty lines leave L2 before the step
-starts), so adapter pages, x and y come from HBM; only the steps themselves
-are timed, with CUDA events on the compute stream.
+adapter (build_segments), then y += s (x A_a) B_a for every projection of the
+layer (one multi-projection apply).  The default run measures three
+workloads, each a line of its own inside one printed JSON object:
 
-Printed: one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
-on a bounded sample of the same workload instead (the reference arm).
+* the headline, the largest single-GPU configuration: a Llama-13B-shaped
+  MLP decode batch -- H = 5120, gate/up 5120 -> 13824 and down 13824 -> 5120,
+  512 tokens (one per request), 2000 adapters of ranks {16, 32, 64} resident
+  in a 120 GB pool filled up with KV slots, token -> adapter Zipf(1.2), bf16;
+* ``configs[0]``: the Llama-7B-shaped decode batch -- q/k/v/o 4096 -> 4096,
+  256 tokens, 1000 adapters of ranks {8, 16, 32, 64}, Zipf(1), fp16;
+* ``configs[1]``: the Llama-7B-shaped prefill batch -- 32 requests of
+  U{8..512} tokens, 200 adapters of ranks {8..128}, fp16, long segments on
+  the tensor cores.
+
+L2 is flushed before every timed step (a 256 MiB device write, then a 256 MiB
+device read, so that the write's dirty lines leave L2 before the step starts),
+so adapter pages, x and y come from HBM; only the steps themselves are timed,
+with CUDA events on the compute stream.  ``--workload NAME`` measures one
+workload alone (one line).  ``--impl reference`` times the CPU oracle on a
+bounded sample of the headline workload instead (the reference arm).
 """
 from __future__ import annotations
 
@@ -35,6 +44,10 @@ METRIC = "lora_delta_tokens_per_s_per_layer"
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20
 TC_THRESHOLD = 64          # the library's default: segments of >= 64 tokens use the tensor cores
+HEADLINE = "llama13b_mlp_decode"
+EXTRA = ("llama7b_decode", "llama7b_prefill")
+DEFAULT_MODE = {"llama13b_mlp_decode": "decode", "llama7b_decode": "decode", "llama7b_prefill": "prefill",
+                "tiny": "decode"}
 
 # ncu DRAM counters of the dominant kernel (dram__bytes_read.sum + write.sum,
 # per launch) on the benchmark workload, with the hash of the kernel source
@@ -45,12 +58,17 @@ NCU_TRAFFIC = {
     # tc_expand on the 7B prefill batch: 360.50 MB read + 221.82 MB written
     ("expand_tc", "llama7b_prefill"): (582319360, "d4e7ece89ac53932"),
 }
+# ncu sm__pipe_tensor_cycles_active of the tensor-core expand kernel (% of
+# its active cycles) on the prefill batch, with the kernel-source hash.
+NCU_TENSOR_PIPE = {
+    "llama7b_prefill": (9.2, "d4e7ece89ac53932"),
+}
 
 
 def _kernel_source_hash() -> str:
     """Hash of the kernel sources' code: comments and whitespace do not count."""
     h = hashlib.sha256()
-    for f in ("kernels.cu", "tc_kernels.cu", "internal.h"):
+    for f in ("kernels.cu", "tc_kernels.cu", "internal.h", "ptx.cuh"):
         p = os.path.join(ROOT, "lora_adapters_gb300", "csrc", f)
         if os.path.exists(p):
             src = open(p).read()
@@ -66,6 +84,15 @@ def _peaks():
         d = json.load(open(path))
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def _tensor_peak():
+    """Dense 16-bit tensor peak (TFLOP/s): fp16 and bf16 run at the same rate."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["bf16_tflops"]), "measured (bf16 burst; fp16 has the same dense rate)"
+    return 1900.0, "fallback"
 
 
 # ---------------------------------------------------------------- workload
@@ -94,7 +121,27 @@ def algorithmic_bytes(wl, tc_threshold=None, elt=2):
     return out
 
 
+def algorithmic_flops(wl, tc_threshold=None):
+    """Multiply-add flops of one step (2 per product), split like the bytes:
+    shrink 2 T_s r_a H_in and expand 2 T_s r_a H_out per segment and projection."""
+    ta = wl.token_adapter
+    ids, counts = np.unique(ta[ta >= 0], return_counts=True)
+    out = {"shrink_cc": 0, "expand_cc": 0, "shrink_tc": 0, "expand_tc": 0}
+    for a, n in zip(ids, counts):
+        r, n = int(wl.ranks[a]), int(n)
+        path = "tc" if tc_threshold is not None and n >= tc_threshold else "cc"
+        out["shrink_" + path] += sum(2 * n * r * p.h_in for p in wl.projections)
+        out["expand_" + path] += sum(2 * n * r * p.h_out for p in wl.projections)
+    out["step"] = sum(out[k] for k in ("shrink_cc", "expand_cc", "shrink_tc", "expand_tc"))
+    return out
+
+
 def setup_device(wl, device):
+    """A device pool holding the workload's adapters, and its inputs.
+
+    Adapters that the batch uses get their drawn weights; the others (whose
+    pages are allocated in the same order but never read by this batch) get
+    zeros, so that the 2000-adapter pools load in seconds."""
     import torch
 
     from lora_adapters_gb300 import slora
@@ -103,7 +150,18 @@ def setup_device(wl, device):
     dims = [(p.h_in, p.h_out) for p in sp.projections]
     pool = slora.Pool(wl.pool_pages, wl.H, sp.dtype, dims, sp.num_adapters, max(sp.rank_set),
                       max(wl.T, 1), device=device)
-    pool.replay(wl.pool_ops, wl.ranks, wl.adapter)
+    used = set(int(a) for a in wl.token_adapter if a >= 0)
+    zeros = {}
+
+    def weights_of(a):
+        if a in used:
+            return wl.adapter(a)
+        r = int(wl.ranks[a])
+        if r not in zeros:
+            zeros[r] = [(np.zeros((r, i), np.uint16), np.zeros((r, o), np.uint16)) for i, o in dims]
+        return zeros[r]
+
+    pool.replay(wl.pool_ops, wl.ranks, weights_of)
     tdt = pool.tdtype
 
     def dev(bits):
@@ -211,6 +269,36 @@ def cpu_threads() -> int:
         return os.cpu_count() or 1
 
 
+def workload_config(wl, mode, gpus):
+    sp = wl.spec
+    return {"workload": sp.name, "H": sp.H, "tokens_per_step": wl.T,
+            "projections": [f"{p.name}:{p.h_in}->{p.h_out}" for p in sp.projections],
+            "adapters_resident": sp.num_adapters, "ranks": list(sp.rank_set),
+            "popularity": f"{sp.popularity}{'(alpha=%g)' % sp.zipf_alpha if sp.popularity == 'zipf' else ''}",
+            "pool_pages": wl.pool_pages, "page_bytes": sp.H * 2, "pool_gb": wl.pool_pages * sp.H * 2 / 1e9,
+            "mode": mode,
+            "l2": "flushed before every timed step: 256 MiB device write, then 256 MiB device read",
+            "parallelism": f"replicas x{gpus}"}
+
+
+def oracle_baseline(wl, seconds: float):
+    """The CPU oracle on a bounded token sample, at all host threads and at one."""
+    orc = OracleSample(wl)
+    out = {}
+    for threads in (cpu_threads(), 1):
+        t1, n1 = orc.run(2, threads)
+        n_tok = int(max(2, min(wl.T, seconds / 4 / max(t1 / n1, 1e-6))))
+        t, nn, reps = 0.0, 0, 0
+        while t < seconds and reps < 200:
+            dt, dn = orc.run(n_tok, threads, seed=1 + reps)
+            t, nn, reps = t + dt, nn + dn, reps + 1
+        out[threads] = (nn / t, f"{reps} x {n_tok} of the {wl.T} tokens, all {len(wl.projections)} projections, "
+                                f"fp64 C loops, {t:.1f} s of oracle time")
+    threads = cpu_threads()
+    return {"value": out[threads][0], "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": out[threads][1], "value_1_thread": out[1][0], "sample_1_thread": out[1][1]}
+
+
 def run_reference(args, wl, cfg):
     """The reference arm: the CPU oracle, as it stands, on host cores."""
     rank = int(os.environ.get("RANK", "0"))
@@ -236,7 +324,8 @@ def run_reference(args, wl, cfg):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": cfg,
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                             "sample": f"{sample} tokens of the batch per step, all 4 projections"},
+                             "sample": f"{sample} tokens of the batch per step, all {len(wl.projections)} "
+                                       f"projections"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -286,48 +375,40 @@ class Replicas:
 
 
 # ---------------------------------------------------------------- GPU arm
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference", "bmm"],
-                    help="bmm: the padded batched-matmul comparator through slora_lora_apply_bmm")
-    ap.add_argument("--workload", default="llama7b_decode")
-    ap.add_argument("--mode", default="decode", choices=["auto", "decode", "prefill"])
-    ap.add_argument("--ref-tokens", type=int, default=24)
-    ap.add_argument("--cpu-tokens", type=int, default=0, help="oracle sample size (0: sized to ~10 s)")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    args = ap.parse_args()
-    args.warmup = max(args.warmup, 3)
+def _link_gbs(torch, device, h2d: int, d2h: int):
+    """A plain pinned-memory copy of one step's bytes each way, alone: the
+    link-bound floor of the end-to-end step."""
+    out = {}
+    for name, nbytes, up in (("h2d", h2d, True), ("d2h", d2h, False)):
+        host = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+        dev = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        s = torch.cuda.Stream(device=device)
+        best = None
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(s):
+                a.record(s)
+                (dev.copy_(host, non_blocking=True) if up else host.copy_(dev, non_blocking=True))
+                b.record(s)
+            b.synchronize()
+            ms = a.elapsed_time(b)
+            best = ms if best is None else min(best, ms)
+        out[name + "_gbs"] = nbytes / (best * 1e-3) / 1e9
+        out[name + "_ms"] = best
+        del host, dev
+    return out
 
-    from lora_adapters_gb300 import workloads
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    wl = workloads.make(args.workload, seed=rank)      # each replica draws its own batch
-    sp = wl.spec
-    cfg = {"workload": sp.name, "H": sp.H, "tokens_per_step": wl.T,
-           "projections": [f"{p.name}:{p.h_in}->{p.h_out}" for p in sp.projections],
-           "adapters_resident": sp.num_adapters, "ranks": list(sp.rank_set),
-           "popularity": f"{sp.popularity}{'(alpha=%g)' % sp.zipf_alpha if sp.popularity == 'zipf' else ''}",
-           "pool_pages": wl.pool_pages, "page_bytes": sp.H * 2, "mode": args.mode,
-           "l2": "flushed before every timed step: 256 MiB device write, then 256 MiB device read",
-           "parallelism": f"replicas x{args.gpus}"}
-    if args.impl == "reference":
-        run_reference(args, wl, cfg)
-        return
-
+def measure(name, mode_name, args, rep, device, rank, world):
+    """Every number of one workload's line (rank 0 prints it)."""
     import torch
 
-    from lora_adapters_gb300 import build, slora
+    from lora_adapters_gb300 import slora, workloads
 
-    build.build()
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    rep = Replicas("nccl", device)
-    mode = {"auto": slora.MODE_AUTO, "decode": slora.MODE_DECODE, "prefill": slora.MODE_PREFILL}[args.mode]
+    wl = workloads.make(name, seed=rank)      # each replica draws its own batch
+    sp = wl.spec
+    cfg = workload_config(wl, mode_name, args.gpus)
+    mode = {"auto": slora.MODE_AUTO, "decode": slora.MODE_DECODE, "prefill": slora.MODE_PREFILL}[mode_name]
 
     pool, ta, xs, ys, y0 = setup_device(wl, device)
     n = len(sp.projections)
@@ -371,19 +452,17 @@ def main():
     wall = time.perf_counter() - wall0
     clk = clocks.stop()
     rep.barrier()
-    ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    if pool.status() != slora.OK:
+        raise RuntimeError(f"{name}: a kernel reported an error during the timed steps")
+    ms = sum(s_.elapsed_time(e) for s_, e in zip(starts, ends))
     ms_step = rep.max(ms / args.steps)
     value = rep.rate(wl.T, ms_step * 1e-3)
-
+    hbm_peak, peak_kind = _peaks()
 
     if args.impl == "bmm":
         # the comparator: step time and the same algorithmic bytes only
         ab = algorithmic_bytes(wl, None)
-        hbm_peak = _peaks()[0]
-        rep.close()
-        if rank == 0:
-            print(json.dumps({
-                "impl": "bmm", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        line = {"impl": "bmm", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": sp.dtype, "data": "synthetic", "config": cfg,
                 "comparator": "every token's rows gathered and padded to the pool's max rank, two cuBLAS "
@@ -391,9 +470,9 @@ def main():
                 "scratch_bytes": slora.slora_bmm_scratch_bytes(pool.handle),
                 "step_algorithmic_bytes": ab["step"],
                 "step_frac_of_hbm": ab["step"] / (ms_step * 1e-3) / 1e9 / hbm_peak,
-                "clocks": clk, "gpu_launches": (1 + 3 * n) * args.steps}), flush=True)
+                "clocks": clk, "gpu_launches": (1 + 3 * n) * args.steps}
         pool.close()
-        return
+        return line
 
     # ---- per-kernel durations: the same steps again, each kernel bracketed by
     # events on the compute stream (this serialises the launches a little, so
@@ -409,17 +488,19 @@ def main():
     slora.slora_timing_enable(pool.handle, False)
 
     # ---- roofline of the dominant kernel
-    hbm_peak, peak_kind = _peaks()
-    ab = algorithmic_bytes(wl, {"decode": None, "auto": TC_THRESHOLD, "prefill": 0}[args.mode])
+    thr = {"decode": None, "auto": TC_THRESHOLD, "prefill": 0}[mode_name]
+    ab = algorithmic_bytes(wl, thr)
+    fl = algorithmic_flops(wl, thr)
     per_kernel = {}
-    for name, (tms, cnt) in kern.items():
+    for kname, (tms, cnt) in kern.items():
         if cnt:
-            per_kernel[name] = {"avg_us": 1e3 * tms / cnt, "launches": int(cnt),
-                                "us_per_step": 1e3 * tms / hook_steps}
-            if name in ab:
-                per_launch = ab[name] * hook_steps / cnt
-                per_kernel[name]["bytes_per_launch"] = per_launch
-                per_kernel[name]["gbs"] = per_launch / (per_kernel[name]["avg_us"] * 1e-6) / 1e9
+            per_kernel[kname] = {"avg_us": 1e3 * tms / cnt, "launches": int(cnt),
+                                 "us_per_step": 1e3 * tms / hook_steps}
+            if kname in ab:
+                per_launch = ab[kname] * hook_steps / cnt
+                per_kernel[kname]["bytes_per_launch"] = per_launch
+                per_kernel[kname]["gbs"] = per_launch / (per_kernel[kname]["avg_us"] * 1e-6) / 1e9
+                per_kernel[kname]["frac_of_hbm"] = per_kernel[kname]["gbs"] / hbm_peak
     # the dominant kernel: the one with the most device time per step among
     # those that move the path's algorithmic bytes
     movers = [k for k in per_kernel if "gbs" in per_kernel[k]]
@@ -430,20 +511,37 @@ def main():
     traffic = tr[0] if tr and tr[1] == src_hash else None
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                 "frac": achieved / hbm_peak, "peak_source": peak_kind, "traffic": traffic,
+                "traffic_over_algorithmic": (traffic / per_kernel[dom]["bytes_per_launch"]) if traffic else None,
                 "algorithmic_bytes_per_launch": per_kernel[dom]["bytes_per_launch"],
                 "avg_launch_us": per_kernel[dom]["avg_us"],
                 "step_algorithmic_bytes": ab["step"],
                 "step_achieved_gbs": ab["step"] / (ms_step * 1e-3) / 1e9,
                 "step_frac": ab["step"] / (ms_step * 1e-3) / 1e9 / hbm_peak,
                 "kernels": per_kernel, "source_hash": src_hash}
+    tc_us = sum(per_kernel.get(k, {}).get("us_per_step", 0.0) for k in ("shrink_tc", "expand_tc"))
+    if tc_us > 0:
+        # the tensor-core kernels against the dense 16-bit tensor peak (their
+        # arithmetic intensity is below the ridge: HBM stays the bound)
+        tpk, tkind = _tensor_peak()
+        tflops = (fl["shrink_tc"] + fl["expand_tc"]) / (tc_us * 1e-6) / 1e12
+        tensor = {"achieved_tflops": tflops, "peak_tflops": tpk, "frac": tflops / tpk, "peak_source": tkind,
+                  "algorithmic_flops_per_step": fl["shrink_tc"] + fl["expand_tc"]}
+        for k in ("shrink_tc", "expand_tc"):
+            if k in per_kernel:
+                per_kernel[k]["tflops"] = fl[k] / (per_kernel[k]["us_per_step"] * 1e-6) / 1e12
+        pipe = NCU_TENSOR_PIPE.get(sp.name)
+        if pipe and pipe[1] == src_hash:
+            tensor["ncu_tensor_pipe_active"] = pipe[0]
+        roofline["tensor"] = tensor
     launches = int(round(sum(c for _, c in kern.values()) / hook_steps)) * args.steps
 
     # ---- end to end through the C ABI with host buffers.  Every step copies
     # its token ids, x and y in from pinned host memory and its y back out, as
     # a serving loop would: inputs of step k+1 go in on one copy stream and the
     # result of step k-1 comes out on another while step k computes (two sets
-    # of device buffers).  No L2 flush here: the adapter rows a step reads
-    # (about 260 MB) exceed L2 and x, y arrive from the host every step.
+    # of device buffers).  No L2 flush here: x and y arrive from the host
+    # every step and the adapter rows a step reads exceed L2 on the decode
+    # batches.
     pin_x = [x.cpu().pin_memory() for x in xs]
     pin_y = [y.cpu().pin_memory() for y in y0]
     pin_ta = ta.cpu().pin_memory()
@@ -505,36 +603,75 @@ def main():
                 raise RuntimeError("pipelined end-to-end steps disagree")
     rep.barrier()
     e_ms = rep.max(e_ms)
+    link = _link_gbs(torch, device, h2d, d2h)
     e2e = {"value": rep.rate(wl.T, e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
            "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms,
-           "pipelining": "inputs of step k+1 in and step k-1's y out while step k computes", "l2": "not flushed"}
+           "pipelining": "inputs of step k+1 in and step k-1's y out while step k computes", "l2": "not flushed",
+           "link": dict(link, note="one plain pinned copy of the step's input bytes (h2d) and of its output "
+                                   "bytes (d2h), each alone: the end-to-end step cannot beat the larger "
+                                   "of the two"),
+           "link_bound_ms": max(link["h2d_ms"], link["d2h_ms"])}
+    pool.close()
+    del step, e2e_step, pool, xs, ys, y0, sets, out_y, pin_x, pin_y, flush_w, flush_r, ta
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
 
     # ---- CPU baseline: the oracle on a bounded sample, rank 0 at N = 1 only
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        threads = cpu_threads()
-        orc = OracleSample(wl)
-        n_tok = args.cpu_tokens
-        if n_tok <= 0:
-            t1, n1 = orc.run(4, threads)
-            n_tok = int(max(4, min(wl.T, 10.0 / max(t1 / n1, 1e-6))))
-        t, nn, reps = 0.0, 0, 0
-        while t < 10.0 and reps < 200:                   # about 10 s of CPU work
-            dt, dn = orc.run(n_tok, threads, seed=1 + reps)
-            t, nn, reps = t + dt, nn + dn, reps + 1
-        cpu = {"value": nn / t, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": f"{reps} x {n_tok} of the {wl.T} tokens, all {n} projections, "
-                         f"fp64 C loops, {t:.1f} s of oracle time"}
+        cpu = oracle_baseline(wl, args.cpu_seconds if name == HEADLINE else args.cpu_seconds / 2)
 
-    pool.close()
-    if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": sp.dtype, "data": "synthetic", "config": cfg,
-                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-                "gpu_launches": launches, "wall_s_timed_region": wall}
-        print(json.dumps(line), flush=True)
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": sp.dtype, "data": "synthetic", "config": cfg,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+            "gpu_launches": launches, "wall_s_timed_region": wall}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference", "bmm"],
+                    help="bmm: the padded batched-matmul comparator through slora_lora_apply_bmm")
+    ap.add_argument("--workload", default="all",
+                    help="all: the headline workload plus the two 7B batches; else one workload")
+    ap.add_argument("--mode", default=None, choices=["auto", "decode", "prefill"],
+                    help="default: decode for decode batches, prefill for the prefill batch")
+    ap.add_argument("--ref-tokens", type=int, default=24)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time per thread count (headline)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from lora_adapters_gb300 import workloads
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    names = [HEADLINE, *EXTRA] if args.workload == "all" else [args.workload]
+    if args.impl == "reference":
+        wl = workloads.make(names[0], seed=rank)
+        run_reference(args, wl, workload_config(wl, args.mode or DEFAULT_MODE.get(names[0], "decode"), args.gpus))
+        return
+
+    import torch
+
+    from lora_adapters_gb300 import build
+
+    build.build()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    rep = Replicas("nccl", device)
+    lines = [measure(nm, args.mode or DEFAULT_MODE.get(nm, "decode"), args, rep, device, rank, world)
+             for nm in names]
     rep.close()
+    if rank == 0:
+        line = dict(lines[0])
+        if len(lines) > 1:
+            line["configs"] = lines[1:]
+        print(json.dumps(line), flush=True)
 
 
 if __name__ == "__main__":

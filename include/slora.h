@@ -54,7 +54,8 @@ extern "C" {
 #define SLORA_ERR_OOM (-2)          /* not enough free pages; state unchanged */
 #define SLORA_ERR_EXISTS (-3)       /* adapter id already resident */
 #define SLORA_ERR_NOT_RESIDENT (-4) /* adapter id not resident */
-#define SLORA_ERR_BUSY (-5)         /* reserved: the pool orders reuse by events instead */
+#define SLORA_ERR_BUSY (-5)         /* reserved, never returned: an evict of an adapter still in use
+                                       is ordered by events instead (see slora_adapter_evict) */
 #define SLORA_ERR_CUDA (-6)         /* a CUDA runtime call failed (see error string) */
 #define SLORA_ERR_DEVICE (-7)       /* a kernel reported bad input (see slora_device_status) */
 #define SLORA_ERR_TIMEOUT (-8)      /* a kernel's bounded wait gave up (device status only) */
@@ -98,7 +99,13 @@ typedef struct slora_segments {
 } slora_segments;
 
 /*
- * Create a pool over a caller-owned device buffer.
+ * Create a pool over a caller-owned device buffer.  The pool is the unified
+ * memory pool of S-LoRA's Unified Paging (dongaigc.com summary, section 1
+ * "Unified Paging": one pool of pages managed together for adapter weights
+ * and KV-cache tensors; nubint.ai review, method list): pages of H elements,
+ * the unit one token's K or V vector of one layer takes, so that adapter rows
+ * of every rank and KV slots of every length are allocated from one free list
+ * without fragmenting it.
  *   d_pool      device buffer of num_pages * page_elems 16-bit elements,
  *               16-byte aligned; caller-owned, must outlive the pool.  NULL
  *               creates a PLANNING pool: host allocator and page tables only,
@@ -173,7 +180,12 @@ int slora_adapter_load(slora_pool* pool, int32_t adapter_id, int32_t rank,
 /*
  * Evict a resident adapter: its pages return to the free list at once and
  * its device rank is cleared on the compute stream (work queued before the
- * evict still sees the adapter).  Every segment handle built before the
+ * evict still sees the adapter).  The pages' "race conditions in the adapter
+ * manager under dynamic loading" (cmlonder.com newsletter, section "Iddia ve
+ * Gerceklik") are answered by stream order rather than by refusing the evict
+ * with SLORA_ERR_BUSY: a later load into the freed pages is queued after all
+ * work queued on the compute stream before it, so no kernel still reading the
+ * old rows can see the new ones.  Every segment handle built before the
  * evict becomes stale (build the segments again).  SLORA_ERR_NOT_RESIDENT if
  * it is not loaded.
  */
@@ -204,6 +216,11 @@ int slora_build_segments(slora_pool* pool, const int32_t* d_token_adapter, int32
                          slora_segments* out);
 
 /*
+ * The heterogeneous-batch LoRA delta (dongaigc.com summary, section 2
+ * "Heterogeneous Batching": the adapter part of tokens that use different
+ * adapters of different ranks computed in one pass by custom kernels that
+ * read the weights directly from the non-contiguous pool; cmlonder.com
+ * newsletter, section "Iddia ve Gerceklik": segmented gather kernels, SGMV):
  * y += s * (x A_a) B_a for one projection `proj` over every token of the
  * batch `seg` was built from (tokens left out of the segments are not
  * touched).  x: device, T rows of proj_in[proj] elements, row stride ldx
@@ -292,7 +309,12 @@ const char* slora_last_error_string(void);
  *                               slora_adapter_load (the layout a pool uses);
  *                               every entry read must name a page of d_pool
  *   d_rank, max_adapters        device int32[max_adapters]; 0 = not resident;
- *                               ranks outside [1, SLORA_MAX_RANK] count as 0
+ *                               ranks outside [1, rmax] count as 0, where
+ *                               rmax = min(SLORA_MAX_RANK, pt_stride / E) and
+ *                               E = sum_q(ceil(in_q/H) + ceil(out_q/H)) is
+ *                               the entries one unit of rank takes, so no
+ *                               adapter's rows run into the next adapter's
+ *                               stretch of the page table
  *   num_proj, proj_in, proj_out host arrays: every projection adapters carry
  *   proj                        the projection to apply
  *   d_token_adapter, T          device int32[T], ids in [-1, max_adapters);
@@ -301,6 +323,16 @@ const char* slora_last_error_string(void);
  *                               non-resident adapter are left unchanged
  *   d_x, ldx, d_y, ldy, s       as in slora_lora_apply
  *   stream                      cudaStream_t (NULL = legacy default stream)
+ *   status                      optional (NULL: not reported): one int32 in
+ *                               device memory or pinned host memory that
+ *                               receives this call's device status on
+ *                               `stream` once its kernels are done --
+ *                               SLORA_OK, SLORA_ERR_NOT_RESIDENT (a token's
+ *                               adapter has rank 0), SLORA_ERR_INVALID (an id
+ *                               other than -1 outside [0, max_adapters)) or
+ *                               SLORA_ERR_TIMEOUT (a kernel's bounded wait
+ *                               gave up; y may be partly updated).  Read it
+ *                               after synchronising the stream.
  * The first call on a device sets that device up (it looks up the device
  * address of the scratch array and sizes the kernels' grids); make that first
  * call before any stream capture.  Every call shares the one scratch array
@@ -315,7 +347,7 @@ int slora_lora_apply_noalloc(const void* d_pool, int32_t page_elems, int32_t dty
                              int32_t max_adapters, int32_t num_proj, const int32_t* proj_in,
                              const int32_t* proj_out, int32_t proj, const int32_t* d_token_adapter,
                              int32_t T, const void* d_x, int64_t ldx, void* d_y, int64_t ldy, float s,
-                             void* stream);
+                             void* stream, int32_t* status);
 
 #ifdef __cplusplus
 }

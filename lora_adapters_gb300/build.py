@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 OBJ_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libslora.so")
 SOURCES = ["pool.cpp", "kernels.cu", "tc_kernels.cu", "noalloc.cu", "bmm.cu"]
-HEADERS = [os.path.join(CSRC, "internal.h"), os.path.join(ROOT, "include", "slora.h")]
+HEADERS = [os.path.join(CSRC, "internal.h"), os.path.join(CSRC, "ptx.cuh"), os.path.join(ROOT, "include", "slora.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
 

@@ -54,13 +54,14 @@ int na_fail(int code, const char* msg, cudaError_t e = cudaSuccess) {
   return code;
 }
 
-// Copy of the caller's ranks with every value outside [1, SLORA_MAX_RANK] set
-// to 0 (treated as "not resident"), so that no rank can index past the rows
-// of the static v buffer.
-__global__ void sanitize_ranks_kernel(const int32_t* in, int32_t* out, int n) {
+// Copy of the caller's ranks with every value outside [1, rmax] set to 0
+// (treated as "not resident").  rmax = min(SLORA_MAX_RANK, pt_stride /
+// entries per unit of rank): no rank can index past the rows of the static v
+// buffer, nor past its adapter's own stretch of the page table.
+__global__ void sanitize_ranks_kernel(const int32_t* in, int32_t* out, int n, int32_t rmax) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
     const int32_t r = in[i];
-    out[i] = (r >= 1 && r <= kMaxRank) ? r : 0;
+    out[i] = (r >= 1 && r <= rmax) ? r : 0;
   }
 }
 
@@ -96,7 +97,8 @@ extern "C" int slora_lora_apply_noalloc(const void* d_pool, int32_t page_elems, 
                                         const int32_t* d_rank, int32_t max_adapters, int32_t num_proj,
                                         const int32_t* proj_in, const int32_t* proj_out, int32_t proj,
                                         const int32_t* d_token_adapter, int32_t T, const void* d_x,
-                                        int64_t ldx, void* d_y, int64_t ldy, float s, void* stream) {
+                                        int64_t ldx, void* d_y, int64_t ldy, float s, void* stream,
+                                        int32_t* status) {
   if (!d_pool || !d_page_table || !d_rank || !proj_in || !proj_out)
     return na_fail(SLORA_ERR_INVALID, "NULL pool, page table, ranks or projection dims");
   if (page_elems <= 0 || page_elems % 8 || page_elems > 65536)
@@ -117,13 +119,17 @@ extern "C" int slora_lora_apply_noalloc(const void* d_pool, int32_t page_elems, 
   }
   if (pt_stride < per_rank)
     return na_fail(SLORA_ERR_INVALID, "pt_stride smaller than one adapter's page-table entries");
-  if (T == 0) return SLORA_OK;
-  if (!d_token_adapter || !d_x || !d_y) return na_fail(SLORA_ERR_INVALID, "NULL tokens, x or y");
-  if ((reinterpret_cast<uintptr_t>(d_x) | reinterpret_cast<uintptr_t>(d_y) |
-       reinterpret_cast<uintptr_t>(d_pool)) & 15)
-    return na_fail(SLORA_ERR_INVALID, "pool, x and y must be 16-byte aligned");
-  if (ldx < proj_in[proj] || ldx % 8 || ldy < proj_out[proj] || ldy % 8)
-    return na_fail(SLORA_ERR_INVALID, "row strides must be multiples of 8 and cover the row");
+  // the largest rank whose entries fit in an adapter's stretch of the table
+  const int64_t rfit = pt_stride / per_rank;
+  const int32_t rmax = rfit < kMaxRank ? (int32_t)rfit : kMaxRank;
+  if (T > 0) {
+    if (!d_token_adapter || !d_x || !d_y) return na_fail(SLORA_ERR_INVALID, "NULL tokens, x or y");
+    if ((reinterpret_cast<uintptr_t>(d_x) | reinterpret_cast<uintptr_t>(d_y) |
+         reinterpret_cast<uintptr_t>(d_pool)) & 15)
+      return na_fail(SLORA_ERR_INVALID, "pool, x and y must be 16-byte aligned");
+    if (ldx < proj_in[proj] || ldx % 8 || ldy < proj_out[proj] || ldy % 8)
+      return na_fail(SLORA_ERR_INVALID, "row strides must be multiples of 8 and cover the row");
+  }
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -162,7 +168,16 @@ extern "C" int slora_lora_apply_noalloc(const void* d_pool, int32_t page_elems, 
   // fully rewritten by the kernels before it is read.
   e = cudaMemsetAsync(err, 0, sizeof(int32_t), st);
   if (e != cudaSuccess) return na_fail(SLORA_ERR_CUDA, "cudaMemsetAsync(error word)", e);
-  sanitize_ranks_kernel<<<(max_adapters + 255) / 256, 256, 0, st>>>(d_rank, rank_c, max_adapters);
+  // The call's device status, once its kernels are done, into the caller's
+  // word (device memory or pinned host memory; no allocation).
+  auto copy_status = [&]() -> int {
+    if (!status) return SLORA_OK;
+    cudaError_t e2 = cudaMemcpyAsync(status, err, sizeof(int32_t), cudaMemcpyDefault, st);
+    if (e2 != cudaSuccess) return na_fail(SLORA_ERR_CUDA, "cudaMemcpyAsync(status)", e2);
+    return SLORA_OK;
+  };
+  if (T == 0) return copy_status();
+  sanitize_ranks_kernel<<<(max_adapters + 255) / 256, 256, 0, st>>>(d_rank, rank_c, max_adapters, rmax);
   if ((e = cudaGetLastError()) != cudaSuccess) return na_fail(SLORA_ERR_CUDA, "rank copy launch", e);
 
   SegBuildArgs b{};
@@ -212,7 +227,7 @@ extern "C" int slora_lora_apply_noalloc(const void* d_pool, int32_t page_elems, 
   d.seg_desc = sd.seg_desc;
   d.off_n = (T < max_adapters ? T : max_adapters) + 1 < kSegSmem ? (T < max_adapters ? T : max_adapters) + 1 : kSegSmem;
   if ((e = launch_apply_cc(d, dtype, g_grid[dev], st)) != cudaSuccess) return na_fail(SLORA_ERR_CUDA, "apply launch", e);
-  return SLORA_OK;
+  return copy_status();
 }
 
 static_assert(kNaBytes == SLORA_NOALLOC_SCRATCH_BYTES, "SLORA_NOALLOC_SCRATCH_BYTES must describe the array");

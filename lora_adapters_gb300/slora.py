@@ -78,7 +78,7 @@ _SIGS = {
     "slora_timing_read": [P, I32, P, P, P, P],
     "slora_set_tc_threshold": [P, I32],
     "slora_lora_apply_noalloc": [P, I32, I32, P, I64, P, I32, I32, P, P, I32, P, I32, P, I64, P, I64,
-                                 ctypes.c_float, P],
+                                 ctypes.c_float, P, P],
 }
 
 
@@ -255,12 +255,15 @@ NOALLOC_MAX_TOKENS = 2048
 def slora_lora_apply_noalloc(d_pool: int, page_elems: int, dtype: int, d_page_table: int, pt_stride: int,
                              d_rank: int, max_adapters: int, proj_in: Sequence[int], proj_out: Sequence[int],
                              proj: int, d_token_adapter: int, T: int, d_x: int, ldx: int, d_y: int, ldy: int,
-                             s: float, stream: int = 0) -> None:
-    """The allocation-free apply (every buffer caller-owned; see slora.h)."""
+                             s: float, stream: int = 0, status: int = 0) -> None:
+    """The allocation-free apply (every buffer caller-owned; see slora.h).
+
+    status: address of one int32 (device or pinned host memory) that receives
+    the call's device status on the stream, or 0 for none."""
     _check(lib().slora_lora_apply_noalloc(d_pool, page_elems, dtype, d_page_table, pt_stride, d_rank,
                                           max_adapters, len(proj_in), _arr(proj_in, I32), _arr(proj_out, I32),
-                                          proj, d_token_adapter or None, T, d_x, ldx, d_y, ldy, s,
-                                          stream or None), "slora_lora_apply_noalloc")
+                                          proj, d_token_adapter or None, T, d_x or None, ldx, d_y or None, ldy, s,
+                                          stream or None, status or None), "slora_lora_apply_noalloc")
 
 
 # ---- convenience wrapper for torch tensors -----------------------------------------
