@@ -411,6 +411,11 @@ def measure(name, mode_name, args, rep, device, rank, world):
     mode = {"auto": slora.MODE_AUTO, "decode": slora.MODE_DECODE, "prefill": slora.MODE_PREFILL}[mode_name]
 
     pool, ta, xs, ys, y0 = setup_device(wl, device)
+    tc_threshold = TC_THRESHOLD
+    if args.tc_threshold is not None:
+        tc_threshold = args.tc_threshold
+        slora.slora_set_tc_threshold(pool.handle, tc_threshold)
+        cfg["tc_threshold"] = tc_threshold
     n = len(sp.projections)
     projs = list(range(n))
     stream = pool.compute_stream
@@ -488,7 +493,7 @@ def measure(name, mode_name, args, rep, device, rank, world):
     slora.slora_timing_enable(pool.handle, False)
 
     # ---- roofline of the dominant kernel
-    thr = {"decode": None, "auto": TC_THRESHOLD, "prefill": 0}[mode_name]
+    thr = {"decode": None, "auto": tc_threshold, "prefill": 0}[mode_name]
     ab = algorithmic_bytes(wl, thr)
     fl = algorithmic_flops(wl, thr)
     per_kernel = {}
@@ -639,6 +644,8 @@ def main():
                     help="all: the headline workload plus the two 7B batches; else one workload")
     ap.add_argument("--mode", default=None, choices=["auto", "decode", "prefill"],
                     help="default: decode for decode batches, prefill for the prefill batch")
+    ap.add_argument("--tc-threshold", type=int, default=None,
+                    help="AUTO mode: segments of at least this many tokens on the tensor cores (library default 64)")
     ap.add_argument("--ref-tokens", type=int, default=24)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time per thread count (headline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -27,6 +27,7 @@ namespace {
 
 // ---- 16-bit element helpers ----------------------------------------------------
 struct F16 {
+  static constexpr bool kBf16 = false;
   static __device__ __forceinline__ float2 unpack(uint32_t u) {
     __half2 h;
     memcpy(&h, &u, 4);
@@ -40,6 +41,7 @@ struct F16 {
   }
 };
 struct BF16 {
+  static constexpr bool kBf16 = true;
   static __device__ __forceinline__ float2 unpack(uint32_t u) {
     __nv_bfloat162 h;
     memcpy(&h, &u, 4);
@@ -601,6 +603,220 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
   }
 }
 
+// ---- build_segments for batches of at most 1024 tokens ---------------------------
+// One CTA, one token per thread, no histogram over the adapter ids: a decode
+// batch is short, and this kernel sits on its critical path, so it is built
+// from few block-wide steps, each a handful of instructions.
+//  (1) every thread reads its token's id and the adapter's rank (every rank
+//      comes into shared memory first when there are few adapters) and forms
+//      the composite key (id << 10) | token, unique per token; tokens that
+//      are base-only or invalid get a key above every valid one;
+//  (2) a token's sorted position is the number of keys below its own
+//      (block_rank: sorted runs of 32 keys, binary searches): ascending id,
+//      token order within an id;
+//  (3) segment heads are the sorted positions whose id differs from the
+//      previous one; a ballot scan numbers them;
+//  (4) the work order -- segments by rank, largest first, ties by id -- is
+//      the same ranking of (256 - rank, segment) keys, so it does not depend
+//      on scheduling;
+//  (5) work units per work-order position and their prefix sums (shuffle
+//      scans), then the segment arrays go out.
+constexpr int kSmallSegMax = 1024;
+
+// Exclusive block scan of K ints per thread and their totals: shuffle scans
+// inside each warp, one warp scans the warp totals.
+template <int K>
+__device__ __forceinline__ void small_block_scan(int (&v)[K], int (&excl)[K], int (&total)[K], int (*wtot)[K]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int inc[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) inc[k] = v[k];
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1)
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int n = __shfl_up_sync(0xffffffffu, inc[k], off);
+      if (lane >= off) inc[k] += n;
+    }
+  if (lane == 31)
+#pragma unroll
+    for (int k = 0; k < K; ++k) wtot[warp][k] = inc[k];
+  __syncthreads();
+  if (warp == 0) {   // row nw of wtot receives the totals
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int t = lane < nw ? wtot[lane][k] : 0;
+      int x = t;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += n;
+      }
+      __syncwarp();
+      if (lane < nw) wtot[lane][k] = x - t;
+      if (lane == 31) wtot[32][k] = x;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    excl[k] = wtot[warp][k] + inc[k] - v[k];
+    total[k] = wtot[32][k];
+  }
+}
+
+// Rank of every thread's key among the block's keys (keys unique, at most
+// blockDim of them; absent keys = INT_MAX): each warp sorts its 32 keys with
+// a bitonic network in registers and lays them out as a sorted run in
+// `runs`; a thread's rank is the sum over the runs of the keys below its own,
+// found by binary search.  Ends with the block synchronised.
+__device__ __forceinline__ int block_rank(int key, int* runs) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int v = key;
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const int o = __shfl_xor_sync(0xffffffffu, v, j);
+      const bool keep_min = ((lane & j) == 0) == ((lane & k) == 0);
+      v = keep_min ? min(v, o) : max(v, o);
+    }
+  runs[warp * 32 + lane] = v;
+  __syncthreads();
+  int rank = 0;
+  for (int w = 0; w < nw; ++w) {
+    const int* r = runs + w * 32;
+    int c = 0;   // keys of run w below `key`
+#pragma unroll
+    for (int step = 16; step > 0; step >>= 1)
+      if (r[c + step - 1] < key) c += step;
+    if (c == 31 && r[31] < key) c = 32;
+    rank += c;
+  }
+  __syncthreads();
+  return rank;
+}
+
+__global__ void __launch_bounds__(kSmallSegMax) build_segments_small_kernel(const SegBuildArgs args) {
+  __shared__ int32_t s_rank_all[4 * kSmallSegMax];   // every adapter's rank, when there are few
+  __shared__ __align__(16) int32_t s_key[kSmallSegMax];   // composite keys, then work-order keys
+  __shared__ int32_t s_kr[kSmallSegMax];             // sorted position -> id | rank << 16
+  __shared__ int32_t s_start[kSmallSegMax + 1], s_adapter[kSmallSegMax], s_rnk[kSmallSegMax];
+  __shared__ int32_t s_order[kSmallSegMax];
+  __shared__ int32_t s_wcnt[32];
+  __shared__ int32_t s_wtot[33][6];
+  __shared__ int32_t s_bad, s_err;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x;
+  const int A = args.max_adapters, T = args.T;
+  const SegDev& sd = args.seg;
+  pdl_trigger();
+
+  // (1) ids and ranks: one round of independent loads when the ranks fit
+  const bool rank_smem = A <= 4 * nthr;
+  const int key = tid < T ? args.token_adapter[tid] : -1;
+  if (rank_smem)
+    for (int a = tid; a < A; a += nthr) s_rank_all[a] = args.rank[a];
+  if (tid == 0) {
+    s_bad = 0;
+    s_err = 0;
+    // No apply kernel runs now, so the apply kernel's barrier count can be
+    // reset: a call that gave up part-way cannot leave later calls a stale count.
+    if (args.grid_sync) args.grid_sync[kSyncCount] = 0;
+  }
+  __syncthreads();
+  const bool in_range = key >= 0 && key < A;
+  const int r = in_range ? (rank_smem ? s_rank_all[key] : __ldg(args.rank + key)) : 0;
+  const bool valid = in_range && r > 0;
+  if (tid < T && !valid && key != -1) {
+    atomicAdd(&s_bad, 1);
+    atomicCAS(&s_err, 0, in_range ? -4 /* SLORA_ERR_NOT_RESIDENT */ : -1 /* SLORA_ERR_INVALID */);
+  }
+  const int ckey = valid ? (key << 10) | tid : 0x7fffffff;
+  const int n_sorted = __syncthreads_count(valid);
+
+  // (2) sorted position = keys below this one
+  const int pos = block_rank(ckey, s_key);
+  if (valid) {
+    s_kr[pos] = key | (r << 16);
+    sd.perm[pos] = tid;
+  }
+  __syncthreads();
+
+  // (3) segment heads in sorted order, numbered by a ballot scan
+  const int kr = tid < n_sorted ? s_kr[tid] : 0;
+  const bool head = tid < n_sorted && (tid == 0 || (s_kr[tid - 1] & 0xffff) != (kr & 0xffff));
+  const unsigned hb = __ballot_sync(0xffffffffu, head);
+  if (lane == 0) s_wcnt[warp] = __popc(hb);
+  __syncthreads();
+  int seg_base = 0, S = 0;
+  for (int w = 0; w < (nthr >> 5); ++w) {
+    const int c = s_wcnt[w];
+    if (w < warp) seg_base += c;
+    S += c;
+  }
+  if (head) {
+    const int sg = seg_base + __popc(hb & ((1u << lane) - 1u));
+    s_start[sg] = tid;
+    s_adapter[sg] = kr & 0xffff;
+    s_rnk[sg] = kr >> 16;
+  }
+  if (tid == 0) {
+    s_start[S] = n_sorted;
+    sd.counts[kNumSegs] = S;
+    sd.counts[kNSorted] = n_sorted;
+    sd.counts[kBadTokens] = s_bad;
+    if (s_err != 0) atomicCAS(args.error, 0, s_err);
+  }
+  __syncthreads();
+
+  // (4) work order: (256 - rank, segment) keys, ranked like (2)
+  const int wkey = tid < S ? ((kMaxRank - s_rnk[tid]) << 10) | tid : 0x7fffffff;
+  const int q = block_rank(wkey, s_key);
+  if (tid < S) s_order[q] = tid;
+  __syncthreads();
+
+  // (5) work units per work-order position, their prefix sums, descriptors
+  int u[6] = {0, 0, 0, 0, 0, 0};
+  int sg = 0, len = 0, rk = 0;
+  if (tid < S) {
+    sg = s_order[tid];
+    len = s_start[sg + 1] - s_start[sg];
+    rk = s_rnk[sg];
+    const int ntt = (len + kTT - 1) / kTT;
+    const int nrc = (rk + kShrinkRows - 1) / kShrinkRows;
+    const int nmt = (len + kTcM - 1) / kTcM;
+    const bool is_short = len < args.tc_threshold;
+    u[0] = ntt * nrc;
+    u[1] = ntt;
+    u[2] = is_short ? ntt * nrc : 0;
+    u[3] = is_short ? ntt : 0;
+    u[4] = nmt;
+    u[5] = is_short ? 0 : nmt;
+  }
+  int ex[6], tot[6];
+  small_block_scan<6>(u, ex, tot, s_wtot);
+  int32_t* const pre[6] = {sd.cc_shrink_all, sd.cc_tile_all, sd.cc_shrink_short, sd.cc_tile_short,
+                           sd.tc_tile_all, sd.tc_tile_long};
+  if (tid < S) {
+#pragma unroll
+    for (int k = 0; k < 6; ++k) pre[k][tid] = ex[k];
+    sd.seg_desc[tid] = make_int4(s_adapter[sg], rk, s_start[sg], s_start[sg] + len);
+    sd.seg_order[tid] = sg;
+    sd.seg_adapter[tid] = s_adapter[tid];
+    sd.seg_rank[tid] = s_rnk[tid];
+  }
+  if (tid < S) sd.seg_start[tid] = s_start[tid];
+  if (tid == 0) {
+    sd.seg_start[S] = s_start[S];   // S may equal the block size
+    constexpr int idx[6] = {kCcShrinkAll, kCcTileAll, kCcShrinkShort, kCcTileShort, kTcTileAll, kTcTileLong};
+#pragma unroll
+    for (int k = 0; k < 6; ++k) {
+      pre[k][S] = tot[k];
+      sd.counts[idx[k]] = tot[k];
+    }
+  }
+}
+
 // ---- the CUDA-core apply kernel: shrink, grid barrier, expand (one launch) --------
 // Persistent CTA per SM (grid = number of SMs, all CTAs resident at once):
 // warp 8 is the producer, warps 0-7 consume.  Every CTA first runs its shrink
@@ -612,9 +828,15 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
 // Shrink unit = (segment position q, token tile of <= kTT tokens, chunk of 8
 // rank rows, projection); projection varies fastest.  Per K chunk of <=
 // kShrinkK elements (never crossing a page) a stage holds the 8 A rows, read
-// straight from their pool pages, and the tile's x rows; consumer warp w dots
-// A row w against the x rows, keeps per-lane partial sums across the unit's
-// chunks, reduces them with shuffles and writes v (fp32).
+// straight from their pool pages, and the tile's x rows, each row 16 bytes
+// longer than the chunk.  The eight consumer warps split the chunk's K range
+// in 16-element steps; a step is one ldmatrix (8 A rows and the tile's x rows
+// at once) and one warp-level m16n8k16 MMA (16-bit inputs, fp32 accumulation;
+// rank rows on M, tokens on N).  Its M and N are mostly padding, but one MMA
+// replaces the 512 conversions and multiply-adds the CUDA cores would issue
+// for those 16 K values, which is what bounds this phase: the HBM bytes of a
+// stage arrive in about 1,500 cycles.  At the unit's end the warps' partial
+// sums meet in shared memory and v is written (fp32).
 //
 // Between the phases the CTAs meet once (a grid barrier on two counters in
 // global memory): the expand phase reads v rows that any CTA may have written.
@@ -634,9 +856,13 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
 // fetches the next expand unit's page indices while it streams the current one.
 constexpr int kStages = 4;                             // ring depth (also the v item-ring depth)
 constexpr int kShrinkK = 2048;                         // K chunk (elements) of a shrink stage
+// Shrink rows are kShrinkPitch elements apart: 16 bytes past the chunk, so
+// the 8 rows one ldmatrix phase reads sit in 8 different 16-byte bank groups.
+constexpr int kShrinkPitch = kShrinkK + 8;
 constexpr int kExpandRK = 8;                           // B rows per expand stage
-constexpr int kStageElems = kShrinkRows * kShrinkK + kTT * kShrinkK;   // 48 KB of 16-bit elements
-constexpr int kRowsOff = kShrinkRows * kShrinkK;       // x (shrink) / y (expand) rows start here
+constexpr int kStageElems = (kShrinkRows + kTT) * kShrinkPitch;   // 48.2 KB of 16-bit elements
+constexpr int kRowsOff = kShrinkRows * kShrinkK;       // y rows of an expand stage start here
+static_assert((kShrinkPitch * 2) % 16 == 0 && (kStageElems * 2) % 16 == 0, "bulk copies need 16-byte rows");
 constexpr int kPagesPerLane = kMaxRank / 32;           // B-row page indices one lane prefetches
 static_assert(kExpandRK * kExpandCols <= kRowsOff, "B rows of a stage must fit before the x/y rows");
 static_assert(kTT * kExpandCols <= kStageElems - kRowsOff, "y rows of a stage must fit");
@@ -656,12 +882,20 @@ struct VPending {                   // an expand unit whose v rows wait for the 
 struct ApplySmem {
   uint16_t st[kStages][kStageElems];
   float V[kStages][kTT][kMaxRank];
+  // Shrink: the consumer warps' partial sums of a unit (8 rank rows x 4
+  // tokens each), summed by warp 0.  Unit u uses buffer u % kRedBufs: a warp
+  // can run at most kStages stages (so kStages units) ahead of warp 0, so
+  // warp 0 has read a buffer before any warp writes it again.
+  float red[kStages + 1][kCcConsumerWarps][32];
+  uint64_t redbar[kStages + 1];
   StageMeta meta[kStages];
   VPending pend[kStages];
   uint64_t full[kStages], empty[kStages], vfull[kStages];
   int32_t off_s[kSegSmem], off_e[kSegSmem];
   int32_t gen0;
 };
+constexpr int kRedBufs = kStages + 1;
+static_assert(sizeof(ApplySmem) <= 232448, "apply kernel shared memory exceeds 227 KB");
 
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   unsigned long long ua, ub, uc, r;
@@ -684,6 +918,47 @@ __device__ __forceinline__ int ld_acquire(const int32_t* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
+}
+
+// ldmatrix: four (or two) 8 x 8 matrices of 16-bit elements; lane l gives
+// the address of row l % 8 of matrix l / 8.
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(addr));
+}
+// Warp-level MMA, fp32 accumulation: D[16 x 8] += A[16 x 16] B[16 x 8] with
+// A rows 8..15 zero (a1 = a3 = 0), and the 8-deep form for a K tail.
+template <bool BF>
+__device__ __forceinline__ void mma_k16(float (&c)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  if constexpr (BF)
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+  else
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+template <bool BF>
+__device__ __forceinline__ void mma_k8(float (&c)[4], uint32_t a0, uint32_t b0) {
+  if constexpr (BF)
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5}, {%6}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a0), "r"(0u), "r"(b0));
+  else
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5}, {%6}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a0), "r"(0u), "r"(b0));
 }
 
 // 1-D bulk copy global -> shared through the TMA engine; completion is
@@ -737,37 +1012,8 @@ __device__ __forceinline__ void load_b_pages(const ApplyDev& d, int a, int r, in
   }
 }
 
-// Stage compute of the consumer warps, specialised on the tile's token count
-// so that no issue slot goes to absent tokens.
-template <class D, int NT>
-__device__ __forceinline__ void shrink_stage(const uint16_t* arow, const uint16_t* xrows, int n8, int lane,
-                                             float (&acc)[kTT]) {
-  float s0[NT], s1[NT];
-#pragma unroll
-  for (int t = 0; t < NT; ++t) s0[t] = s1[t] = 0.f;
-  for (int v = lane; v < n8; v += 64) {   // two vectors per lane, independent chains
-    const bool two = v + 32 < n8;
-    float fa0[8], fa1[8];
-    unpack8<D>(*reinterpret_cast<const uint4*>(arow + v * 8), fa0);
-    unpack8<D>(two ? *reinterpret_cast<const uint4*>(arow + (v + 32) * 8) : make_uint4(0u, 0u, 0u, 0u), fa1);
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      float fx0[8], fx1[8];
-      unpack8<D>(*reinterpret_cast<const uint4*>(xrows + t * kShrinkK + v * 8), fx0);
-      unpack8<D>(two ? *reinterpret_cast<const uint4*>(xrows + t * kShrinkK + (v + 32) * 8)
-                     : make_uint4(0u, 0u, 0u, 0u),
-                 fx1);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        s0[t] = fmaf(fa0[e], fx0[e], s0[t]);
-        s1[t] = fmaf(fa1[e], fx1[e], s1[t]);
-      }
-    }
-  }
-#pragma unroll
-  for (int t = 0; t < NT; ++t) acc[t] += s0[t] + s1[t];
-}
-
+// Expand stage compute of the consumer threads, specialised on the tile's
+// token count so that no issue slot goes to absent tokens.
 template <class D, int NT>
 __device__ __forceinline__ void expand_stage(const uint16_t* brows, const float (*V)[kMaxRank], int k0, int nk,
                                              int col, float2 (&acc)[kTT][4]) {
@@ -796,6 +1042,7 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
       mbar_init(&sm.empty[s], kCcConsumerWarps);
       mbar_init(&sm.vfull[s], 1);
     }
+    for (int s = 0; s < kRedBufs; ++s) mbar_init(&sm.redbar[s], kCcConsumerWarps);
     mbar_fence_init();
   }
   pdl_wait();  // the work lists come from the segment kernel; an earlier apply has finished
@@ -967,10 +1214,12 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
             }
             __syncwarp();
             uint16_t* dst = sm.st[stage];
+            // A row i and token row t at rows i and kShrinkRows + t of the stage
             if (lane < nrows)
-              bulk_load(dst + lane * kShrinkK, d.pool + (int64_t)my * d.H + o, (uint32_t)len * 2u, &sm.full[stage]);
+              bulk_load(dst + lane * kShrinkPitch, d.pool + (int64_t)my * d.H + o, (uint32_t)len * 2u,
+                        &sm.full[stage]);
             else if (lane >= kShrinkRows && lane < kShrinkRows + ntok)
-              bulk_load(dst + kRowsOff + (lane - kShrinkRows) * kShrinkK, xbase + (int64_t)my * P.ldx + (int64_t)c * d.H + o,
+              bulk_load(dst + lane * kShrinkPitch, xbase + (int64_t)my * P.ldx + (int64_t)c * d.H + o,
                         (uint32_t)len * 2u, &sm.full[stage]);
             mark(issued, ipar, stage, phase);
             if (++stage == kStages) {
@@ -1110,59 +1359,83 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
   } else {  // ====================================================== consumer warps
     uint32_t stage = 0, phase = 0;
     bool ok = true;
-    // ---- shrink units: warp w owns rank row k0 + w of the unit
-    for (int64_t i = 0; i < ns && ok; ++i) {
-      float acc[kTT];
-#pragma unroll
-      for (int t = 0; t < kTT; ++t) acc[t] = 0.f;
-      while (true) {
-        if (!mbar_wait(&sm.full[stage], phase)) {
-          ok = false;
-          break;
-        }
-        const StageMeta& ms = sm.meta[stage];
-        const int ntok = ms.ntok, len = ms.len, nrows = ms.nrows, last = ms.last;
-        const int p = ms.p, j0 = ms.j0, k0 = ms.k0;
-        const float sa = ms.sa;
-        if (warp < nrows) {
-          float accs[kTT];
-#pragma unroll
-          for (int t = 0; t < kTT; ++t) accs[t] = 0.f;
-          const uint16_t* arow = &sm.st[stage][warp * kShrinkK];
-          const uint16_t* xrows = &sm.st[stage][kRowsOff];
-          const int n8 = len >> 3;
-          switch (ntok) {
-            case 1: shrink_stage<D, 1>(arow, xrows, n8, lane, accs); break;
-            case 2: shrink_stage<D, 2>(arow, xrows, n8, lane, accs); break;
-            case 3: shrink_stage<D, 3>(arow, xrows, n8, lane, accs); break;
-            default: shrink_stage<D, 4>(arow, xrows, n8, lane, accs); break;
+    // ---- shrink units: warp w takes the 16-element K steps w, w + 8, ... of
+    // every stage; per step one ldmatrix.x4 brings A rows 0-7 (k, k + 8) and
+    // the tile's token rows (k, k + 8): lanes 0-15 address the A rows, lanes
+    // 16-31 the token rows (rows 4-7 of the MMA's N side repeat tokens 0-3;
+    // those accumulator columns are never read).
+    {
+      const int lq = lane >> 3, lr = lane & 7;
+      const int lrow = lq < 2 ? lr : kShrinkRows + (lr & 3);
+      const uint32_t lofs = (uint32_t)(lrow * kShrinkPitch + (lq & 1) * 8) * 2u;
+      // the K tail of 8 (m16n8k8): lanes 0-7 A rows, lanes 8-15 token rows
+      const uint32_t lofs8 = (uint32_t)((lane < 8 ? lane : kShrinkRows + (lane & 3)) * kShrinkPitch) * 2u;
+      uint32_t rb = 0, rph = 0;   // partial-sum buffer of this unit and its phase
+      for (int64_t i = 0; i < ns && ok; ++i) {
+        float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+        while (true) {
+          if (!mbar_wait(&sm.full[stage], phase)) {
+            ok = false;
+            break;
           }
-#pragma unroll
-          for (int t = 0; t < kTT; ++t) acc[t] += accs[t];
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[stage]);
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1;
-        }
-        if (last) {
-          if (warp < nrows) {
-            float tot[kTT];
-#pragma unroll
-            for (int t = 0; t < kTT; ++t) {
-              tot[t] = acc[t];
-#pragma unroll
-              for (int off = 16; off > 0; off >>= 1) tot[t] += __shfl_xor_sync(0xffffffffu, tot[t], off);
-            }
-            if (lane == 0) {
-              float* vrow = d.proj[p].v + (int64_t)j0 * d.v_ld + k0 + warp;
-#pragma unroll
-              for (int t = 0; t < kTT; ++t)
-                if (t < ntok) vrow[(int64_t)t * d.v_ld] = sa * tot[t];
-            }
+          const StageMeta& ms = sm.meta[stage];
+          const int ntok = ms.ntok, len = ms.len, nrows = ms.nrows, last = ms.last;
+          const int p = ms.p, j0 = ms.j0, k0 = ms.k0;
+          const float sa = ms.sa;
+          const uint32_t sbase = smem_addr(&sm.st[stage][0]);
+          const int nk16 = len >> 4;
+          int ks = warp;
+          for (; ks + kCcConsumerWarps < nk16; ks += 2 * kCcConsumerWarps) {   // two chains in flight
+            uint32_t r0[4], r1[4];
+            ldsm_x4(r0, sbase + lofs + (uint32_t)ks * 32u);
+            ldsm_x4(r1, sbase + lofs + (uint32_t)(ks + kCcConsumerWarps) * 32u);
+            mma_k16<D::kBf16>(acc0, r0[0], r0[1], r0[2], r0[3]);
+            mma_k16<D::kBf16>(acc1, r1[0], r1[1], r1[2], r1[3]);
           }
-          break;
+          if (ks < nk16) {
+            uint32_t r0[4];
+            ldsm_x4(r0, sbase + lofs + (uint32_t)ks * 32u);
+            mma_k16<D::kBf16>(acc0, r0[0], r0[1], r0[2], r0[3]);
+          }
+          if ((len & 15) && warp == nk16 % kCcConsumerWarps) {   // chunk lengths are multiples of 8
+            uint32_t r0[2];
+            ldsm_x2(r0, sbase + lofs8 + (uint32_t)nk16 * 32u);
+            mma_k8<D::kBf16>(acc1, r0[0], r0[1]);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+          if (last) {
+            // lane (g, c) holds rank row g = lane / 4, tokens 2c and 2c + 1
+            float* red = &sm.red[rb][0][0];
+            if ((lane & 3) < 2) {
+              red[warp * 32 + (lane >> 2) * kTT + 2 * (lane & 3)] = acc0[0] + acc1[0];
+              red[warp * 32 + (lane >> 2) * kTT + 2 * (lane & 3) + 1] = acc0[1] + acc1[1];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.redbar[rb]);
+            if (warp == 0) {   // the eight partial sums, in warp order
+              bool got = true;
+              if (lane == 0) got = mbar_wait(&sm.redbar[rb], rph);
+              if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
+                ok = false;
+                break;
+              }
+              const int row = lane / kTT, t = lane % kTT;
+              float tot = 0.f;
+#pragma unroll
+              for (int w = 0; w < kCcConsumerWarps; ++w) tot += red[w * 32 + lane];
+              if (row < nrows && t < ntok) d.proj[p].v[(int64_t)(j0 + t) * d.v_ld + k0 + row] = sa * tot;
+            }
+            if (++rb == kRedBufs) {
+              rb = 0;
+              rph ^= 1;
+            }
+            break;
+          }
         }
       }
     }
@@ -1310,6 +1583,12 @@ cudaError_t prepare_kernels(int /*device*/) {
 }
 
 cudaError_t launch_build_segments(const SegBuildArgs& in, cudaStream_t st) {
+  if (in.T <= kSmallSegMax) {
+    // one token per thread; whole warps, at least two
+    const int threads = in.T <= 64 ? 64 : (in.T + 31) / 32 * 32;
+    build_segments_small_kernel<<<1, threads, 0, st>>>(in);
+    return cudaGetLastError();
+  }
   // Shared memory: the histogram, then (if they fit) the rank cache and the
   // segment arrays; anything that does not fit stays in global memory.
   SegBuildArgs a = in;

@@ -59,11 +59,9 @@ def test_bmm_comparator_per_adapter_scale():
     case.pool.close()
 
 
-def test_bmm_comparator_full_size_llama7b_decode_sampled():
-    """The benchmark workload (H=4096, q/k/v/o, 256 tokens, 1000 adapters), sampled rows."""
+def test_bmm_comparator_full_size_llama7b_decode_every_row():
+    """The 7B decode batch (H=4096, q/k/v/o, 256 tokens, 1000 adapters): every row."""
     wl = workloads.make("llama7b_decode")
     case = G.build_case(wl, weights="touched")
-    rng = np.random.default_rng(3)
-    rows = np.asarray(sorted(set(rng.choice(wl.T, 48, replace=False).tolist()) | {0, wl.T - 1}), dtype=np.int32)
-    _run_bmm(case, rows=rows)
+    _run_bmm(case)
     case.pool.close()

@@ -131,21 +131,19 @@ def test_full_size_llama7b_decode():
     case.pool.close()
 
 
-def _sample_rows(wl, n, seed=0):
-    rng = np.random.default_rng(seed)
-    rows = set(rng.choice(wl.T, size=min(n, wl.T), replace=False).tolist())
-    rows |= {0, wl.T - 1}
-    return np.asarray(sorted(rows), dtype=np.int32)
-
-
-def test_full_size_llama7b_prefill_sampled():
+def test_full_size_llama7b_prefill_every_row():
+    """The prefill batch (8,561 tokens, 29 segments): every row of every
+    projection against the oracle, in every mode and with every segment on
+    the tensor cores as well as with the AUTO split."""
     wl = workloads.make("llama7b_prefill")
     case = G.build_case(wl, weights="touched")
-    rows = _sample_rows(wl, 384)
-    want = G.oracle_outputs(case, tokens=rows)
+    want = G.oracle_outputs(case)
     for mode in (slora.MODE_DECODE, slora.MODE_AUTO, slora.MODE_PREFILL):
-        seg, _ = _run_and_check(case, mode, want, rows=rows)
+        seg, _ = _run_and_check(case, mode, want)
     _check_segments(case, seg)
+    for thr in (0, 200):
+        slora.slora_set_tc_threshold(case.pool.handle, thr)
+        _run_and_check(case, slora.MODE_AUTO, want)
     case.pool.close()
 
 
@@ -239,6 +237,44 @@ def test_segment_build_token_orders():
         assert np.array_equal(adapter, want.seg_adapter), name
         status = pool.status()   # reading clears it
         assert (status != slora.OK) == bad, (name, status)
+    pool.close()
+
+
+def test_segment_build_small_batches():
+    """Batches of up to 1024 tokens take the one-token-per-thread segment
+    kernel: checked bit for bit at warp and block edges, with every token on
+    its own adapter (as many segments as threads), one adapter for every
+    token, base-only tokens, and invalid and non-resident ids."""
+    wl = workloads.make(SMALL["many_tokens_f16"])
+    case = G.build_case(wl, max_tokens=1024)
+    pool = case.pool
+    slora.slora_adapter_evict(pool.handle, 7)
+    rank = case.oracle_pool.rank.copy()
+    rank[7] = 0
+    N = wl.spec.num_adapters
+    rng = np.random.default_rng(11)
+    orders = {}
+    for T in (1, 2, 31, 32, 33, 63, 64, 65, 255, 256, 300):
+        ids = rng.permutation(np.setdiff1d(np.arange(N), [7]))[:T]   # every token its own adapter
+        orders[f"distinct {T}"] = (ids.astype(np.int32), False)
+    orders["one adapter x 1024"] = (np.full(1024, 5, np.int32), False)
+    orders["random 512"] = (rng.integers(-1, N, 512).astype(np.int32), True)   # includes adapter 7
+    orders["random 1024"] = (rng.choice(np.arange(40), 1024).astype(np.int32), True)
+    orders["bad ids 1000"] = (rng.choice([0, 1, 2, 7, -1, -2, N, N + 5], 1000).astype(np.int32), True)
+    orders["base only 77"] = (np.full(77, -1, np.int32), False)
+    for name, (ta, bad) in orders.items():
+        seg = pool.build_segments(torch.from_numpy(ta).to("cuda"))
+        torch.cuda.synchronize()
+        want = opool.build_segments(ta, rank)
+        perm, start, adapter, counts = G.seg_arrays(seg)
+        assert counts[0] == want.num_segs and counts[1] == want.perm.shape[0], name
+        assert counts[2] == want.bad_tokens, name
+        assert np.array_equal(perm, want.perm), name
+        assert np.array_equal(start, want.seg_start), name
+        assert np.array_equal(adapter, want.seg_adapter), name
+        status = pool.status()
+        assert (status != slora.OK) == (want.bad_tokens > 0), (name, status)
+        assert bad or want.bad_tokens == 0, name
     pool.close()
 
 
