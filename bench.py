@@ -43,7 +43,8 @@ sys.path.insert(0, ROOT)
 METRIC = "lora_delta_tokens_per_s_per_layer"
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20
-TC_THRESHOLD = 64          # the library's default: segments of >= 64 tokens use the tensor cores
+TC_THRESHOLD = 8           # the library's AUTO defaults: segments of >= 8 tokens on the tensor cores,
+TC_MIN_BATCH = 2048        # in batches of >= 2048 tokens
 HEADLINE = "llama13b_mlp_decode"
 EXTRA = ("llama7b_decode", "llama7b_prefill")
 DEFAULT_MODE = {"llama13b_mlp_decode": "decode", "llama7b_decode": "decode", "llama7b_prefill": "prefill",
@@ -493,7 +494,7 @@ def measure(name, mode_name, args, rep, device, rank, world):
     slora.slora_timing_enable(pool.handle, False)
 
     # ---- roofline of the dominant kernel
-    thr = {"decode": None, "auto": tc_threshold, "prefill": 0}[mode_name]
+    thr = {"decode": None, "auto": tc_threshold if wl.T >= TC_MIN_BATCH else None, "prefill": 0}[mode_name]
     ab = algorithmic_bytes(wl, thr)
     fl = algorithmic_flops(wl, thr)
     per_kernel = {}

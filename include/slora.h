@@ -64,7 +64,7 @@ extern "C" {
 #define SLORA_F16 0
 #define SLORA_BF16 1
 
-#define SLORA_MODE_AUTO 0    /* CUDA-core tiles below the tensor-core threshold, tcgen05 tiles above */
+#define SLORA_MODE_AUTO 0    /* large batches: tcgen05 for long segments, CUDA cores for the rest; small batches: CUDA cores */
 #define SLORA_MODE_DECODE 1  /* every segment on the CUDA-core gather kernels */
 #define SLORA_MODE_PREFILL 2 /* every segment on the tcgen05 kernels (CUDA-core kernels when the page size is not a multiple of 64) */
 
@@ -285,9 +285,52 @@ int slora_timing_enable(slora_pool* pool, int32_t enable);
 int slora_timing_read(slora_pool* pool, int32_t capacity, const char** names, double* ms,
                       int64_t* launches, int32_t* n);
 
-/* Tensor-core threshold of SLORA_MODE_AUTO: segments with at least this many
- * tokens use the tcgen05 kernels (default 64). */
+/*
+ * SLORA_MODE_AUTO's split.  In a batch of at least `tc_min_batch` tokens
+ * (default 2048), segments of at least `tc_threshold` tokens (default 8) run
+ * on the tcgen05 kernels and the rest on the CUDA-core kernel; a smaller
+ * batch runs wholly on the CUDA-core kernel.  The defaults come from
+ * measurements on GB300: on the 7B prefill batch (8,561 tokens) AUTO then
+ * matches PREFILL, while on decode batches of 256-512 tokens the few long
+ * segments leave the tensor-core kernels bound by latency and the CUDA-core
+ * kernel is 1.8x faster.  tc_threshold takes effect at the next
+ * slora_build_segments; tc_min_batch at the next apply.
+ */
 int slora_set_tc_threshold(slora_pool* pool, int32_t min_tokens);
+int slora_set_tc_min_batch(slora_pool* pool, int32_t min_tokens);
+
+/*
+ * Failure injection on the host, for tests of the error paths (the pages'
+ * concern about the adapter manager under dynamic loading: cmlonder.com
+ * newsletter, section "Iddia ve Gerceklik").  Arms one fault on this pool;
+ * it fires once, on the nth (counted from 1) event of its kind from now on:
+ *   SLORA_FAULT_PAGE_ALLOC  a call that takes pages (slora_pages_alloc,
+ *                           slora_adapter_load) fails with SLORA_ERR_OOM as
+ *                           if the pool were full; nothing changes;
+ *   SLORA_FAULT_COPY        a copy or kernel that slora_adapter_load enqueues
+ *                           fails as a CUDA error would: the load returns
+ *                           SLORA_ERR_CUDA and, once the copy stream has
+ *                           finished what the load queued before the failure,
+ *                           its pages are released again, the host state
+ *                           (slora_pool_snapshot) exactly as before the call.
+ * SLORA_FAULT_NONE (or nth = 0) disarms.  The environment variable
+ * SLORA_FAULT="alloc:N" or "copy:N" arms the same fault in every pool the
+ * process creates.  Nothing here touches a GPU.
+ */
+#define SLORA_FAULT_NONE 0
+#define SLORA_FAULT_PAGE_ALLOC 1
+#define SLORA_FAULT_COPY 2
+int slora_debug_set_fault(slora_pool* pool, int32_t kind, int64_t nth);
+
+/*
+ * Polls that each of the CUDA-core apply kernel's waits on other warps
+ * (stages, v rows, partial sums, the grid barrier) makes before it gives up
+ * (0: the built-in limit, 2^24).  A kernel that gives up records
+ * SLORA_ERR_TIMEOUT in the device status (slora_device_status), waits with
+ * the built-in limit for its own copies still in flight, and returns; y may
+ * be partly updated.  For tests of the time-out path.
+ */
+int slora_debug_set_wait_limit(slora_pool* pool, uint32_t polls);
 
 const char* slora_last_error_string(void);
 

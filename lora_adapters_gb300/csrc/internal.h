@@ -121,6 +121,7 @@ struct ApplyDev {
   // kernel also zeroes it), [kSyncGen] generation (incremented when the
   // barrier opens).  Zero-initialised with the pool.
   int32_t* grid_sync;
+  uint32_t wait_limit;           // polls of a wait on other warps before it gives up (0: kWaitLimit)
 };
 enum : int { kSyncCount = 0, kSyncGen = 1, kGridSyncInts = 2 };
 

@@ -145,8 +145,8 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait for the phase of the given parity to complete.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit = kWaitLimit) {
+  for (uint32_t i = 0; i < limit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
@@ -1077,6 +1077,9 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
     return R + (((R & 1) ? G - 1 - b : b) < rem ? 1 : 0);
   };
   const int64_t ns = snake_count(Gs), ne = snake_count(Ge);   // this CTA's units
+  // Polls of a wait on other warps (or CTAs) before this kernel gives up;
+  // the waits for its own copies in flight before it exits keep kWaitLimit.
+  const uint32_t lim = d.wait_limit ? d.wait_limit : kWaitLimit;
 
   if (warp == kCcConsumerWarps) {  // ============================ producer warp
     uint32_t stage = 0, phase = 0, nitem = 0;
@@ -1113,7 +1116,7 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
     // free slot also watches the grid barrier (the consumers cannot free a
     // slot before those v rows arrive), without blocking on the slot.
     auto acquire = [&]() -> bool {
-      for (uint32_t it = 0; it < kWaitLimit; ++it) {
+      for (uint32_t it = 0; it < lim; ++it) {
         int got = 0;
         if (lane == 0)
           got = (npend > 0 ? mbar_test_wait(&sm.empty[stage], phase ^ 1) : mbar_try_wait(&sm.empty[stage], phase ^ 1))
@@ -1342,14 +1345,16 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
     // barrier here
     if (ok && npend > 0) {
       bool open = false;
-      for (uint32_t it = 0; it < kWaitLimit && !open; ++it) open = barrier_open();
+      for (uint32_t it = 0; it < lim && !open; ++it) open = barrier_open();
       if (open) release_pending();
       else ok = false;
     }
-    // No copy may still be landing when the CTA exits.  On the normal path
-    // the consumers have waited for every stage and every v buffer; after a
-    // time-out, wait (bounded) for the last phase issued on each barrier.
-    if (!ok && lane == 0) {
+    // No copy may still be landing when the CTA exits: wait (with the
+    // built-in limit) for the last phase issued on each barrier.  On the
+    // normal path the consumers have already waited for every stage and v
+    // buffer and these waits return at once; they matter when the consumers
+    // gave up, which they can do while the producer never had to.
+    if (lane == 0) {
       for (int s2 = 0; s2 < kStages; ++s2) {
         if (issued >> s2 & 1u) (void)mbar_wait(&sm.full[s2], ipar >> s2 & 1u);
         if (vissued >> s2 & 1u) (void)mbar_wait(&sm.vfull[s2], vpar >> s2 & 1u);
@@ -1374,7 +1379,7 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
       for (int64_t i = 0; i < ns && ok; ++i) {
         float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
         while (true) {
-          if (!mbar_wait(&sm.full[stage], phase)) {
+          if (!mbar_wait(&sm.full[stage], phase, lim)) {
             ok = false;
             break;
           }
@@ -1419,7 +1424,7 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
             if (lane == 0) mbar_arrive(&sm.redbar[rb]);
             if (warp == 0) {   // the eight partial sums, in warp order
               bool got = true;
-              if (lane == 0) got = mbar_wait(&sm.redbar[rb], rph);
+              if (lane == 0) got = mbar_wait(&sm.redbar[rb], rph, lim);
               if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
                 ok = false;
                 break;
@@ -1463,7 +1468,7 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
         for (int e = 0; e < 4; ++e) acc[t][e] = make_float2(0.f, 0.f);
       bool first = true;
       while (true) {
-        if (!mbar_wait(&sm.full[stage], phase)) {
+        if (!mbar_wait(&sm.full[stage], phase, lim)) {
           ok = false;
           break;
         }
@@ -1471,7 +1476,7 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
         const int ntok = me.ntok, len = me.len, nk = me.nk, k0 = me.k0, buf = me.buf, last = me.last;
         if (first) {
           first = false;
-          if (!mbar_wait(&sm.vfull[buf], (uint32_t)me.vph)) {
+          if (!mbar_wait(&sm.vfull[buf], (uint32_t)me.vph, lim)) {
             ok = false;
             break;
           }

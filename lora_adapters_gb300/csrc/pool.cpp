@@ -28,6 +28,8 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/slora.h"
 #include "internal.h"
 
@@ -36,6 +38,14 @@ using namespace slora;
 namespace {
 
 thread_local std::string g_err;
+
+// An NVTX range around every call of the C ABI, named after the call, so a
+// timeline profiler shows where the host spends its time per call.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+#define SLORA_RANGE(name) NvtxRange nvtx_range_(name)
 
 int fail(int code, const char* fmt, ...) {
   char buf[512];
@@ -76,7 +86,10 @@ struct slora_pool {
   int64_t pt_stride = 0;         // entries reserved per adapter id
   int64_t staging_elems = 0;
   bool planning = true;
-  int32_t tc_threshold = 64;
+  // AUTO mode: segments of at least tc_threshold tokens on the tensor cores,
+  // in batches of at least tc_min_batch tokens (smaller batches: CUDA cores)
+  int32_t tc_threshold = 8;
+  int32_t tc_min_batch = 2048;
 
   // allocator
   std::vector<int32_t> owner;    // per page: -1 free, -2 KV, else adapter id
@@ -120,6 +133,11 @@ struct slora_pool {
   float* d_vpart = nullptr;      // tc_shrink's K-part partial sums, [kTcShrinkParts][kMaxProj][rows][v_ld]
   CUtensorMap pool_map{};
   CUtensorMap vhi_map[kMaxProj]{}, vlo_map[kMaxProj]{};
+
+  // fault injection on the host (slora_debug_set_fault / SLORA_FAULT):
+  // countdown to the failing event per kind, 0 = disarmed
+  int64_t fault_left[3] = {0, 0, 0};
+  uint32_t wait_limit = 0;       // polls of the apply kernel's bounded waits (0: the built-in limit)
 
   // timing
   bool timing = false;
@@ -219,6 +237,25 @@ int check_device_pool(const slora_pool* p) {
   if (!p) return fail(SLORA_ERR_INVALID, "pool is NULL");
   if (p->planning) return fail(SLORA_ERR_INVALID, "planning pool (no device buffer): no GPU work");
   return SLORA_OK;
+}
+
+// ---- fault injection ----------------------------------------------------------
+// True when this event is the one the armed fault of `kind` names (it then
+// disarms).  The caller fails the call as the real failure would.
+bool fault_fires(slora_pool* p, int kind) {
+  int64_t& left = p->fault_left[kind];
+  if (left <= 0) return false;
+  return --left == 0;
+}
+
+// SLORA_FAULT="alloc:N" or "copy:N" arms the fault of slora_debug_set_fault
+// for every pool the process creates.
+void arm_fault_from_env(slora_pool* p) {
+  const char* env = std::getenv("SLORA_FAULT");
+  if (!env) return;
+  long long n = 0;
+  if (std::sscanf(env, "alloc:%lld", &n) == 1 && n > 0) p->fault_left[SLORA_FAULT_PAGE_ALLOC] = n;
+  else if (std::sscanf(env, "copy:%lld", &n) == 1 && n > 0) p->fault_left[SLORA_FAULT_COPY] = n;
 }
 
 // ---- timing ---------------------------------------------------------------------
@@ -347,6 +384,7 @@ int slora_pool_create(slora_pool** out, void* d_pool, int64_t num_pages, int32_t
                       int32_t dtype, int32_t max_adapters, int32_t max_rank, int32_t max_tokens,
                       int32_t num_proj, const int32_t* proj_in, const int32_t* proj_out,
                       void* compute_stream, void* copy_stream) {
+  SLORA_RANGE("slora_pool_create");
   if (!out) return fail(SLORA_ERR_INVALID, "out is NULL");
   *out = nullptr;
   if (num_pages <= 0 || num_pages >= (1ll << 31))
@@ -400,6 +438,7 @@ int slora_pool_create(slora_pool** out, void* d_pool, int64_t num_pages, int32_t
   p->rank_h.assign((size_t)max_adapters, 0);
   p->npages_h.assign((size_t)max_adapters, 0);
   p->planning = (d_pool == nullptr);
+  arm_fault_from_env(p);
 
   if (p->planning) {
     p->pt_h = static_cast<int32_t*>(std::malloc(sizeof(int32_t) * (size_t)pt_entries));
@@ -505,6 +544,7 @@ int slora_pool_create(slora_pool** out, void* d_pool, int64_t num_pages, int32_t
 }
 
 int slora_pool_destroy(slora_pool* p) {
+  SLORA_RANGE("slora_pool_destroy");
   if (!p) return fail(SLORA_ERR_INVALID, "pool is NULL");
   int rc = SLORA_OK;
   if (!p->planning) {
@@ -520,15 +560,18 @@ int slora_pool_destroy(slora_pool* p) {
 }
 
 int slora_pages_alloc(slora_pool* p, int64_t n, int32_t* out_pages) {
+  SLORA_RANGE("slora_pages_alloc");
   if (int rc = check_pool(p)) return rc;
   if (n < 0 || (n > 0 && !out_pages)) return fail(SLORA_ERR_INVALID, "bad count or NULL output");
   if (n > p->free_count)
     return fail(SLORA_ERR_OOM, "need %lld pages, %lld free", (long long)n, (long long)p->free_count);
+  if (fault_fires(p, SLORA_FAULT_PAGE_ALLOC)) return fail(SLORA_ERR_OOM, "injected page-allocation failure");
   take_lowest(p, n, kOwnerKV, out_pages);
   return SLORA_OK;
 }
 
 int slora_pages_free(slora_pool* p, int64_t n, const int32_t* pages) {
+  SLORA_RANGE("slora_pages_free");
   if (int rc = check_pool(p)) return rc;
   if (n < 0 || (n > 0 && !pages)) return fail(SLORA_ERR_INVALID, "bad count or NULL pages");
   int64_t i = 0;
@@ -552,6 +595,7 @@ int slora_pages_free(slora_pool* p, int64_t n, const int32_t* pages) {
 
 int slora_pool_info(const slora_pool* p, int64_t* free_pages, int64_t* num_pages, int32_t* page_elems,
                     int64_t* pages_per_rank) {
+  SLORA_RANGE("slora_pool_info");
   if (int rc = check_pool(p)) return rc;
   if (free_pages) *free_pages = p->free_count;
   if (num_pages) *num_pages = p->num_pages;
@@ -562,6 +606,7 @@ int slora_pool_info(const slora_pool* p, int64_t* free_pages, int64_t* num_pages
 
 int slora_adapter_load(slora_pool* p, int32_t a, int32_t rank, const void* const* h_A,
                        const void* const* h_B, void** done) {
+  SLORA_RANGE("slora_adapter_load");
   if (int rc = check_pool(p)) return rc;
   if (done) *done = nullptr;
   if (a < 0 || a >= p->max_adapters) return fail(SLORA_ERR_INVALID, "adapter id %d out of range", a);
@@ -575,6 +620,7 @@ int slora_adapter_load(slora_pool* p, int32_t a, int32_t rank, const void* const
   const int64_t n = (int64_t)rank * p->chunks_per_rank;
   if (n > p->free_count)
     return fail(SLORA_ERR_OOM, "adapter %d needs %lld pages, %lld free", a, (long long)n, (long long)p->free_count);
+  if (fault_fires(p, SLORA_FAULT_PAGE_ALLOC)) return fail(SLORA_ERR_OOM, "injected page-allocation failure");
 
   if (!p->planning && p->load_pending[a]) {
     // The previous load of this id may still read its page-table mirror.
@@ -587,12 +633,21 @@ int slora_adapter_load(slora_pool* p, int32_t a, int32_t rank, const void* const
   p->npages_h[a] = n;
   if (p->planning) return SLORA_OK;
 
+  // A failed enqueue: the pages go back and the host state is as before the
+  // call.  Work already queued on the copy stream (staging copies, the page
+  // table, the scatter into the pages) is waited for first, so that nothing
+  // writes the pages once another owner may hold them; the id's device rank
+  // stays 0, so nothing reads what it wrote.  This wait is the error path's
+  // only blocking call.
   auto rollback = [&](int code) {
     const std::string why = g_err;
+    (void)cudaStreamSynchronize(p->copy);
+    (void)cudaGetLastError();
     give_back(p, n, tab);
     std::fill(tab, tab + n, -1);
     p->rank_h[a] = 0;
     p->npages_h[a] = 0;
+    p->rank_pin[a] = 0;
     g_err = why;
     return code;
   };
@@ -604,6 +659,9 @@ int slora_adapter_load(slora_pool* p, int32_t a, int32_t rank, const void* const
     CUDA_TRY(cudaEventRecord(p->order_event, p->compute));
     CUDA_TRY(cudaStreamWaitEvent(p->copy, p->order_event, 0));
     p->rank_pin[a] = rank;
+    // every copy or kernel the load enqueues is one event of SLORA_FAULT_COPY
+    auto injected = [&]() { return fault_fires(p, SLORA_FAULT_COPY); };
+    if (injected()) return fail(SLORA_ERR_CUDA, "injected failure of a copy enqueue");
     CUDA_TRY(cudaMemcpyAsync(p->d_pt + (int64_t)a * p->pt_stride, tab, sizeof(int32_t) * (size_t)n,
                              cudaMemcpyHostToDevice, p->copy));
     int64_t off = 0;
@@ -624,17 +682,22 @@ int slora_adapter_load(slora_pool* p, int32_t a, int32_t rank, const void* const
       sd.ppo[q] = p->ppo[q];
       sd.src_base[q] = off;
       sd.entry_base[q] = (int32_t)((int64_t)rank * p->rows_before[q]);
+      if (injected()) return fail(SLORA_ERR_CUDA, "injected failure of a copy enqueue");
       CUDA_TRY(cudaMemcpyAsync(p->d_staging + off, h_A[q], bytesA, cudaMemcpyHostToDevice, p->copy));
       off += (int64_t)rank * p->proj_in[q];
+      if (injected()) return fail(SLORA_ERR_CUDA, "injected failure of a copy enqueue");
       CUDA_TRY(cudaMemcpyAsync(p->d_staging + off, h_B[q], bytesB, cudaMemcpyHostToDevice, p->copy));
       off += (int64_t)rank * p->proj_out[q];
     }
     {
       Timed tm(p, kTScatter, p->copy);
+      if (injected()) return fail(SLORA_ERR_CUDA, "injected failure of a copy enqueue");
       CUDA_TRY(launch_scatter(sd, p->copy));
       tm.done();
     }
+    if (injected()) return fail(SLORA_ERR_CUDA, "injected failure of a copy enqueue");
     CUDA_TRY(launch_set_f32(p->d_scale + a, 1.0f, p->copy));   // a fresh adapter: s_a = 1
+    if (injected()) return fail(SLORA_ERR_CUDA, "injected failure of a copy enqueue");
     CUDA_TRY(cudaMemcpyAsync(p->d_rank + a, p->rank_pin + a, sizeof(int32_t), cudaMemcpyHostToDevice,
                              p->copy));
     CUDA_TRY(cudaEventRecord(p->load_event[a], p->copy));
@@ -649,6 +712,7 @@ int slora_adapter_load(slora_pool* p, int32_t a, int32_t rank, const void* const
 }
 
 int slora_adapter_evict(slora_pool* p, int32_t a) {
+  SLORA_RANGE("slora_adapter_evict");
   if (int rc = check_pool(p)) return rc;
   if (a < 0 || a >= p->max_adapters || p->rank_h[a] == 0)
     return fail(SLORA_ERR_NOT_RESIDENT, "adapter %d is not resident", a);
@@ -668,6 +732,7 @@ int slora_adapter_evict(slora_pool* p, int32_t a) {
 }
 
 int slora_adapter_set_scale(slora_pool* p, int32_t a, float scale) {
+  SLORA_RANGE("slora_adapter_set_scale");
   if (int rc = check_device_pool(p)) return rc;
   if (a < 0 || a >= p->max_adapters || p->rank_h[a] == 0)
     return fail(SLORA_ERR_NOT_RESIDENT, "adapter %d is not resident", a);
@@ -679,6 +744,7 @@ int slora_adapter_set_scale(slora_pool* p, int32_t a, float scale) {
 }
 
 int slora_adapter_pages(const slora_pool* p, int32_t a, int32_t* out_pages, int64_t capacity, int64_t* n) {
+  SLORA_RANGE("slora_adapter_pages");
   if (int rc = check_pool(p)) return rc;
   if (a < 0 || a >= p->max_adapters || p->rank_h[a] == 0)
     return fail(SLORA_ERR_NOT_RESIDENT, "adapter %d is not resident", a);
@@ -692,6 +758,7 @@ int slora_adapter_pages(const slora_pool* p, int32_t a, int32_t* out_pages, int6
 }
 
 int slora_build_segments(slora_pool* p, const int32_t* d_ta, int32_t T, slora_segments* out) {
+  SLORA_RANGE("slora_build_segments");
   if (int rc = check_device_pool(p)) return rc;
   if (!out) return fail(SLORA_ERR_INVALID, "out is NULL");
   if (T < 0 || T > p->max_tokens) return fail(SLORA_ERR_INVALID, "T=%d not in [0, %d]", T, p->max_tokens);
@@ -727,6 +794,7 @@ int slora_build_segments(slora_pool* p, const int32_t* d_ta, int32_t T, slora_se
 int slora_lora_apply_multi(slora_pool* p, const slora_segments* seg, int32_t n, const int32_t* projs,
                            const void* const* d_x, const int64_t* ldx, void* const* d_y,
                            const int64_t* ldy, float s, int32_t mode) {
+  SLORA_RANGE("slora_lora_apply_multi");
   if (int rc = check_device_pool(p)) return rc;
   if (!seg || seg->generation != p->seg_generation || seg->generation == 0)
     return fail(SLORA_ERR_INVALID, "segments are missing or stale (rebuild them after every build call)");
@@ -752,6 +820,7 @@ int slora_lora_apply_multi(slora_pool* p, const slora_segments* seg, int32_t n, 
   d.scale = p->d_scale;
   d.off_n = std::min<int32_t>(kSegSmem, std::max(1, std::min(p->seg_T, p->max_adapters)) + 1);
   d.s = s;
+  d.wait_limit = p->wait_limit;
   for (int i = 0; i < n; ++i) {
     const int q = projs[i];
     if (q < 0 || q >= p->num_proj) return fail(SLORA_ERR_INVALID, "projection %d out of range", q);
@@ -774,7 +843,11 @@ int slora_lora_apply_multi(slora_pool* p, const slora_segments* seg, int32_t n, 
     P.v = p->d_v + (int64_t)i * std::max(p->max_tokens, 1) * v_ld(p);
   }
   if (p->seg_T == 0) return SLORA_OK;
-  const bool use_tc = p->tc_ok && mode != SLORA_MODE_DECODE;
+  // PREFILL: every segment on the tensor cores.  AUTO: the long segments of a
+  // large batch; a small batch (decode) has too few long segments to fill the
+  // tensor-core kernels, which are then bound by latency, not bandwidth.
+  const bool use_tc = p->tc_ok && (mode == SLORA_MODE_PREFILL ||
+                                   (mode == SLORA_MODE_AUTO && p->seg_T >= p->tc_min_batch));
   if (use_tc) {
     // short segments on the CUDA-core kernels, long ones on the tensor cores
     d.shrink_off = p->seg.cc_shrink_short;
@@ -845,6 +918,7 @@ int slora_lora_apply_multi(slora_pool* p, const slora_segments* seg, int32_t n, 
 
 int slora_lora_apply(slora_pool* p, const slora_segments* seg, int32_t proj, const void* d_x, int64_t ldx,
                      void* d_y, int64_t ldy, float s, int32_t mode) {
+  SLORA_RANGE("slora_lora_apply");
   const void* xs[1] = {d_x};
   void* ys[1] = {d_y};
   return slora_lora_apply_multi(p, seg, 1, &proj, xs, &ldx, ys, &ldy, s, mode);
@@ -852,6 +926,7 @@ int slora_lora_apply(slora_pool* p, const slora_segments* seg, int32_t proj, con
 
 int slora_lora_apply_bmm(slora_pool* p, const slora_segments* seg, int32_t proj, const void* d_x, int64_t ldx,
                          void* d_y, int64_t ldy, float s) {
+  SLORA_RANGE("slora_lora_apply_bmm");
   if (int rc = check_device_pool(p)) return rc;
   if (!seg || seg->generation != p->seg_generation || seg->generation == 0)
     return fail(SLORA_ERR_INVALID, "segments are missing or stale (rebuild them after every build call)");
@@ -933,6 +1008,7 @@ int slora_lora_apply_bmm(slora_pool* p, const slora_segments* seg, int32_t proj,
 }
 
 int slora_bmm_scratch_bytes(const slora_pool* p, size_t* bytes) {
+  SLORA_RANGE("slora_bmm_scratch_bytes");
   if (int rc = check_pool(p)) return rc;
   if (!bytes) return fail(SLORA_ERR_INVALID, "bytes is NULL");
   *bytes = p->bmm_bytes;
@@ -940,6 +1016,7 @@ int slora_bmm_scratch_bytes(const slora_pool* p, size_t* bytes) {
 }
 
 int slora_device_status(slora_pool* p, int32_t* status) {
+  SLORA_RANGE("slora_device_status");
   if (int rc = check_device_pool(p)) return rc;
   if (!status) return fail(SLORA_ERR_INVALID, "status is NULL");
   int32_t v = 0;
@@ -957,6 +1034,7 @@ int slora_device_status(slora_pool* p, int32_t* status) {
 }
 
 int slora_pool_snapshot(const slora_pool* p, void* buf, size_t* len) {
+  SLORA_RANGE("slora_pool_snapshot");
   if (int rc = check_pool(p)) return rc;
   if (!len) return fail(SLORA_ERR_INVALID, "len is NULL");
   const size_t need = 2 * sizeof(int64_t) + 2 * sizeof(int32_t) +
@@ -984,6 +1062,7 @@ int slora_pool_snapshot(const slora_pool* p, void* buf, size_t* len) {
 }
 
 int slora_timing_enable(slora_pool* p, int32_t enable) {
+  SLORA_RANGE("slora_timing_enable");
   if (int rc = check_device_pool(p)) return rc;
   p->timing = enable != 0;
   return SLORA_OK;
@@ -991,6 +1070,7 @@ int slora_timing_enable(slora_pool* p, int32_t enable) {
 
 int slora_timing_read(slora_pool* p, int32_t capacity, const char** names, double* ms, int64_t* launches,
                       int32_t* n) {
+  SLORA_RANGE("slora_timing_read");
   if (int rc = check_device_pool(p)) return rc;
   for (auto& r : p->recs) {
     CUDA_TRY(cudaEventSynchronize(r.b));
@@ -1017,9 +1097,35 @@ int slora_timing_read(slora_pool* p, int32_t capacity, const char** names, doubl
 }
 
 int slora_set_tc_threshold(slora_pool* p, int32_t min_tokens) {
+  SLORA_RANGE("slora_set_tc_threshold");
   if (int rc = check_pool(p)) return rc;
   if (min_tokens < 0) return fail(SLORA_ERR_INVALID, "threshold %d", min_tokens);
-  p->tc_threshold = min_tokens;
+  if (p->tc_ok || p->planning) p->tc_threshold = min_tokens;
+  return SLORA_OK;
+}
+
+int slora_debug_set_fault(slora_pool* p, int32_t kind, int64_t nth) {
+  SLORA_RANGE("slora_debug_set_fault");
+  if (int rc = check_pool(p)) return rc;
+  if (kind < SLORA_FAULT_NONE || kind > SLORA_FAULT_COPY || nth < 0)
+    return fail(SLORA_ERR_INVALID, "fault kind %d, count %lld", kind, (long long)nth);
+  for (int64_t& f : p->fault_left) f = 0;
+  if (kind != SLORA_FAULT_NONE) p->fault_left[kind] = nth;
+  return SLORA_OK;
+}
+
+int slora_debug_set_wait_limit(slora_pool* p, uint32_t polls) {
+  SLORA_RANGE("slora_debug_set_wait_limit");
+  if (int rc = check_pool(p)) return rc;
+  p->wait_limit = polls;
+  return SLORA_OK;
+}
+
+int slora_set_tc_min_batch(slora_pool* p, int32_t min_tokens) {
+  SLORA_RANGE("slora_set_tc_min_batch");
+  if (int rc = check_pool(p)) return rc;
+  if (min_tokens < 0) return fail(SLORA_ERR_INVALID, "minimum batch %d", min_tokens);
+  p->tc_min_batch = min_tokens;
   return SLORA_OK;
 }
 

@@ -37,8 +37,10 @@ EXPORTED = (
     "slora_build_segments", "slora_lora_apply", "slora_lora_apply_multi", "slora_device_status",
     "slora_pool_snapshot", "slora_timing_enable", "slora_timing_read", "slora_set_tc_threshold",
     "slora_last_error_string", "slora_lora_apply_noalloc", "slora_adapter_set_scale",
-    "slora_lora_apply_bmm", "slora_bmm_scratch_bytes",
+    "slora_lora_apply_bmm", "slora_bmm_scratch_bytes", "slora_set_tc_min_batch", "slora_debug_set_fault",
+    "slora_debug_set_wait_limit",
 )
+FAULT_NONE, FAULT_PAGE_ALLOC, FAULT_COPY = 0, 1, 2
 
 
 class SloraError(RuntimeError):
@@ -77,6 +79,9 @@ _SIGS = {
     "slora_timing_enable": [P, I32],
     "slora_timing_read": [P, I32, P, P, P, P],
     "slora_set_tc_threshold": [P, I32],
+    "slora_set_tc_min_batch": [P, I32],
+    "slora_debug_set_fault": [P, I32, I64],
+    "slora_debug_set_wait_limit": [P, ctypes.c_uint32],
     "slora_lora_apply_noalloc": [P, I32, I32, P, I64, P, I32, I32, P, P, I32, P, I32, P, I64, P, I64,
                                  ctypes.c_float, P, P],
 }
@@ -247,6 +252,18 @@ def slora_timing_read(pool: int) -> dict:
 
 def slora_set_tc_threshold(pool: int, min_tokens: int) -> None:
     _check(lib().slora_set_tc_threshold(pool, min_tokens), "slora_set_tc_threshold")
+
+
+def slora_set_tc_min_batch(pool: int, min_tokens: int) -> None:
+    _check(lib().slora_set_tc_min_batch(pool, min_tokens), "slora_set_tc_min_batch")
+
+
+def slora_debug_set_fault(pool: int, kind: int, nth: int) -> None:
+    _check(lib().slora_debug_set_fault(pool, kind, nth), "slora_debug_set_fault")
+
+
+def slora_debug_set_wait_limit(pool: int, polls: int) -> None:
+    _check(lib().slora_debug_set_wait_limit(pool, polls), "slora_debug_set_wait_limit")
 
 
 NOALLOC_MAX_TOKENS = 2048

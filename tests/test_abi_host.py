@@ -188,3 +188,60 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(slora, "LIB_PATH", str(tmp_path / "libslora.so"))
     with pytest.raises(ImportError):
         slora.slora_pool_create(0, 64, 256, slora.F16, 4, 16, 16, [256], [256])
+
+
+def _snapshot_bytes(S, h):
+    import ctypes
+
+    n = ctypes.c_size_t()
+    S.lib().slora_pool_snapshot(h, None, ctypes.byref(n))
+    buf = np.zeros(n.value, np.uint8)
+    assert S.lib().slora_pool_snapshot(h, buf.ctypes.data, ctypes.byref(n)) == S.OK
+    return buf
+
+
+def test_injected_page_allocation_failure_changes_nothing(S):
+    """SLORA_FAULT_PAGE_ALLOC: the nth page-taking call fails with OOM as if
+    the pool were full, the allocator state stays byte for byte as before, and
+    the fault fires once."""
+    h = S.slora_pool_create(0, 200, 64, S.F16, 8, 8, 16, [64, 128], [128, 64])
+    S.slora_adapter_load(h, 0, 4, None, None)
+    S.slora_debug_set_fault(h, S.FAULT_PAGE_ALLOC, 3)
+    S.slora_pages_alloc(h, 5)                                   # event 1
+    S.slora_adapter_load(h, 1, 2, None, None)                   # event 2
+    before = _snapshot_bytes(S, h)
+    with pytest.raises(S.SloraError) as e:                      # event 3: fails
+        S.slora_adapter_load(h, 2, 3, None, None)
+    assert e.value.code == S.ERR_OOM and "injected" in str(e.value)
+    assert np.array_equal(_snapshot_bytes(S, h), before)
+    S.slora_adapter_load(h, 2, 3, None, None)                   # disarmed: the same call succeeds
+    S.slora_debug_set_fault(h, S.FAULT_PAGE_ALLOC, 1)
+    before = _snapshot_bytes(S, h)
+    with pytest.raises(S.SloraError) as e:
+        S.slora_pages_alloc(h, 1)
+    assert e.value.code == S.ERR_OOM
+    assert np.array_equal(_snapshot_bytes(S, h), before)
+    S.slora_debug_set_fault(h, S.FAULT_PAGE_ALLOC, 1)
+    S.slora_debug_set_fault(h, S.FAULT_NONE, 0)                 # disarmed before it fires
+    S.slora_pages_alloc(h, 1)
+    for kind, nth in ((3, 1), (-1, 1), (S.FAULT_COPY, -2)):
+        with pytest.raises(S.SloraError) as e:
+            S.slora_debug_set_fault(h, kind, nth)
+        assert e.value.code == S.ERR_INVALID
+    S.slora_pool_destroy(h)
+
+
+def test_fault_armed_from_the_environment():
+    """SLORA_FAULT=alloc:2 arms the fault in every pool the process creates."""
+    import subprocess
+    import sys
+
+    code = ("from lora_adapters_gb300 import slora as S\n"
+            "h = S.slora_pool_create(0, 64, 64, S.F16, 4, 4, 4, [64], [64])\n"
+            "S.slora_pages_alloc(h, 1)\n"
+            "try:\n    S.slora_pages_alloc(h, 1)\nexcept S.SloraError as e:\n    print('code', e.code)\n")
+    env = dict(os.environ, SLORA_FAULT="alloc:2")
+    out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True,
+                         timeout=120)
+    assert out.returncode == 0, out.stderr
+    assert "code -2" in out.stdout

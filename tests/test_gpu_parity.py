@@ -112,10 +112,13 @@ def test_small_cases_all_modes(name):
         seg, want = _run_and_check(case, mode, want)
         _check_segments(case, seg)
     _run_and_check(case, slora.MODE_AUTO, want, multi=False)
-    # every segment on the tensor-core kernels, then a mixed split
+    # AUTO's split at any batch size: every segment on the tensor-core
+    # kernels, then short segments on the CUDA cores and long ones on the
+    # tensor cores
+    slora.slora_set_tc_min_batch(case.pool.handle, 0)
     for thr in (0, 3):
         slora.slora_set_tc_threshold(case.pool.handle, thr)
-        seg, _ = _run_and_check(case, slora.MODE_PREFILL, want)
+        seg, _ = _run_and_check(case, slora.MODE_AUTO, want)
         _check_segments(case, seg)
     case.pool.close()
 
@@ -317,6 +320,7 @@ def test_per_adapter_scale(name):
     for mode in MODES:
         _run_and_check(case, mode, want)
     slora.slora_set_tc_threshold(case.pool.handle, 0)
+    slora.slora_set_tc_min_batch(case.pool.handle, 0)
     _run_and_check(case, slora.MODE_AUTO, want)
     # evict + reload: the adapter's scale is 1 again (page placement does not
     # change the result)
@@ -346,3 +350,26 @@ def test_timing_hooks_count_launches():
     assert t["build_segments"][1] == 1 and t["apply_cc"][1] == 1
     assert all(ms >= 0 for ms, _ in t.values())
     case.pool.close()
+
+
+def test_auto_mode_split_follows_the_batch_size():
+    """AUTO runs a batch below tc_min_batch tokens wholly on the CUDA-core
+    kernel, and a batch at or above it with long segments on the tensor
+    cores; both give the oracle's answer."""
+    wl = workloads.make(SMALL["prefill_ragged_f16"])
+    case = G.build_case(wl)
+    pool = case.pool
+    slora.slora_set_tc_threshold(pool.handle, 16)
+    want = G.oracle_outputs(case)
+    for min_batch, tc in ((wl.T + 1, False), (wl.T, True)):
+        slora.slora_set_tc_min_batch(pool.handle, min_batch)
+        slora.slora_timing_enable(pool.handle, True)
+        slora.slora_timing_read(pool.handle)
+        _run_and_check(case, slora.MODE_AUTO, want)
+        t = slora.slora_timing_read(pool.handle)
+        slora.slora_timing_enable(pool.handle, False)
+        assert t["apply_cc"][1] == 1
+        assert (t["shrink_tc"][1] > 0) == tc and (t["expand_tc"][1] > 0) == tc, (min_batch, t)
+    with pytest.raises(slora.SloraError):
+        slora.slora_set_tc_min_batch(pool.handle, -1)
+    pool.close()
