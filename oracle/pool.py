@@ -96,8 +96,10 @@ class OraclePool:
         return pages
 
     def _give_back(self, pages: np.ndarray) -> None:
+        # the freed pages are not in the free list: their union, kept sorted,
+        # is the merge of two sorted runs (a stable sort finds and merges runs)
         self.owner[pages] = FREE
-        self._free = np.union1d(self._free, pages.astype(np.int64))
+        self._free = np.sort(np.concatenate([self._free, np.sort(pages.astype(np.int64))]), kind="stable")
 
     def kv_alloc(self, n: int) -> np.ndarray:
         if n < 0:
@@ -191,23 +193,27 @@ class OracleStore:
         self._n = 0
         self._data: Optional[np.ndarray] = None
 
-    def write_adapter(self, pool: OraclePool, a: int, weights) -> None:
+    def write_adapter(self, pool: OraclePool, a: int, weights, only=None) -> None:
+        """Place adapter a's rows on its pages.  ``only``: the projections to
+        write (all if None); the others' pages keep no contents, so a check
+        of one layer of a many-layer pool stores only that layer's rows."""
         r = int(pool.rank[a])
         H = self.H
-        table = pool.tables[a]
-        rows = []
+        table = pool.tables[a].astype(np.int64)
+        entry = 0
         for p, (A, B) in enumerate(weights):
             for M, dim in ((A, pool.proj[p].h_in), (B, pool.proj[p].h_out)):
-                assert M.shape == (r, dim), (M.shape, r, dim)
                 pp = _ceil_div(dim, H)
-                padded = np.zeros((r, pp * H), dtype=np.uint16)   # tail of the last page: zeros
-                padded[:, :dim] = M
-                rows.append(padded.reshape(r * pp, H))
-        chunks = np.concatenate(rows, axis=0)
-        assert chunks.shape[0] == table.shape[0]
-        self.page_slot[table.astype(np.int64)] = np.arange(self._n, self._n + chunks.shape[0])
-        self._chunks.append(chunks)
-        self._n += chunks.shape[0]
+                if only is None or p in only:
+                    assert M.shape == (r, dim), (M.shape, r, dim)
+                    padded = np.zeros((r, pp * H), dtype=np.uint16)   # tail of the last page: zeros
+                    padded[:, :dim] = M
+                    chunks = padded.reshape(r * pp, H)
+                    self.page_slot[table[entry:entry + r * pp]] = np.arange(self._n, self._n + r * pp)
+                    self._chunks.append(chunks)
+                    self._n += r * pp
+                entry += r * pp
+        assert entry == table.shape[0]
         self._data = None
 
     @property
