@@ -539,7 +539,7 @@ def measure(name, mode_name, args, rep, device, rank, world):
         if pipe and pipe[1] == src_hash:
             tensor["ncu_tensor_pipe_active"] = pipe[0]
         roofline["tensor"] = tensor
-    launches = int(round(sum(c for _, c in kern.values()) / hook_steps)) * args.steps
+    launches = int(round(sum(c for k, (_, c) in kern.items() if k != "load_wait") / hook_steps)) * args.steps
 
     # ---- end to end through the C ABI with host buffers.  Every step copies
     # its token ids, x and y in from pinned host memory and its y back out, as

@@ -69,7 +69,8 @@ extern "C" {
 #define SLORA_MODE_PREFILL 2 /* every segment on the tcgen05 kernels (CUDA-core kernels when the page size is not a multiple of 64) */
 
 /* Library limits (also checked at run time). */
-#define SLORA_MAX_PROJ 8           /* projections per pool */
+#define SLORA_MAX_PROJ 128         /* projections per pool (e.g. 32 layers x q, k, v, o) */
+#define SLORA_MAX_PROJ_PER_CALL 8  /* projections of one slora_lora_apply_multi call */
 #define SLORA_MAX_RANK 256         /* largest adapter rank */
 #define SLORA_MAX_ADAPTERS 32768   /* adapter ids 0 .. max_adapters-1 */
 
@@ -124,7 +125,7 @@ typedef struct slora_segments {
  *               equal; NULL = legacy default stream)
  * Allocates with cudaMalloc: the device page table (max_adapters * max_rank
  * * sum_q(ceil(in_q/H)+ceil(out_q/H)) int32), segment arrays, the fp32
- * shrink scratch (SLORA_MAX_PROJ * max_tokens * max_rank floats) and one
+ * shrink scratch (SLORA_MAX_PROJ_PER_CALL * max_tokens * max_rank floats) and one
  * adapter-sized staging buffer; pins an equally sized host page-table mirror.
  */
 int slora_pool_create(slora_pool** out, void* d_pool, int64_t num_pages, int32_t page_elems,
@@ -166,7 +167,9 @@ int slora_pool_info(const slora_pool* pool, int64_t* free_pages, int64_t* num_pa
  *   done    optional out: a cudaEvent_t (owned by the pool, valid until the
  *           adapter is evicted) that completes when the pages are written
  * The copies are queued on the copy stream after all work queued so far on
- * the compute stream (so pages freed earlier are no longer being read) and
+ * the compute stream (so pages freed earlier are no longer being read; weight
+ * blocks that follow each other in host memory in the order above move in one
+ * copy) and
  * the host buffers must stay untouched until `done` completes.  Later
  * slora_build_segments calls make the compute stream wait for pending loads.
  * Errors: SLORA_ERR_INVALID (id/rank out of range, NULL buffer),
@@ -180,7 +183,8 @@ int slora_adapter_load(slora_pool* pool, int32_t adapter_id, int32_t rank,
 /*
  * Evict a resident adapter: its pages return to the free list at once and
  * its device rank is cleared on the compute stream (work queued before the
- * evict still sees the adapter).  The pages' "race conditions in the adapter
+ * evict still sees the adapter; if the adapter's load is still copying, work
+ * queued on the compute stream after the evict waits for those copies).  The pages' "race conditions in the adapter
  * manager under dynamic loading" (cmlonder.com newsletter, section "Iddia ve
  * Gerceklik") are answered by stream order rather than by refusing the evict
  * with SLORA_ERR_BUSY: a later load into the freed pages is queued after all
@@ -202,6 +206,16 @@ int slora_adapter_evict(slora_pool* pool, int32_t adapter_id);
  */
 int slora_adapter_set_scale(slora_pool* pool, int32_t adapter_id, float scale);
 
+/*
+ * *ready = 1 once adapter `adapter_id`'s load has finished on the copy
+ * stream (always on a planning pool), 0 while its copies are still running;
+ * never blocks.  A scheduler that admits a request only when its adapter is
+ * ready keeps slora_build_segments from making the compute stream wait for
+ * copies (it waits for every load still running).  SLORA_ERR_NOT_RESIDENT if
+ * the adapter is not loaded.
+ */
+int slora_adapter_ready(slora_pool* pool, int32_t adapter_id, int32_t* ready);
+
 /* Host copy of an adapter's page table (page-table order above); *n = entries. */
 int slora_adapter_pages(const slora_pool* pool, int32_t adapter_id, int32_t* out_pages,
                         int64_t capacity, int64_t* n);
@@ -214,6 +228,17 @@ int slora_adapter_pages(const slora_pool* pool, int32_t adapter_id, int32_t* out
  */
 int slora_build_segments(slora_pool* pool, const int32_t* d_token_adapter, int32_t T,
                          slora_segments* out);
+
+/*
+ * The same, for a caller that also holds the batch's ids on the host (a
+ * scheduler builds them there): h_token_adapter, host int32[T], must list the
+ * same ids as d_token_adapter.  The compute stream then waits only for the
+ * pending loads of the adapters the batch names, not for every pending load
+ * -- a load started for a request that has not joined the batch yet does not
+ * hold this batch back.  h_token_adapter NULL: as slora_build_segments.
+ */
+int slora_build_segments_for(slora_pool* pool, const int32_t* d_token_adapter, int32_t T,
+                             const int32_t* h_token_adapter, slora_segments* out);
 
 /*
  * The heterogeneous-batch LoRA delta (dongaigc.com summary, section 2
@@ -231,7 +256,8 @@ int slora_build_segments(slora_pool* pool, const int32_t* d_token_adapter, int32
 int slora_lora_apply(slora_pool* pool, const slora_segments* seg, int32_t proj, const void* d_x,
                      int64_t ldx, void* d_y, int64_t ldy, float s, int32_t mode);
 
-/* The same for n projections of one layer in one set of launches. */
+/* The same for n <= SLORA_MAX_PROJ_PER_CALL projections (e.g. one layer's
+ * q, k, v, o) in one set of launches. */
 int slora_lora_apply_multi(slora_pool* pool, const slora_segments* seg, int32_t n,
                            const int32_t* projs, const void* const* d_x, const int64_t* ldx,
                            void* const* d_y, const int64_t* ldy, float s, int32_t mode);

@@ -8,7 +8,8 @@
 
 namespace slora {
 
-constexpr int kMaxProj = 8;            // == SLORA_MAX_PROJ
+constexpr int kMaxProj = 8;            // == SLORA_MAX_PROJ_PER_CALL: projections of one apply call
+constexpr int kMaxPoolProj = 128;      // == SLORA_MAX_PROJ: projections a pool's adapters carry
 constexpr int kMaxRank = 256;          // == SLORA_MAX_RANK
 constexpr int kMaxAdapters = 32768;    // == SLORA_MAX_ADAPTERS (segment kernel keeps a histogram in smem)
 
@@ -158,6 +159,15 @@ struct TcDev {
   int32_t tc_total_idx;
 };
 
+// Layout of one of a pool's projections, for the adapter-load kernel (a
+// device table written when the pool is created).
+struct ProjLayout {
+  int32_t h_in, h_out, ppi, ppo;
+  int32_t rows_before;           // page chunks per unit of rank in earlier projections
+  int32_t pad;
+  int64_t elems_before;          // elements per unit of rank in earlier projections (staging layout)
+};
+
 // Adapter load: staging -> pages.
 struct ScatterDev {
   const uint16_t* staging;       // packed: per projection, A rows then B rows
@@ -167,10 +177,7 @@ struct ScatterDev {
   int32_t n_entries;
   int32_t rank;
   int32_t nproj;
-  int32_t h_in[kMaxProj], h_out[kMaxProj];
-  int32_t ppi[kMaxProj], ppo[kMaxProj];
-  int64_t src_base[kMaxProj];    // element offset of projection q's A rows in staging
-  int32_t entry_base[kMaxProj];  // first page-table entry of projection q
+  const ProjLayout* proj;        // [nproj] (device)
 };
 
 // The padded batched-matmul comparator (bmm.cu): one projection.

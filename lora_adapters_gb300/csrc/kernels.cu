@@ -1526,25 +1526,33 @@ __global__ void set_f32_kernel(float* p, float v) { *p = v; }
 
 // ---- adapter load: staging -> pages ---------------------------------------------
 // One CTA per page-table entry: copies that row chunk (<= H elements) from the
-// packed staging copy to its page and zero-fills the rest of the page.
+// packed staging copy to its page and zero-fills the rest of the page.  The
+// entry's projection q is the last one whose entries start at or before it
+// (entries of q start at rank * rows_before[q]; a binary search over the
+// pool's projection table).
 __global__ void __launch_bounds__(128) scatter_kernel(const __grid_constant__ ScatterDev d) {
   for (int e = blockIdx.x; e < d.n_entries; e += gridDim.x) {
-    int q = 0;
-    while (q + 1 < d.nproj && e >= d.entry_base[q + 1]) ++q;
-    int local = e - d.entry_base[q];
-    const int na = d.rank * d.ppi[q];
+    int lo = 0, hi = d.nproj - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (d.rank * __ldg(&d.proj[mid].rows_before) <= e) lo = mid;
+      else hi = mid - 1;
+    }
+    const ProjLayout L = d.proj[lo];
+    int local = e - d.rank * L.rows_before;
+    const int64_t src_base = (int64_t)d.rank * L.elems_before;
+    const int na = d.rank * L.ppi;
     const uint16_t* src;
     int len;
     if (local < na) {
-      const int k = local / d.ppi[q], c = local - k * d.ppi[q];
-      src = d.staging + d.src_base[q] + (int64_t)k * d.h_in[q] + (int64_t)c * d.H;
-      len = min(d.H, d.h_in[q] - c * d.H);
+      const int k = local / L.ppi, c = local - k * L.ppi;
+      src = d.staging + src_base + (int64_t)k * L.h_in + (int64_t)c * d.H;
+      len = min(d.H, L.h_in - c * d.H);
     } else {
       local -= na;
-      const int k = local / d.ppo[q], c = local - k * d.ppo[q];
-      src = d.staging + d.src_base[q] + (int64_t)d.rank * d.h_in[q] + (int64_t)k * d.h_out[q] +
-            (int64_t)c * d.H;
-      len = min(d.H, d.h_out[q] - c * d.H);
+      const int k = local / L.ppo, c = local - k * L.ppo;
+      src = d.staging + src_base + (int64_t)d.rank * L.h_in + (int64_t)k * L.h_out + (int64_t)c * d.H;
+      len = min(d.H, L.h_out - c * d.H);
     }
     uint16_t* dst = d.pool + (int64_t)d.pages[e] * d.H;
     for (int v = threadIdx.x; v < d.H / 8; v += blockDim.x) {

@@ -106,7 +106,7 @@ extern "C" int slora_lora_apply_noalloc(const void* d_pool, int32_t page_elems, 
   if (dtype != SLORA_F16 && dtype != SLORA_BF16) return na_fail(SLORA_ERR_INVALID, "dtype");
   if (max_adapters <= 0 || max_adapters > kNaMaxAdapters)
     return na_fail(SLORA_ERR_INVALID, "max_adapters out of [1, SLORA_MAX_ADAPTERS]");
-  if (num_proj <= 0 || num_proj > kMaxProj || proj < 0 || proj >= num_proj)
+  if (num_proj <= 0 || num_proj > kMaxPoolProj || proj < 0 || proj >= num_proj)
     return na_fail(SLORA_ERR_INVALID, "projection index or count out of range");
   if (T < 0 || T > kNaMaxTokens)
     return na_fail(SLORA_ERR_INVALID, "T exceeds SLORA_NOALLOC_MAX_TOKENS (the static scratch holds 2048 tokens)");

@@ -70,8 +70,10 @@ constexpr int32_t kOwnerFree = -1;
 constexpr int32_t kOwnerKV = -2;
 constexpr int32_t kOwnerPending = -3;
 
-enum TimerKind { kTBuild = 0, kTApplyCC, kTShrinkTC, kTExpandTC, kTScatter, kTNum };
-const char* kTimerNames[kTNum] = {"build_segments", "apply_cc", "shrink_tc", "expand_tc", "scatter"};
+enum TimerKind { kTBuild = 0, kTApplyCC, kTShrinkTC, kTExpandTC, kTScatter, kTLoadWait, kTNum };
+// load_wait is not a kernel: the time the compute stream waited for adapter
+// copies before a segment build (recorded only when it had to wait)
+const char* kTimerNames[kTNum] = {"build_segments", "apply_cc", "shrink_tc", "expand_tc", "scatter", "load_wait"};
 
 }  // namespace
 
@@ -80,8 +82,9 @@ struct slora_pool {
   int64_t num_pages = 0;
   int32_t H = 0, dtype = 0, max_adapters = 0, max_rank = 0, max_tokens = 0, num_proj = 0;
   int32_t max_segs = 0;
-  int32_t proj_in[kMaxProj] = {}, proj_out[kMaxProj] = {};
-  int32_t ppi[kMaxProj] = {}, ppo[kMaxProj] = {}, rows_before[kMaxProj] = {};
+  int32_t proj_in[kMaxPoolProj] = {}, proj_out[kMaxPoolProj] = {};
+  int32_t ppi[kMaxPoolProj] = {}, ppo[kMaxPoolProj] = {}, rows_before[kMaxPoolProj] = {};
+  ProjLayout* d_layout = nullptr;        // the projections' layout for the load kernel
   int64_t chunks_per_rank = 0;   // page-table entries per unit of rank
   int64_t pt_stride = 0;         // entries reserved per adapter id
   int64_t staging_elems = 0;
@@ -291,8 +294,30 @@ struct Timed {
   }
 };
 
-// Make the compute stream wait for adapter loads that may still be running.
-int wait_pending_loads(slora_pool* p) {
+// Make the compute stream wait for adapter loads that may still be running:
+// every one of them, or (h_ids not NULL) only those of the adapters the T
+// host ids name.  *waits: the waits enqueued.
+int wait_pending_loads(slora_pool* p, const int32_t* h_ids, int32_t T, int* waits) {
+  *waits = 0;
+  if (h_ids) {
+    for (int32_t i = 0; i < T; ++i) {
+      const int32_t a = h_ids[i];
+      if (a < 0 || a >= p->max_adapters || !p->load_pending[a]) continue;
+      cudaError_t q = cudaEventQuery(p->load_event[a]);
+      if (q == cudaErrorNotReady) {
+        // still copying: the compute stream waits for it; the load stays
+        // pending (a reload of the id must still wait for its copies)
+        (void)cudaGetLastError();
+        CUDA_TRY(cudaStreamWaitEvent(p->compute, p->load_event[a], 0));
+        ++*waits;
+      } else if (q == cudaSuccess) {
+        p->load_pending[a] = 0;
+      } else {
+        return fail(SLORA_ERR_CUDA, "cudaEventQuery: %s", cudaGetErrorString(q));
+      }
+    }
+    return SLORA_OK;
+  }
   std::vector<int32_t> still;
   for (int32_t a : p->pending) {
     if (!p->load_pending[a]) continue;
@@ -304,6 +329,7 @@ int wait_pending_loads(slora_pool* p) {
     if (q != cudaErrorNotReady) return fail(SLORA_ERR_CUDA, "cudaEventQuery: %s", cudaGetErrorString(q));
     (void)cudaGetLastError();  // clear the sticky-free not-ready status
     CUDA_TRY(cudaStreamWaitEvent(p->compute, p->load_event[a], 0));
+    ++*waits;
     still.push_back(a);
   }
   p->pending.swap(still);
@@ -355,6 +381,7 @@ void free_device(slora_pool* p) {
   for (auto e : p->load_event)
     if (e) cudaEventDestroy(e);
   if (p->order_event) cudaEventDestroy(p->order_event);
+  cudaFree(p->d_layout);
   cudaFree(p->d_pt);
   cudaFree(p->d_rank);
   cudaFree(p->d_scale);
@@ -397,8 +424,8 @@ int slora_pool_create(slora_pool** out, void* d_pool, int64_t num_pages, int32_t
   if (max_rank <= 0 || max_rank > kMaxRank)
     return fail(SLORA_ERR_INVALID, "max_rank %d not in [1, %d]", max_rank, kMaxRank);
   if (max_tokens < 0 || max_tokens > (1 << 24)) return fail(SLORA_ERR_INVALID, "max_tokens %d", max_tokens);
-  if (num_proj <= 0 || num_proj > kMaxProj || !proj_in || !proj_out)
-    return fail(SLORA_ERR_INVALID, "num_proj %d not in [1, %d]", num_proj, kMaxProj);
+  if (num_proj <= 0 || num_proj > kMaxPoolProj || !proj_in || !proj_out)
+    return fail(SLORA_ERR_INVALID, "num_proj %d not in [1, %d]", num_proj, kMaxPoolProj);
   if (d_pool && (reinterpret_cast<uintptr_t>(d_pool) & 15))
     return fail(SLORA_ERR_INVALID, "d_pool must be 16-byte aligned");
 
@@ -494,6 +521,16 @@ int slora_pool_create(slora_pool** out, void* d_pool, int64_t num_pages, int32_t
     p->seg.tc_tile_long = q; q += S1;
     CUDA_TRY(cudaMalloc(&p->d_v, sizeof(float) * (size_t)kMaxProj * std::max(max_tokens, 1) * v_ld(p)));
     CUDA_TRY(cudaMalloc(&p->d_staging, sizeof(uint16_t) * (size_t)p->staging_elems));
+    {
+      std::vector<ProjLayout> lay((size_t)num_proj);
+      int64_t elems = 0;
+      for (int q = 0; q < num_proj; ++q) {
+        lay[q] = ProjLayout{p->proj_in[q], p->proj_out[q], p->ppi[q], p->ppo[q], p->rows_before[q], 0, elems};
+        elems += p->proj_in[q] + p->proj_out[q];
+      }
+      CUDA_TRY(cudaMalloc(&p->d_layout, sizeof(ProjLayout) * (size_t)num_proj));
+      CUDA_TRY(cudaMemcpy(p->d_layout, lay.data(), sizeof(ProjLayout) * (size_t)num_proj, cudaMemcpyHostToDevice));
+    }
     CUDA_TRY(cudaMalloc(&p->d_grid_sync, kGridSyncInts * sizeof(int32_t)));
     CUDA_TRY(cudaMemsetAsync(p->d_grid_sync, 0, kGridSyncInts * sizeof(int32_t), p->compute));
     CUDA_TRY(cudaMemsetAsync(p->d_pt, 0xff, sizeof(int32_t) * (size_t)pt_entries, p->compute));
@@ -673,22 +710,36 @@ int slora_adapter_load(slora_pool* p, int32_t a, int32_t rank, const void* const
     sd.n_entries = (int32_t)n;
     sd.rank = rank;
     sd.nproj = p->num_proj;
+    sd.proj = p->d_layout;
+    // The staging buffer takes projection by projection the A rows, then the
+    // B rows.  Host blocks that follow each other in host memory as they do
+    // in staging go in one copy: an adapter stored contiguously (per layer,
+    // or whole) moves in a few large copies instead of two per projection.
+    const char* run_src = nullptr;
+    size_t run_bytes = 0;
+    int64_t run_dst = 0;
+    auto flush = [&]() -> int {
+      if (run_bytes == 0) return SLORA_OK;
+      if (injected()) return fail(SLORA_ERR_CUDA, "injected failure of a copy enqueue");
+      CUDA_TRY(cudaMemcpyAsync(p->d_staging + run_dst, run_src, run_bytes, cudaMemcpyHostToDevice, p->copy));
+      run_bytes = 0;
+      return SLORA_OK;
+    };
     for (int q = 0; q < p->num_proj; ++q) {
-      const size_t bytesA = sizeof(uint16_t) * (size_t)rank * p->proj_in[q];
-      const size_t bytesB = sizeof(uint16_t) * (size_t)rank * p->proj_out[q];
-      sd.h_in[q] = p->proj_in[q];
-      sd.h_out[q] = p->proj_out[q];
-      sd.ppi[q] = p->ppi[q];
-      sd.ppo[q] = p->ppo[q];
-      sd.src_base[q] = off;
-      sd.entry_base[q] = (int32_t)((int64_t)rank * p->rows_before[q]);
-      if (injected()) return fail(SLORA_ERR_CUDA, "injected failure of a copy enqueue");
-      CUDA_TRY(cudaMemcpyAsync(p->d_staging + off, h_A[q], bytesA, cudaMemcpyHostToDevice, p->copy));
-      off += (int64_t)rank * p->proj_in[q];
-      if (injected()) return fail(SLORA_ERR_CUDA, "injected failure of a copy enqueue");
-      CUDA_TRY(cudaMemcpyAsync(p->d_staging + off, h_B[q], bytesB, cudaMemcpyHostToDevice, p->copy));
-      off += (int64_t)rank * p->proj_out[q];
+      for (int half = 0; half < 2; ++half) {
+        const char* src = static_cast<const char*>(half == 0 ? h_A[q] : h_B[q]);
+        const size_t bytes = sizeof(uint16_t) * (size_t)rank * (half == 0 ? p->proj_in[q] : p->proj_out[q]);
+        if (run_bytes > 0 && src != run_src + run_bytes)
+          if (int rc = flush()) return rc;
+        if (run_bytes == 0) {
+          run_src = src;
+          run_dst = off;
+        }
+        run_bytes += bytes;
+        off += (int64_t)(bytes / sizeof(uint16_t));
+      }
     }
+    if (int rc = flush()) return rc;
     {
       Timed tm(p, kTScatter, p->copy);
       if (injected()) return fail(SLORA_ERR_CUDA, "injected failure of a copy enqueue");
@@ -717,6 +768,9 @@ int slora_adapter_evict(slora_pool* p, int32_t a) {
   if (a < 0 || a >= p->max_adapters || p->rank_h[a] == 0)
     return fail(SLORA_ERR_NOT_RESIDENT, "adapter %d is not resident", a);
   if (!p->planning) {
+    // A load of this adapter still copying writes its pages: later work on
+    // the compute stream (which may reuse them) waits for it.
+    if (p->load_pending[a]) CUDA_TRY(cudaStreamWaitEvent(p->compute, p->load_event[a], 0));
     // Work queued before this call still sees the adapter; later work does not.
     CUDA_TRY(cudaMemsetAsync(p->d_rank + a, 0, sizeof(int32_t), p->compute));
   }
@@ -743,6 +797,27 @@ int slora_adapter_set_scale(slora_pool* p, int32_t a, float scale) {
   return SLORA_OK;
 }
 
+int slora_adapter_ready(slora_pool* p, int32_t a, int32_t* ready) {
+  SLORA_RANGE("slora_adapter_ready");
+  if (int rc = check_pool(p)) return rc;
+  if (!ready) return fail(SLORA_ERR_INVALID, "ready is NULL");
+  if (a < 0 || a >= p->max_adapters || p->rank_h[a] == 0)
+    return fail(SLORA_ERR_NOT_RESIDENT, "adapter %d is not resident", a);
+  *ready = 1;
+  if (!p->planning && p->load_pending[a]) {
+    const cudaError_t q = cudaEventQuery(p->load_event[a]);
+    if (q == cudaSuccess) {
+      p->load_pending[a] = 0;
+    } else if (q == cudaErrorNotReady) {
+      (void)cudaGetLastError();
+      *ready = 0;
+    } else {
+      return fail(SLORA_ERR_CUDA, "cudaEventQuery: %s", cudaGetErrorString(q));
+    }
+  }
+  return SLORA_OK;
+}
+
 int slora_adapter_pages(const slora_pool* p, int32_t a, int32_t* out_pages, int64_t capacity, int64_t* n) {
   SLORA_RANGE("slora_adapter_pages");
   if (int rc = check_pool(p)) return rc;
@@ -759,11 +834,32 @@ int slora_adapter_pages(const slora_pool* p, int32_t a, int32_t* out_pages, int6
 
 int slora_build_segments(slora_pool* p, const int32_t* d_ta, int32_t T, slora_segments* out) {
   SLORA_RANGE("slora_build_segments");
+  return slora_build_segments_for(p, d_ta, T, nullptr, out);
+}
+
+int slora_build_segments_for(slora_pool* p, const int32_t* d_ta, int32_t T, const int32_t* h_ta,
+                             slora_segments* out) {
+  SLORA_RANGE("slora_build_segments_for");
   if (int rc = check_device_pool(p)) return rc;
   if (!out) return fail(SLORA_ERR_INVALID, "out is NULL");
   if (T < 0 || T > p->max_tokens) return fail(SLORA_ERR_INVALID, "T=%d not in [0, %d]", T, p->max_tokens);
   if (T > 0 && !d_ta) return fail(SLORA_ERR_INVALID, "token_adapter is NULL");
-  if (int rc = wait_pending_loads(p)) return rc;
+  {
+    // the waits, timed when timing is on and a wait was enqueued
+    cudaEvent_t w0 = p->timing ? get_event(p) : nullptr;
+    if (w0) cudaEventRecord(w0, p->compute);
+    int waits = 0;
+    if (int rc = wait_pending_loads(p, h_ta, T, &waits)) return rc;
+    if (w0) {
+      cudaEvent_t w1 = waits ? get_event(p) : nullptr;
+      if (w1) {
+        cudaEventRecord(w1, p->compute);
+        p->recs.push_back({kTLoadWait, w0, w1});
+      } else {
+        p->spare_events.push_back(w0);
+      }
+    }
+  }
   SegBuildArgs args{};
   args.token_adapter = d_ta;
   args.T = T;

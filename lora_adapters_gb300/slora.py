@@ -38,7 +38,7 @@ EXPORTED = (
     "slora_pool_snapshot", "slora_timing_enable", "slora_timing_read", "slora_set_tc_threshold",
     "slora_last_error_string", "slora_lora_apply_noalloc", "slora_adapter_set_scale",
     "slora_lora_apply_bmm", "slora_bmm_scratch_bytes", "slora_set_tc_min_batch", "slora_debug_set_fault",
-    "slora_debug_set_wait_limit",
+    "slora_debug_set_wait_limit", "slora_adapter_ready", "slora_build_segments_for",
 )
 FAULT_NONE, FAULT_PAGE_ALLOC, FAULT_COPY = 0, 1, 2
 
@@ -68,8 +68,10 @@ _SIGS = {
     "slora_adapter_load": [P, I32, I32, P, P, ctypes.POINTER(P)],
     "slora_adapter_evict": [P, I32],
     "slora_adapter_set_scale": [P, I32, ctypes.c_float],
+    "slora_adapter_ready": [P, I32, P],
     "slora_adapter_pages": [P, I32, P, I64, P],
     "slora_build_segments": [P, P, I32, ctypes.POINTER(slora_segments)],
+    "slora_build_segments_for": [P, P, I32, P, ctypes.POINTER(slora_segments)],
     "slora_lora_apply": [P, ctypes.POINTER(slora_segments), I32, P, I64, P, I64, ctypes.c_float, I32],
     "slora_lora_apply_multi": [P, ctypes.POINTER(slora_segments), I32, P, P, P, P, P, ctypes.c_float, I32],
     "slora_lora_apply_bmm": [P, ctypes.POINTER(slora_segments), I32, P, I64, P, I64, ctypes.c_float],
@@ -169,6 +171,12 @@ def slora_adapter_evict(pool: int, adapter_id: int) -> None:
     _check(lib().slora_adapter_evict(pool, adapter_id), "slora_adapter_evict")
 
 
+def slora_adapter_ready(pool: int, adapter_id: int) -> bool:
+    r = I32()
+    _check(lib().slora_adapter_ready(pool, adapter_id, ctypes.byref(r)), "slora_adapter_ready")
+    return bool(r.value)
+
+
 def slora_adapter_set_scale(pool: int, adapter_id: int, scale: float) -> None:
     _check(lib().slora_adapter_set_scale(pool, adapter_id, float(scale)), "slora_adapter_set_scale")
 
@@ -186,6 +194,18 @@ def slora_build_segments(pool: int, d_token_adapter: int, T: int) -> slora_segme
     seg = slora_segments()
     _check(lib().slora_build_segments(pool, d_token_adapter or None, T, ctypes.byref(seg)),
            "slora_build_segments")
+    return seg
+
+
+def slora_build_segments_for(pool: int, d_token_adapter: int, T: int, h_token_adapter) -> slora_segments:
+    """h_token_adapter: host int32 array of the same ids (or None)."""
+    seg = slora_segments()
+    h = None
+    if h_token_adapter is not None:
+        h_token_adapter = np.ascontiguousarray(h_token_adapter, dtype=np.int32)
+        h = h_token_adapter.ctypes.data
+    _check(lib().slora_build_segments_for(pool, d_token_adapter or None, T, h, ctypes.byref(seg)),
+           "slora_build_segments_for")
     return seg
 
 

@@ -36,19 +36,23 @@ def test_failed_copy_enqueue_rolls_the_load_back():
     a = case.touched[0]
     r = int(wl.ranks[a])
     slora.slora_adapter_evict(pool.handle, a)
-    # a load enqueues 1 page-table copy, 2 copies per projection, the scatter
-    # kernel, the scale kernel and the rank copy: fail each in turn
-    n_events = 1 + 2 * len(wl.projections) + 3
-    for nth in range(1, n_events + 1):
+    # a load enqueues the page-table copy, one copy per contiguous run of
+    # host weight blocks, the scatter kernel, the scale kernel and the rank
+    # copy: fail each in turn until the load gets past all of them
+    failed = 0
+    for nth in range(1, 64):
         before = _snapshot_bytes(slora, pool.handle)
         slora.slora_debug_set_fault(pool.handle, slora.FAULT_COPY, nth)
-        with pytest.raises(slora.SloraError) as e:
+        try:
             pool.load(a, r, wl.adapter(a))
-        assert e.value.code == slora.ERR_CUDA and "injected" in str(e.value)
-        assert np.array_equal(_snapshot_bytes(slora, pool.handle), before), nth
-        pool.sync_loads()
-    slora.slora_debug_set_fault(pool.handle, slora.FAULT_COPY, n_events + 1)   # one past the load: no effect
-    pool.load(a, r, wl.adapter(a))
+        except slora.SloraError as e:
+            assert e.code == slora.ERR_CUDA and "injected" in str(e)
+            assert np.array_equal(_snapshot_bytes(slora, pool.handle), before), nth
+            pool.sync_loads()
+            failed += 1
+            continue
+        break                       # the fault lay past the load's last enqueue
+    assert failed >= 5
     slora.slora_debug_set_fault(pool.handle, slora.FAULT_NONE, 0)
     pool.sync_loads()
     _run_and_check(case, slora.MODE_DECODE, want)

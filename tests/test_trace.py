@@ -14,11 +14,20 @@ from oracle import pool as opool
 
 
 def small_spec(**kw):
-    base = dict(H=256, projections=workloads._qkvo(256), num_adapters=60, pool_bytes=256 * 2 * 3000,
-                token_budget=128, max_running=24, arrivals_per_step=1.5, prompt_len=(4, 60),
-                output_len=(4, 40), steps=300, max_loads_per_step=4)
+    # two layers of q, k, v, o; K and V of both layers per token
+    base = dict(H=256, layer_projections=workloads._qkvo(256), layers=2, kv_pages_per_token=4,
+                num_adapters=60, pool_bytes=256 * 2 * 6000, token_budget=128, max_running=24,
+                arrivals_per_step=1.5, prompt_len=(4, 60), output_len=(4, 40), steps=300, max_loads_per_step=4)
     base.update(kw)
     return dataclasses.replace(trace.TraceSpec(), **base)
+
+
+def test_spec_lists_every_layers_projections():
+    sp = small_spec(layers=3)
+    assert len(sp.projections) == 12
+    assert [p.name for p in sp.projections[4:8]] == ["L1.q", "L1.k", "L1.v", "L1.o"]
+    full = trace.TraceSpec()
+    assert len(full.projections) == 128 and full.kv_pages_per_token == 2 * full.layers
 
 
 def test_trace_pool_state_replays_on_the_oracle_allocator():
@@ -77,3 +86,21 @@ def test_trace_accounts_for_every_request_and_the_load_stall():
     assert s["adapter_hit_rate"] == 1.0 - res.arrival_misses / res.arrivals
     tr.close()
 
+
+
+def test_full_size_trace_replays_on_the_oracle_allocator():
+    """The full-size trace's bookkeeping (32 layers, 2000 adapters, 80 GB
+    pool, 9.8 M pages) for 600 steps: evictions happen, and the pool state
+    after them replays bit for bit on the oracle's allocator."""
+    sp = dataclasses.replace(trace.TraceSpec(), steps=600)
+    tr = trace.Trace(sp)
+    res = tr.run()
+    assert res.evictions > 0 and res.loads > res.evictions
+    op = opool.OraclePool(sp.pool_pages, sp.H, [(p.h_in, p.h_out) for p in sp.projections], sp.num_adapters,
+                          max(sp.rank_set))
+    op.replay(res.ops, res.ranks)
+    snap = slora.slora_pool_snapshot(tr.pool.handle)
+    assert snap["free_pages"] == op.free_count
+    assert np.array_equal(snap["owner"], op.owner)
+    assert np.array_equal(snap["rank"], op.rank)
+    tr.close()
