@@ -50,19 +50,23 @@ EXTRA = ("llama7b_decode", "llama7b_prefill")
 DEFAULT_MODE = {"llama13b_mlp_decode": "decode", "llama7b_decode": "decode", "llama7b_prefill": "prefill",
                 "tiny": "decode"}
 
-# ncu DRAM counters of the dominant kernel (dram__bytes_read.sum + write.sum,
-# per launch) on the benchmark workload, with the hash of the kernel source
-# they were taken from; reported as null once the source has changed.
+# ncu DRAM counters of the dominant kernel (dram__bytes_read.sum +
+# dram__bytes_write.sum, per launch) on each workload, with the hash of the
+# kernel source they were taken from; reported as null once the source has
+# changed.  The 13B MLP batch was captured in a compact pool holding only the
+# batch's adapters (--compact-pool: the same kernel work on the same rows).
 NCU_TRAFFIC = {
-    # apply_cc on the 7B decode batch: 277.71 MB read + 4.12 MB written
-    ("apply_cc", "llama7b_decode"): (281831424, "d4e7ece89ac53932"),
-    # tc_expand on the 7B prefill batch: 360.50 MB read + 221.82 MB written
-    ("expand_tc", "llama7b_prefill"): (582319360, "d4e7ece89ac53932"),
+    # apply_cc, 13B MLP decode: 793.70 MB read + 25.10 MB written (mean of 2 launches)
+    ("apply_cc", "llama13b_mlp_decode"): (818800768, "732740120efcd736"),
+    # apply_cc, 7B decode: 277.73 MB read + 1.08 MB written (mean of 2 launches)
+    ("apply_cc", "llama7b_decode"): (278809856, "732740120efcd736"),
+    # tc_expand, 7B prefill: 360.41 MB read + 218.00 MB written
+    ("expand_tc", "llama7b_prefill"): (578409728, "732740120efcd736"),
 }
-# ncu sm__pipe_tensor_cycles_active of the tensor-core expand kernel (% of
-# its active cycles) on the prefill batch, with the kernel-source hash.
+# ncu sm__pipe_tensor_cycles_active (% of active cycles) of the tensor-core
+# kernels on the prefill batch, with the kernel-source hash.
 NCU_TENSOR_PIPE = {
-    "llama7b_prefill": (9.2, "d4e7ece89ac53932"),
+    "llama7b_prefill": ({"expand_tc": 9.18, "shrink_tc": 19.44}, "732740120efcd736"),
 }
 
 
@@ -135,6 +139,24 @@ def algorithmic_flops(wl, tc_threshold=None):
         out["expand_" + path] += sum(2 * n * r * p.h_out for p in wl.projections)
     out["step"] = sum(out[k] for k in ("shrink_cc", "expand_cc", "shrink_tc", "expand_tc"))
     return out
+
+
+def compact_pool(wl):
+    """The same batch in a pool that holds only the adapters the batch uses
+    (pre-fragmented the same way: the pool filled with KV slots, a seeded half
+    released, then the adapters loaded), for profilers that save and restore
+    device memory: every kernel does the same work on the same rows as on the
+    full pool, whose other adapters and KV slots this batch never reads."""
+    import dataclasses
+
+    used = sorted(set(int(a) for a in wl.token_adapter if a >= 0))
+    per_rank = sum(-(-p.h_in // wl.H) + -(-p.h_out // wl.H) for p in wl.projections)
+    need = sum(int(wl.ranks[a]) * per_rank for a in used)
+    pages = 2 * need
+    free = np.sort(np.random.default_rng(np.random.SeedSequence(wl.spec.seed, spawn_key=(6,))).choice(
+        pages, size=need + need // 2, replace=False)).astype(np.int64)
+    ops = [("kv_alloc", "kv0", pages), ("kv_free", "kv0", free)] + [("load", a) for a in used]
+    return dataclasses.replace(wl, pool_pages=pages, pool_ops=ops)
 
 
 def setup_device(wl, device):
@@ -407,8 +429,12 @@ def measure(name, mode_name, args, rep, device, rank, world):
     from lora_adapters_gb300 import slora, workloads
 
     wl = workloads.make(name, seed=rank)      # each replica draws its own batch
+    if args.compact_pool:
+        wl = compact_pool(wl)
     sp = wl.spec
     cfg = workload_config(wl, mode_name, args.gpus)
+    if args.compact_pool:
+        cfg["pool"] = "compact: only the batch's adapters (profiling)"
     mode = {"auto": slora.MODE_AUTO, "decode": slora.MODE_DECODE, "prefill": slora.MODE_PREFILL}[mode_name]
 
     pool, ta, xs, ys, y0 = setup_device(wl, device)
@@ -537,7 +563,7 @@ def measure(name, mode_name, args, rep, device, rank, world):
                 per_kernel[k]["tflops"] = fl[k] / (per_kernel[k]["us_per_step"] * 1e-6) / 1e12
         pipe = NCU_TENSOR_PIPE.get(sp.name)
         if pipe and pipe[1] == src_hash:
-            tensor["ncu_tensor_pipe_active"] = pipe[0]
+            tensor["ncu_tensor_pipe_active_pct"] = pipe[0]
         roofline["tensor"] = tensor
     launches = int(round(sum(c for k, (_, c) in kern.items() if k != "load_wait") / hook_steps)) * args.steps
 
@@ -650,6 +676,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=24)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time per thread count (headline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--compact-pool", action="store_true",
+                    help="profiling: a pool holding only the batch's adapters (same kernel work, small footprint)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
