@@ -56,17 +56,17 @@ DEFAULT_MODE = {"llama13b_mlp_decode": "decode", "llama7b_decode": "decode", "ll
 # changed.  The 13B MLP batch was captured in a compact pool holding only the
 # batch's adapters (--compact-pool: the same kernel work on the same rows).
 NCU_TRAFFIC = {
-    # apply_cc, 13B MLP decode: 793.70 MB read + 25.10 MB written (mean of 2 launches)
-    ("apply_cc", "llama13b_mlp_decode"): (818800768, "732740120efcd736"),
-    # apply_cc, 7B decode: 277.73 MB read + 1.08 MB written (mean of 2 launches)
-    ("apply_cc", "llama7b_decode"): (278809856, "732740120efcd736"),
-    # tc_expand, 7B prefill: 360.41 MB read + 218.00 MB written
-    ("expand_tc", "llama7b_prefill"): (578409728, "732740120efcd736"),
+    # apply_cc, 13B MLP decode: 793.67 MB read + 25.23 MB written (mean of 2 launches)
+    ("apply_cc", "llama13b_mlp_decode"): (818904064, "2eddbd4ca0e59a27"),
+    # apply_cc, 7B decode: 277.73 MB read + 1.09 MB written (mean of 2 launches)
+    ("apply_cc", "llama7b_decode"): (278820352, "2eddbd4ca0e59a27"),
+    # tc_expand, 7B prefill: 360.38 MB read + 217.95 MB written (mean of 2 launches)
+    ("expand_tc", "llama7b_prefill"): (578338432, "2eddbd4ca0e59a27"),
 }
 # ncu sm__pipe_tensor_cycles_active (% of active cycles) of the tensor-core
 # kernels on the prefill batch, with the kernel-source hash.
 NCU_TENSOR_PIPE = {
-    "llama7b_prefill": ({"expand_tc": 9.18, "shrink_tc": 19.44}, "732740120efcd736"),
+    "llama7b_prefill": ({"expand_tc": 9.19, "shrink_tc": 18.72}, "2eddbd4ca0e59a27"),
 }
 
 
@@ -569,16 +569,21 @@ def measure(name, mode_name, args, rep, device, rank, world):
 
     # ---- end to end through the C ABI with host buffers.  Every step copies
     # its token ids, x and y in from pinned host memory and its y back out, as
-    # a serving loop would: inputs of step k+1 go in on one copy stream and the
-    # result of step k-1 comes out on another while step k computes (two sets
-    # of device buffers).  No L2 flush here: x and y arrive from the host
-    # every step and the adapter rows a step reads exceed L2 on the decode
-    # batches.
+    # a serving loop would: inputs of later steps go in on one copy stream and
+    # results of earlier steps come out on another while a step computes.
+    # With small copies (decode batches) three sets of device buffers let a
+    # step's inputs go in without waiting for the result of the step two
+    # before it; with large ones (the prefill batch: 840 MB per step) two sets
+    # measured faster, since more copies in flight at once share the link.
+    # No L2 flush here: x and y arrive from the host every step and the
+    # adapter rows a step reads exceed L2 on the decode batches.
     pin_x = [x.cpu().pin_memory() for x in xs]
     pin_y = [y.cpu().pin_memory() for y in y0]
     pin_ta = ta.cpu().pin_memory()
+    copy_bytes = sum(t.numel() * t.element_size() for t in pin_x + pin_y + ys)
+    n_sets = 3 if copy_bytes <= (256 << 20) else 2
     sets = [(ta, xs, ys)] + [(torch.empty_like(ta), [torch.empty_like(x) for x in xs],
-                              [torch.empty_like(y) for y in ys])]
+                              [torch.empty_like(y) for y in ys]) for _ in range(n_sets - 1)]
     out_y = [[torch.empty_like(y, device="cpu").pin_memory() for y in ys] for _ in sets]
     h2d = sum(t.numel() * t.element_size() for t in pin_x + pin_y) + pin_ta.numel() * 4
     d2h = sum(t.numel() * t.element_size() for t in out_y[0])
@@ -593,7 +598,7 @@ def measure(name, mode_name, args, rep, device, rank, world):
     def e2e_step(k):
         b = k % len(sets)
         d_ta, d_xs, d_ys = sets[b]
-        s_in.wait_event(ev_out[b])          # step k-2's result has left this set
+        s_in.wait_event(ev_out[b])          # the result of the set's previous step has left it
         with torch.cuda.stream(s_in):
             d_ta.copy_(pin_ta, non_blocking=True)
             for d, h in zip(d_xs, pin_x):
@@ -627,18 +632,20 @@ def measure(name, mode_name, args, rep, device, rank, world):
     t_end.record(stream)
     t_end.synchronize()
     e_ms = t_start.elapsed_time(t_end) / args.steps
-    # both buffer sets computed the same batch from the same inputs: their
+    # every buffer set computed the same batch from the same inputs: their
     # results must agree bit for bit (a copy racing a kernel would show here)
     if args.steps >= len(sets):
-        for a_, b_ in zip(out_y[0], out_y[1]):
-            if not torch.equal(a_, b_):
-                raise RuntimeError("pipelined end-to-end steps disagree")
+        for other in out_y[1:]:
+            for a_, b_ in zip(out_y[0], other):
+                if not torch.equal(a_, b_):
+                    raise RuntimeError("pipelined end-to-end steps disagree")
     rep.barrier()
     e_ms = rep.max(e_ms)
     link = _link_gbs(torch, device, h2d, d2h)
     e2e = {"value": rep.rate(wl.T, e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
            "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms,
-           "pipelining": "inputs of step k+1 in and step k-1's y out while step k computes", "l2": "not flushed",
+           "pipelining": f"{n_sets} buffer sets: later steps' inputs in and earlier steps' y out while a step "
+                         "computes", "l2": "not flushed",
            "link": dict(link, note="one plain pinned copy of the step's input bytes (h2d) and of its output "
                                    "bytes (d2h), each alone: the end-to-end step cannot beat the larger "
                                    "of the two"),

@@ -28,7 +28,7 @@ constexpr int kSegThreads = 1024;
 // of 16-bit elements).
 constexpr int kTcM = 128;
 constexpr int kTcK = 64;
-constexpr int kTcShrinkParts = 2;        // K parts of one tc_shrink (tile, projection)
+constexpr int kTcShrinkParts = 3;        // K parts of one tc_shrink (tile, projection)
 
 // Indices into SegDev::counts.
 enum CountIdx {
