@@ -18,7 +18,7 @@ constexpr int kMaxAdapters = 32768;    // == SLORA_MAX_ADAPTERS (segment kernel 
 constexpr int kTT = 4;                 // tokens per tile
 constexpr int kShrinkRows = 8;         // rank rows per shrink work unit (one per consumer warp)
 constexpr int kCcConsumerWarps = 8;
-constexpr int kCcThreads = (kCcConsumerWarps + 1) * 32;
+constexpr int kCcThreads = (kCcConsumerWarps + 2) * 32;   // + the planner and the issuer warp
 constexpr int kExpandCols = kCcConsumerWarps * 32 * 8;  // 8 output columns (16 bytes) per thread
 constexpr int kSegSmem = 1536;         // work-list prefix entries searched in shared memory
 constexpr int kSegThreads = 1024;

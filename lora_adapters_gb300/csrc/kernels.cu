@@ -819,11 +819,14 @@ __global__ void __launch_bounds__(kSmallSegMax) build_segments_small_kernel(cons
 
 // ---- the CUDA-core apply kernel: shrink, grid barrier, expand (one launch) --------
 // Persistent CTA per SM (grid = number of SMs, all CTAs resident at once):
-// warp 8 is the producer, warps 0-7 consume.  Every CTA first runs its shrink
-// units, then its expand units; both kinds stream through the same 4-deep ring
-// of 48 KB shared-memory stages.  The producer fills a stage with 1-D bulk
-// copies (TMA engine) of whole row chunks, one per lane, and lane 0 announces
-// the stage's bytes on its mbarrier after writing the stage's metadata.
+// warps 0-7 consume; warp 8 plans the stages and warp 9 issues their copies.
+// Every CTA first runs its shrink units, then its expand units; both kinds
+// stream through the same 4-deep ring of 48 KB shared-memory stages.  The
+// planner claims a free stage, writes its metadata, announces its bytes on the
+// stage's mbarrier and lists its copies (one per lane: a whole row chunk,
+// source and place in the stage); the issuer turns the list into 1-D bulk
+// copies (TMA engine).  Issuing a stage's bulk copies holds a warp for about
+// as long as planning the next stage does, so the two run side by side.
 //
 // Shrink unit = (segment position q, token tile of <= kTT tokens, chunk of 8
 // rank rows, projection); projection varies fastest.  Per K chunk of <=
@@ -836,7 +839,7 @@ __global__ void __launch_bounds__(kSmallSegMax) build_segments_small_kernel(cons
 // replaces the 512 conversions and multiply-adds the CUDA cores would issue
 // for those 16 K values, which is what bounds this phase: the HBM bytes of a
 // stage arrive in about 1,500 cycles.  At the unit's end the warps' partial
-// sums meet in shared memory and v is written (fp32).
+// sums meet in shared memory and one warp writes v (fp32).
 //
 // Between the phases the CTAs meet once (a grid barrier on two counters in
 // global memory): the expand phase reads v rows that any CTA may have written.
@@ -849,7 +852,9 @@ __global__ void __launch_bounds__(kSmallSegMax) build_segments_small_kernel(cons
 // fastest.  Stages carry kExpandRK B rows each, and the unit's last stage also
 // carries the tile's y rows.  Each consumer thread owns 8 adjacent columns:
 // fp32 accumulation over the unit's rank rows for every token of the tile,
-// then y + s * acc, one rounding, a 16-byte store.
+// then y + s * acc, one rounding, a 16-byte store.  (Warp-level MMAs were
+// measured here too: with 4 of 8 token slots used and the legacy MMA path's
+// rate on this GPU they took twice as long per stage as the FMAs.)
 //
 // The producer resolves units 32 at a time (one per lane), so page-table and
 // segment lookups of a whole batch of units cost one round of loads, and it
@@ -869,6 +874,13 @@ static_assert(kTT * kExpandCols <= kStageElems - kRowsOff, "y rows of a stage mu
 static_assert(32 % kExpandRK == 0, "a stage's B rows come from one 32-row block of page indices");
 
 enum : int { kKindShrink = 0, kKindExpand = 1 };
+// A stage's copy list: at most kCpMax copies; entry = source address and
+// (byte offset in the stage << 13 | bytes), 0 = no copy for that lane.
+constexpr int kCpMax = 12;
+static_assert(kShrinkRows + kTT <= kCpMax && kExpandRK + kTT <= kCpMax, "a stage's copies must fit its list");
+static_assert(kStageElems * 2 < (1 << 19) && kShrinkK * 2 < (1 << 13) && kExpandCols * 2 < (1 << 13),
+              "stage offsets and copy sizes must fit the packed copy entry");
+__device__ __forceinline__ uint32_t cp_entry(uint32_t off_bytes, uint32_t bytes) { return off_bytes << 13 | bytes; }
 struct __align__(16) StageMeta {
   int kind, ntok, p, len, last;
   int j0, k0, nrows;                // shrink
@@ -883,14 +895,19 @@ struct ApplySmem {
   uint16_t st[kStages][kStageElems];
   float V[kStages][kTT][kMaxRank];
   // Shrink: the consumer warps' partial sums of a unit (8 rank rows x 4
-  // tokens each), summed by warp 0.  Unit u uses buffer u % kRedBufs: a warp
-  // can run at most kStages stages (so kStages units) ahead of warp 0, so
-  // warp 0 has read a buffer before any warp writes it again.
+  // tokens each), summed by one warp (unit u: warp u % 8, so that the extra
+  // work goes round).  Unit u uses buffer u % kRedBufs: a warp can run at
+  // most kStages stages (so kStages units) ahead of any other, so the summing
+  // warp has read a buffer before any warp writes it again.
   float red[kStages + 1][kCcConsumerWarps][32];
   uint64_t redbar[kStages + 1];
   StageMeta meta[kStages];
   VPending pend[kStages];
   uint64_t full[kStages], empty[kStages], vfull[kStages];
+  uint64_t issue[kStages];                 // the planner has listed the stage's copies (32 arrivals)
+  const void* cp_src[kStages][kCpMax];
+  uint32_t cp_desc[kStages][kCpMax];
+  int32_t cp_stop[kStages];                // 1: no more stages (the issuer leaves)
   int32_t off_s[kSegSmem], off_e[kSegSmem];
   int32_t gen0;
 };
@@ -1041,6 +1058,7 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], kCcConsumerWarps);
       mbar_init(&sm.vfull[s], 1);
+      mbar_init(&sm.issue[s], 32);
     }
     for (int s = 0; s < kRedBufs; ++s) mbar_init(&sm.redbar[s], kCcConsumerWarps);
     mbar_fence_init();
@@ -1081,17 +1099,27 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
   // the waits for its own copies in flight before it exits keep kWaitLimit.
   const uint32_t lim = d.wait_limit ? d.wait_limit : kWaitLimit;
 
-  if (warp == kCcConsumerWarps) {  // ============================ producer warp
+  // slots (bit s) with copies issued, and the parity of that phase: what a
+  // warp that gives up must wait for before the CTA exits
+  auto mark = [](uint32_t& set, uint32_t& par, int s2, uint32_t ph) {
+    set |= 1u << s2;
+    par = (par & ~(1u << s2)) | (ph << s2);
+  };
+  if (warp == kCcConsumerWarps) {  // ============================= planner warp
     uint32_t stage = 0, phase = 0, nitem = 0;
     bool ok = true;
     bool opened = false;  // the grid barrier has opened (v rows may be read)
     int npend = 0;        // expand units whose v rows wait for it
-    // slots (bit s) with copies issued, and the parity of that phase: what a
-    // CTA that gives up must wait for before it exits
-    uint32_t issued = 0, ipar = 0, vissued = 0, vpar = 0;
-    auto mark = [](uint32_t& set, uint32_t& par, int s2, uint32_t ph) {
-      set |= 1u << s2;
-      par = (par & ~(1u << s2)) | (ph << s2);
+    uint32_t vissued = 0, vpar = 0;   // v-row copies issued here
+    // The stage's copy list, one entry per lane (src NULL: none), handed to
+    // the issuer warp; every lane arrives on the stage's issue barrier.
+    auto post = [&](const void* src, uint32_t off_bytes, uint32_t bytes) {
+      if (lane < kCpMax) {
+        sm.cp_src[stage][lane] = src;
+        sm.cp_desc[stage][lane] = src ? cp_entry(off_bytes, bytes) : 0u;
+      }
+      if (lane == 0) sm.cp_stop[stage] = 0;
+      mbar_arrive(&sm.issue[stage]);
     };
     const int gen0 = sm.gen0;
     // v rows of the units held back, once the barrier has opened
@@ -1215,16 +1243,12 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
               m.sa = sa;
               mbar_expect_tx(&sm.full[stage], (uint32_t)(nrows + ntok) * (uint32_t)len * 2u);
             }
-            __syncwarp();
-            uint16_t* dst = sm.st[stage];
             // A row i and token row t at rows i and kShrinkRows + t of the stage
-            if (lane < nrows)
-              bulk_load(dst + lane * kShrinkPitch, d.pool + (int64_t)my * d.H + o, (uint32_t)len * 2u,
-                        &sm.full[stage]);
+            const uint16_t* src = nullptr;
+            if (lane < nrows) src = d.pool + (int64_t)my * d.H + o;
             else if (lane >= kShrinkRows && lane < kShrinkRows + ntok)
-              bulk_load(dst + lane * kShrinkPitch, xbase + (int64_t)my * P.ldx + (int64_t)c * d.H + o,
-                        (uint32_t)len * 2u, &sm.full[stage]);
-            mark(issued, ipar, stage, phase);
+              src = xbase + (int64_t)my * P.ldx + (int64_t)c * d.H + o;
+            post(src, (uint32_t)(lane * kShrinkPitch) * 2u, (uint32_t)len * 2u);
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1;
@@ -1322,16 +1346,16 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
             if (last) bytes += (uint32_t)ntok * (uint32_t)len * 2u;
             mbar_expect_tx(&sm.full[stage], bytes);
           }
-          __syncwarp();
-          uint16_t* dst = sm.st[stage];
-          if (lane < nk)
-            bulk_load(dst + lane * kExpandCols, d.pool + (int64_t)page_i * d.H + o, (uint32_t)len * 2u,
-                      &sm.full[stage]);
-          else if (last && lane >= kExpandRK && lane < kExpandRK + ntok)
-            bulk_load(dst + kRowsOff + (lane - kExpandRK) * kExpandCols,
-                      static_cast<const uint16_t*>(P.y) + (int64_t)pick(rows, lane - kExpandRK) * P.ldy + col0,
-                      (uint32_t)len * 2u, &sm.full[stage]);
-          mark(issued, ipar, stage, phase);
+          const uint16_t* src = nullptr;
+          uint32_t off = 0;
+          if (lane < nk) {
+            src = d.pool + (int64_t)page_i * d.H + o;
+            off = (uint32_t)(lane * kExpandCols) * 2u;
+          } else if (last && lane >= kExpandRK && lane < kExpandRK + ntok) {
+            src = static_cast<const uint16_t*>(P.y) + (int64_t)pick(rows, lane - kExpandRK) * P.ldy + col0;
+            off = (uint32_t)(kRowsOff + (lane - kExpandRK) * kExpandCols) * 2u;
+          }
+          post(src, off, (uint32_t)len * 2u);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
@@ -1349,17 +1373,53 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
       if (open) release_pending();
       else ok = false;
     }
-    // No copy may still be landing when the CTA exits: wait (with the
-    // built-in limit) for the last phase issued on each barrier.  On the
-    // normal path the consumers have already waited for every stage and v
-    // buffer and these waits return at once; they matter when the consumers
-    // gave up, which they can do while the producer never had to.
-    if (lane == 0) {
-      for (int s2 = 0; s2 < kStages; ++s2) {
-        if (issued >> s2 & 1u) (void)mbar_wait(&sm.full[s2], ipar >> s2 & 1u);
-        if (vissued >> s2 & 1u) (void)mbar_wait(&sm.vfull[s2], vpar >> s2 & 1u);
+    // Tell the issuer that no stage follows: one more free slot, marked as
+    // the end (a planner that gave up sends nothing; the issuer's own wait
+    // then runs out).
+    if (ok) {
+      if (acquire()) {
+        if (lane == 0) sm.cp_stop[stage] = 1;
+        mbar_arrive(&sm.issue[stage]);
+      } else {
+        ok = false;
       }
     }
+    // No copy may still be landing when the CTA exits: wait (with the
+    // built-in limit) for the last phase issued on each v buffer.  On the
+    // normal path the consumers have already waited for every v buffer and
+    // these waits return at once; they matter when the consumers gave up,
+    // which they can do while the planner never had to.
+    if (lane == 0)
+      for (int s2 = 0; s2 < kStages; ++s2)
+        if (vissued >> s2 & 1u) (void)mbar_wait(&sm.vfull[s2], vpar >> s2 & 1u);
+    if (!ok && lane == 0) report(d.error, kErrTimeout);
+  } else if (warp == kCcConsumerWarps + 1) {  // ===================== issuer warp
+    // Stages in ring order: wait until the planner has listed the copies,
+    // then issue them (one bulk copy per lane) onto the stage's barrier.
+    uint32_t stage = 0, phase = 0, issued = 0, ipar = 0;
+    bool ok = true;
+    for (;;) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&sm.issue[stage], phase, lim))) {
+        ok = false;
+        break;
+      }
+      if (sm.cp_stop[stage]) break;
+      if (lane < kCpMax) {
+        const uint32_t e = sm.cp_desc[stage][lane];
+        if (e)
+          bulk_load(reinterpret_cast<unsigned char*>(&sm.st[stage][0]) + (e >> 13), sm.cp_src[stage][lane],
+                    e & 0x1fffu, &sm.full[stage]);
+      }
+      mark(issued, ipar, stage, phase);
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1;
+      }
+    }
+    // No copy issued here may still be landing when the CTA exits.
+    if (lane == 0)
+      for (int s2 = 0; s2 < kStages; ++s2)
+        if (issued >> s2 & 1u) (void)mbar_wait(&sm.full[s2], ipar >> s2 & 1u);
     if (!ok && lane == 0) report(d.error, kErrTimeout);
   } else {  // ====================================================== consumer warps
     uint32_t stage = 0, phase = 0;
@@ -1378,6 +1438,7 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
       uint32_t rb = 0, rph = 0;   // partial-sum buffer of this unit and its phase
       for (int64_t i = 0; i < ns && ok; ++i) {
         float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+        float acc2[4] = {0.f, 0.f, 0.f, 0.f}, acc3[4] = {0.f, 0.f, 0.f, 0.f};
         while (true) {
           if (!mbar_wait(&sm.full[stage], phase, lim)) {
             ok = false;
@@ -1390,14 +1451,18 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
           const uint32_t sbase = smem_addr(&sm.st[stage][0]);
           const int nk16 = len >> 4;
           int ks = warp;
-          for (; ks + kCcConsumerWarps < nk16; ks += 2 * kCcConsumerWarps) {   // two chains in flight
-            uint32_t r0[4], r1[4];
+          for (; ks + 3 * kCcConsumerWarps < nk16; ks += 4 * kCcConsumerWarps) {   // four chains in flight
+            uint32_t r0[4], r1[4], r2[4], r3[4];
             ldsm_x4(r0, sbase + lofs + (uint32_t)ks * 32u);
             ldsm_x4(r1, sbase + lofs + (uint32_t)(ks + kCcConsumerWarps) * 32u);
+            ldsm_x4(r2, sbase + lofs + (uint32_t)(ks + 2 * kCcConsumerWarps) * 32u);
+            ldsm_x4(r3, sbase + lofs + (uint32_t)(ks + 3 * kCcConsumerWarps) * 32u);
             mma_k16<D::kBf16>(acc0, r0[0], r0[1], r0[2], r0[3]);
             mma_k16<D::kBf16>(acc1, r1[0], r1[1], r1[2], r1[3]);
+            mma_k16<D::kBf16>(acc2, r2[0], r2[1], r2[2], r2[3]);
+            mma_k16<D::kBf16>(acc3, r3[0], r3[1], r3[2], r3[3]);
           }
-          if (ks < nk16) {
+          for (; ks < nk16; ks += kCcConsumerWarps) {
             uint32_t r0[4];
             ldsm_x4(r0, sbase + lofs + (uint32_t)ks * 32u);
             mma_k16<D::kBf16>(acc0, r0[0], r0[1], r0[2], r0[3]);
@@ -1417,12 +1482,12 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
             // lane (g, c) holds rank row g = lane / 4, tokens 2c and 2c + 1
             float* red = &sm.red[rb][0][0];
             if ((lane & 3) < 2) {
-              red[warp * 32 + (lane >> 2) * kTT + 2 * (lane & 3)] = acc0[0] + acc1[0];
-              red[warp * 32 + (lane >> 2) * kTT + 2 * (lane & 3) + 1] = acc0[1] + acc1[1];
+              red[warp * 32 + (lane >> 2) * kTT + 2 * (lane & 3)] = (acc0[0] + acc1[0]) + (acc2[0] + acc3[0]);
+              red[warp * 32 + (lane >> 2) * kTT + 2 * (lane & 3) + 1] = (acc0[1] + acc1[1]) + (acc2[1] + acc3[1]);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.redbar[rb]);
-            if (warp == 0) {   // the eight partial sums, in warp order
+            if (warp == (int)(i % kCcConsumerWarps)) {   // the eight partial sums, in warp order
               bool got = true;
               if (lane == 0) got = mbar_wait(&sm.redbar[rb], rph, lim);
               if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
