@@ -864,12 +864,13 @@ constexpr int kShrinkK = 2048;                         // K chunk (elements) of 
 // Shrink rows are kShrinkPitch elements apart: 16 bytes past the chunk, so
 // the 8 rows one ldmatrix phase reads sit in 8 different 16-byte bank groups.
 constexpr int kShrinkPitch = kShrinkK + 8;
-constexpr int kExpandRK = 8;                           // B rows per expand stage
+constexpr int kExpandRK = 8;                           // B rows per expand stage (a multiple of 4)
 constexpr int kStageElems = (kShrinkRows + kTT) * kShrinkPitch;   // 48.2 KB of 16-bit elements
 constexpr int kRowsOff = kShrinkRows * kShrinkK;       // y rows of an expand stage start here
 static_assert((kShrinkPitch * 2) % 16 == 0 && (kStageElems * 2) % 16 == 0, "bulk copies need 16-byte rows");
 constexpr int kPagesPerLane = kMaxRank / 32;           // B-row page indices one lane prefetches
 static_assert(kExpandRK * kExpandCols <= kRowsOff, "B rows of a stage must fit before the x/y rows");
+static_assert(kExpandRK % 4 == 0, "a full expand stage reads v four ranks at a time");
 static_assert(kTT * kExpandCols <= kStageElems - kRowsOff, "y rows of a stage must fit");
 static_assert(32 % kExpandRK == 0, "a stage's B rows come from one 32-row block of page indices");
 
@@ -1030,10 +1031,37 @@ __device__ __forceinline__ void load_b_pages(const ApplyDev& d, int a, int r, in
 }
 
 // Expand stage compute of the consumer threads, specialised on the tile's
-// token count so that no issue slot goes to absent tokens.
+// token count so that no issue slot goes to absent tokens.  A full stage
+// (kExpandRK rows) loads its 8 B-row pieces and the tokens' 8 v values first
+// and then runs the multiply-adds, so that shared-memory latency is paid once
+// per stage rather than once per row.
 template <class D, int NT>
 __device__ __forceinline__ void expand_stage(const uint16_t* brows, const float (*V)[kMaxRank], int k0, int nk,
                                              int col, float2 (&acc)[kTT][4]) {
+  if (nk == kExpandRK) {
+    uint4 b[kExpandRK];
+#pragma unroll
+    for (int k = 0; k < kExpandRK; ++k) b[k] = *reinterpret_cast<const uint4*>(brows + k * kExpandCols + col);
+    float4 v[NT][kExpandRK / 4];
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int q = 0; q < kExpandRK / 4; ++q) v[t][q] = *reinterpret_cast<const float4*>(&V[t][k0 + 4 * q]);
+#pragma unroll
+    for (int k = 0; k < kExpandRK; ++k) {
+      float2 fb[4];
+      unpack4x2<D>(b[k], fb);
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const float4 vq = v[t][k >> 2];
+        const float vv = (k & 3) == 0 ? vq.x : (k & 3) == 1 ? vq.y : (k & 3) == 2 ? vq.z : vq.w;
+        const float2 v2 = make_float2(vv, vv);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[t][e] = ffma2(v2, fb[e], acc[t][e]);
+      }
+    }
+    return;
+  }
 #pragma unroll 2
   for (int k = 0; k < nk; ++k) {
     float2 fb[4];
