@@ -173,7 +173,7 @@ __device__ __forceinline__ int find_pos(const int32_t* s_off, const int32_t* g_o
   return lo;
 }
 
-// Selects a[i] for a warp-uniform runtime index i without local memory.
+// Selects a[i] for a runtime index i without local memory.
 template <int N>
 __device__ __forceinline__ int pick(const int (&a)[N], int i) {
   int v = a[0];
@@ -849,8 +849,8 @@ __global__ void __launch_bounds__(kSmallSegMax) build_segments_small_kernel(cons
 //
 // Expand unit = (segment position q, token tile, projection, column tile of
 // <= kExpandCols columns inside one page); projection and column tile vary
-// fastest.  Stages carry kExpandRK B rows each, and the unit's last stage also
-// carries the tile's y rows.  Each consumer thread owns 8 adjacent columns:
+// fastest.  Stages carry kExpandRKBig B rows each (a whole stage), and the
+// unit's last stage at most kExpandRK B rows together with the tile's y rows.  Each consumer thread owns 8 adjacent columns:
 // fp32 accumulation over the unit's rank rows for every token of the tile,
 // then y + s * acc, one rounding, a 16-byte store.  (Warp-level MMAs were
 // measured here too: with 4 of 8 token slots used and the legacy MMA path's
@@ -864,20 +864,25 @@ constexpr int kShrinkK = 2048;                         // K chunk (elements) of 
 // Shrink rows are kShrinkPitch elements apart: 16 bytes past the chunk, so
 // the 8 rows one ldmatrix phase reads sit in 8 different 16-byte bank groups.
 constexpr int kShrinkPitch = kShrinkK + 8;
-constexpr int kExpandRK = 8;                           // B rows per expand stage (a multiple of 4)
+constexpr int kExpandRK = 8;                           // B rows of a unit's last expand stage (which also carries y)
+constexpr int kExpandRKBig = 12;                       // B rows of its other stages (a whole 48 KB stage)
 constexpr int kStageElems = (kShrinkRows + kTT) * kShrinkPitch;   // 48.2 KB of 16-bit elements
 constexpr int kRowsOff = kShrinkRows * kShrinkK;       // y rows of an expand stage start here
 static_assert((kShrinkPitch * 2) % 16 == 0 && (kStageElems * 2) % 16 == 0, "bulk copies need 16-byte rows");
 constexpr int kPagesPerLane = kMaxRank / 32;           // B-row page indices one lane prefetches
 static_assert(kExpandRK * kExpandCols <= kRowsOff, "B rows of a stage must fit before the x/y rows");
 static_assert(kExpandRK % 4 == 0, "a full expand stage reads v four ranks at a time");
+static_assert(kExpandRK <= kExpandRKBig, "the last stage takes at most as many rows as the others");
 static_assert(kTT * kExpandCols <= kStageElems - kRowsOff, "y rows of a stage must fit");
-static_assert(32 % kExpandRK == 0, "a stage's B rows come from one 32-row block of page indices");
+static_assert(kExpandRKBig * kExpandCols <= kStageElems, "a stage of B rows must fit");
+static_assert(kExpandRKBig <= 32, "a stage's B rows come from distinct lanes");
+static_assert(kExpandRKBig % 4 == 0, "a full expand stage reads v four ranks at a time");
 
 enum : int { kKindShrink = 0, kKindExpand = 1 };
 // A stage's copy list: at most kCpMax copies; entry = source address and
 // (byte offset in the stage << 13 | bytes), 0 = no copy for that lane.
 constexpr int kCpMax = 12;
+static_assert(kExpandRKBig <= kCpMax, "a stage's B rows must fit its copy list");
 static_assert(kShrinkRows + kTT <= kCpMax && kExpandRK + kTT <= kCpMax, "a stage's copies must fit its list");
 static_assert(kStageElems * 2 < (1 << 19) && kShrinkK * 2 < (1 << 13) && kExpandCols * 2 < (1 << 13),
               "stage offsets and copy sizes must fit the packed copy entry");
@@ -1030,36 +1035,43 @@ __device__ __forceinline__ void load_b_pages(const ApplyDev& d, int a, int r, in
   }
 }
 
+// Expand compute of NK B rows (a multiple of 4): the rows' pieces and the
+// tokens' NK v values are loaded first, then the multiply-adds run, so that
+// shared-memory latency is paid once per group rather than once per row.
+template <class D, int NT, int NK>
+__device__ __forceinline__ void expand_rows(const uint16_t* brows, const float (*V)[kMaxRank], int k0, int col,
+                                            float2 (&acc)[kTT][4]) {
+  uint4 b[NK];
+#pragma unroll
+  for (int k = 0; k < NK; ++k) b[k] = *reinterpret_cast<const uint4*>(brows + k * kExpandCols + col);
+  float4 v[NT][NK / 4];
+#pragma unroll
+  for (int t = 0; t < NT; ++t)
+#pragma unroll
+    for (int q = 0; q < NK / 4; ++q) v[t][q] = *reinterpret_cast<const float4*>(&V[t][k0 + 4 * q]);
+#pragma unroll
+  for (int k = 0; k < NK; ++k) {
+    float2 fb[4];
+    unpack4x2<D>(b[k], fb);
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const float4 vq = v[t][k >> 2];
+      const float vv = (k & 3) == 0 ? vq.x : (k & 3) == 1 ? vq.y : (k & 3) == 2 ? vq.z : vq.w;
+      const float2 v2 = make_float2(vv, vv);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[t][e] = ffma2(v2, fb[e], acc[t][e]);
+    }
+  }
+}
 // Expand stage compute of the consumer threads, specialised on the tile's
-// token count so that no issue slot goes to absent tokens.  A full stage
-// (kExpandRK rows) loads its 8 B-row pieces and the tokens' 8 v values first
-// and then runs the multiply-adds, so that shared-memory latency is paid once
-// per stage rather than once per row.
+// token count so that no issue slot goes to absent tokens; whole stages
+// (kExpandRKBig or kExpandRK rows) in groups of 8 and 4 rows.
 template <class D, int NT>
 __device__ __forceinline__ void expand_stage(const uint16_t* brows, const float (*V)[kMaxRank], int k0, int nk,
                                              int col, float2 (&acc)[kTT][4]) {
-  if (nk == kExpandRK) {
-    uint4 b[kExpandRK];
-#pragma unroll
-    for (int k = 0; k < kExpandRK; ++k) b[k] = *reinterpret_cast<const uint4*>(brows + k * kExpandCols + col);
-    float4 v[NT][kExpandRK / 4];
-#pragma unroll
-    for (int t = 0; t < NT; ++t)
-#pragma unroll
-      for (int q = 0; q < kExpandRK / 4; ++q) v[t][q] = *reinterpret_cast<const float4*>(&V[t][k0 + 4 * q]);
-#pragma unroll
-    for (int k = 0; k < kExpandRK; ++k) {
-      float2 fb[4];
-      unpack4x2<D>(b[k], fb);
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const float4 vq = v[t][k >> 2];
-        const float vv = (k & 3) == 0 ? vq.x : (k & 3) == 1 ? vq.y : (k & 3) == 2 ? vq.z : vq.w;
-        const float2 v2 = make_float2(vv, vv);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[t][e] = ffma2(v2, fb[e], acc[t][e]);
-      }
-    }
+  if (nk == kExpandRKBig || nk == kExpandRK) {   // k0 is a multiple of 4 (the planner's split)
+    expand_rows<D, NT, 8>(brows, V, k0, col, acc);
+    if (nk == kExpandRKBig) expand_rows<D, NT, kExpandRKBig - 8>(brows + 8 * kExpandCols, V, k0 + 8, col, acc);
     return;
   }
 #pragma unroll 2
@@ -1333,8 +1345,12 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
         const int col0 = c * d.H + o;
         const int buf = (int)(nitem % kStages);
         const int vph = (int)((nitem / kStages) & 1);
-        for (int k0 = 0; k0 < r; k0 += kExpandRK) {
-          const int nk = min(kExpandRK, r - k0);
+        // the unit's rows: stages of at most kExpandRKBig rows (a multiple of
+        // 4, so that every stage starts at a multiple of 4 and its v values
+        // load as float4), then a last stage of at most kExpandRK rows
+        // together with the tile's y rows
+        for (int k0 = 0, nk = 0; k0 < r; k0 += nk) {
+          nk = r - k0 <= kExpandRK ? r - k0 : min(kExpandRKBig, (r - k0 - 1) & ~3);
           const bool first = k0 == 0;
           const int last = k0 + nk >= r;
           if (!acquire()) {
@@ -1354,8 +1370,10 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
               ++npend;
             }
           }
-          // B row k0 + i's page: held by lane (k0 % 32) + i, slot k0 / 32
-          const int page_i = __shfl_sync(0xffffffffu, pick(pg, k0 >> 5), (k0 & 31) + (lane % kExpandRK));
+          // B row k0 + i's page is held by lane (k0 + i) % 32, slot (k0 + i) / 32:
+          // each lane offers the row of the window k0 .. k0 + 31 it holds
+          const int offer = pick(pg, (k0 + ((lane - k0) & 31)) >> 5);
+          const int page_i = __shfl_sync(0xffffffffu, offer, (k0 + lane) & 31);
           if (lane == 0) {
             StageMeta& m = sm.meta[stage];
             m.kind = kKindExpand;
