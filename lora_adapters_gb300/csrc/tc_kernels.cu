@@ -469,6 +469,8 @@ constexpr int kTcNe = 128;                        // expand column tile
 constexpr int kEAtoms = kTcNe / 64;               // 64-column swizzle atoms per tile
 constexpr int kEKBlocks = kMaxRank / kTcK;        // B row blocks of 64 ranks
 constexpr int kEBufs = 3;                         // y tiles and TMEM accumulators in flight
+// warps: 0 y tiles and B rows, 1 MMAs, 2-5 epilogue, 6 v halves
+constexpr int kExpandTcThreads = kTcThreads + 32;
 constexpr int kETmemCols = 512;                   // power of two >= kEBufs * kTcNe
 static_assert(kEBufs * kTcNe <= kETmemCols, "accumulators must fit the TMEM allocation");
 struct TcExpandSmem {
@@ -513,7 +515,7 @@ __device__ __forceinline__ TcEUnit tc_eunit(const TcDev& t, int64_t g, int per_s
 }
 
 template <class E>
-__global__ void __launch_bounds__(kTcThreads, 1) tc_expand_kernel(const __grid_constant__ TcDev t) {
+__global__ void __launch_bounds__(kExpandTcThreads, 1) tc_expand_kernel(const __grid_constant__ TcDev t) {
   extern __shared__ uint8_t smem_raw[];
   TcExpandSmem& sm = *reinterpret_cast<TcExpandSmem*>(smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023));
   const ApplyDev& d = t.a;
@@ -554,7 +556,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expand_kernel(const __grid_c
   };
 
   if (warp == 0) {  // ------------------------------------------ producer
-    uint32_t bu0 = 0, bu1 = 0, nv = 0, ny = 0;  // B uses per half, v stages, y tiles issued
+    uint32_t bu0 = 0, bu1 = 0, ny = 0;  // B uses per half, y tiles issued
     int bsel = 0;
     for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x) {
       const TcEUnit u = tc_eunit(t, g, per_seg);
@@ -627,7 +629,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expand_kernel(const __grid_c
                         tok[3], &sm.y_full[yb]);
           }
         }
-        // v halves, one 64-rank block per stage
+      }
+    }
+  } else if (warp == 6) {  // ------------------------------------ v halves
+    // In the MMA warp's order: per unit, per token tile, per 64-rank block,
+    // the tile's v hi and lo halves into one of the two v stages.  Apart from
+    // the producer, so that they do not queue behind the y and B copies.
+    uint32_t nv = 0;
+    for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x) {
+      const TcEUnit u = tc_eunit(t, g, per_seg);
+      if (u.ntm == 0) continue;
+      const int nkb = (((u.r + 15) & ~15) + kTcK - 1) / kTcK;
+      for (int mt = 0; mt < u.ntm && ok; ++mt) {
+        const int j0 = u.start + mt * kTcM;
         for (int kb = 0; kb < nkb; ++kb) {
           const int vb = nv & 1;
           if (!wait_lane0(&sm.v_empty[vb], ((nv >> 1) & 1) ^ 1)) { ok = false; break; }
@@ -845,8 +859,8 @@ cudaError_t launch_tc_shrink(const TcDev& a, int dtype, int grid, cudaStream_t s
 }
 
 cudaError_t launch_tc_expand(const TcDev& a, int dtype, int grid, cudaStream_t st) {
-  if (dtype == 0) return launch_pdl_tc(tc_expand_kernel<__half>, grid, kTcThreads, kExpandTcSmem, st, a);
-  return launch_pdl_tc(tc_expand_kernel<__nv_bfloat16>, grid, kTcThreads, kExpandTcSmem, st, a);
+  if (dtype == 0) return launch_pdl_tc(tc_expand_kernel<__half>, grid, kExpandTcThreads, kExpandTcSmem, st, a);
+  return launch_pdl_tc(tc_expand_kernel<__nv_bfloat16>, grid, kExpandTcThreads, kExpandTcSmem, st, a);
 }
 
 int32_t tc_col_tiles(int32_t h_out, int32_t H) {
