@@ -484,33 +484,52 @@ struct TcExpandSmem {
 };
 
 // Unit g of the expand list: segment position q (any segment; those with no
-// tensor-core tile do nothing), projection and column tile.
+// tensor-core tile do nothing), projection and column tile
+// (tc_eunit_raw / tc_eunit_done below).
 struct TcEUnit {
   int p, start, len, r, a, c, o, ncols, ntm;  // ntm = 128-token tiles (0: skip)
 };
-__device__ __forceinline__ TcEUnit tc_eunit(const TcDev& t, int64_t g, int per_seg) {
+// The loads of unit g's descriptor, kept apart from the arithmetic on them
+// (tc_eunit_done), so that a warp can have the next unit's loads in flight
+// while it works on this one.  g >= G: no unit (ntm 0), nothing loaded.
+struct TcERaw {
+  int p, c, o, ncols;
+  int off0, off1;
+  int4 sd;
+};
+__device__ __forceinline__ TcERaw tc_eunit_raw(const TcDev& t, int64_t g, int per_seg, int64_t G) {
   const ApplyDev& d = t.a;
-  TcEUnit u;
+  TcERaw w{};
+  if (g >= G) return w;
   const int q = (int)(g / per_seg);
   int nt = (int)(g - (int64_t)q * per_seg);
-  u.p = 0;
-  while (nt >= t.tc_ncol[u.p]) nt -= t.tc_ncol[u.p++];
-  u.ntm = __ldg(t.tc_off + q + 1) - __ldg(t.tc_off + q);
-  const int4 sd = __ldg(d.seg_desc + q);   // adapter, rank, start, end
-  u.start = sd.z;
-  u.len = sd.w - sd.z;
-  u.r = sd.y;
-  u.a = sd.x;
-  for (u.c = 0;; ++u.c) {  // column tile within one page chunk
-    const int lenc = min(d.H, d.proj[u.p].h_out - u.c * d.H);
+  while (nt >= t.tc_ncol[w.p]) nt -= t.tc_ncol[w.p++];
+  for (w.c = 0;; ++w.c) {  // column tile within one page chunk
+    const int lenc = min(d.H, d.proj[w.p].h_out - w.c * d.H);
     const int n = (lenc + kTcNe - 1) / kTcNe;
     if (nt < n) {
-      u.o = nt * kTcNe;
-      u.ncols = min(kTcNe, lenc - u.o);
+      w.o = nt * kTcNe;
+      w.ncols = min(kTcNe, lenc - w.o);
       break;
     }
     nt -= n;
   }
+  w.off0 = __ldg(t.tc_off + q);
+  w.off1 = __ldg(t.tc_off + q + 1);
+  w.sd = __ldg(d.seg_desc + q);   // adapter, rank, start, end
+  return w;
+}
+__device__ __forceinline__ TcEUnit tc_eunit_done(const TcERaw& w) {
+  TcEUnit u;
+  u.p = w.p;
+  u.c = w.c;
+  u.o = w.o;
+  u.ncols = w.ncols;
+  u.ntm = w.off1 - w.off0;
+  u.start = w.sd.z;
+  u.len = w.sd.w - w.sd.z;
+  u.r = w.sd.y;
+  u.a = w.sd.x;
   return u;
 }
 
@@ -558,8 +577,10 @@ __global__ void __launch_bounds__(kExpandTcThreads, 1) tc_expand_kernel(const __
   if (warp == 0) {  // ------------------------------------------ producer
     uint32_t bu0 = 0, bu1 = 0, ny = 0;  // B uses per half, y tiles issued
     int bsel = 0;
+    TcERaw rw = tc_eunit_raw(t, blockIdx.x, per_seg, G);   // one unit ahead
     for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x) {
-      const TcEUnit u = tc_eunit(t, g, per_seg);
+      const TcEUnit u = tc_eunit_done(rw);
+      rw = tc_eunit_raw(t, g + gridDim.x, per_seg, G);
       if (u.ntm == 0) continue;
       const ProjDev& P = d.proj[u.p];
       const int r16 = (u.r + 15) & ~15;
@@ -636,8 +657,10 @@ __global__ void __launch_bounds__(kExpandTcThreads, 1) tc_expand_kernel(const __
     // the tile's v hi and lo halves into one of the two v stages.  Apart from
     // the producer, so that they do not queue behind the y and B copies.
     uint32_t nv = 0;
+    TcERaw rw = tc_eunit_raw(t, blockIdx.x, per_seg, G);   // one unit ahead
     for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x) {
-      const TcEUnit u = tc_eunit(t, g, per_seg);
+      const TcEUnit u = tc_eunit_done(rw);
+      rw = tc_eunit_raw(t, g + gridDim.x, per_seg, G);
       if (u.ntm == 0) continue;
       const int nkb = (((u.r + 15) & ~15) + kTcK - 1) / kTcK;
       for (int mt = 0; mt < u.ntm && ok; ++mt) {
@@ -656,15 +679,18 @@ __global__ void __launch_bounds__(kExpandTcThreads, 1) tc_expand_kernel(const __
       }
     }
   } else if (warp == 1) {  // ----------------------------------- MMA issuer
+    // The next unit's descriptor loads are in flight while this unit's MMAs
+    // are issued (this warp is on the path from the copies to the epilogue).
     uint32_t bu0 = 0, bu1 = 0, nv = 0, nt = 0;
     int bsel = 0;
+    TcERaw rw = tc_eunit_raw(t, blockIdx.x, per_seg, G);
     for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x) {
-      TcEUnit u;
-      if (lane == 0) u = tc_eunit(t, g, per_seg);
-      const int ntm = __shfl_sync(0xffffffffu, lane == 0 ? u.ntm : 0, 0);
+      const TcEUnit u = tc_eunit_done(rw);
+      rw = tc_eunit_raw(t, g + gridDim.x, per_seg, G);
+      const int ntm = u.ntm;
       if (ntm == 0) continue;
-      const int r = __shfl_sync(0xffffffffu, lane == 0 ? u.r : 0, 0);
-      const int ncols = __shfl_sync(0xffffffffu, lane == 0 ? u.ncols : 0, 0);
+      const int r = u.r;
+      const int ncols = u.ncols;
       const int r16 = (r + 15) & ~15;
       const int nkb = (r16 + kTcK - 1) / kTcK;
       const uint32_t idesc = umma_idesc_f16(kTcM, (ncols + 15) & ~15, bf16, true);
@@ -725,8 +751,10 @@ __global__ void __launch_bounds__(kExpandTcThreads, 1) tc_expand_kernel(const __
     const int quarter = warp & 3;
     const int m = 32 * quarter + lane;
     uint32_t nt = 0;
+    TcERaw rw = tc_eunit_raw(t, blockIdx.x, per_seg, G);   // one unit ahead
     for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x) {
-      const TcEUnit u = tc_eunit(t, g, per_seg);
+      const TcEUnit u = tc_eunit_done(rw);
+      rw = tc_eunit_raw(t, g + gridDim.x, per_seg, G);
       if (u.ntm == 0) continue;
       const ProjDev& P = d.proj[u.p];
       const int col0 = u.c * d.H + u.o;
