@@ -65,11 +65,26 @@ template <>
 struct Elem<__half> {
   static __device__ __forceinline__ uint16_t from(float f) { return __half_as_ushort(__float2half_rn(f)); }
   static __device__ __forceinline__ float to(uint16_t u) { return __half2float(__ushort_as_half(u)); }
+  // a pair packed in 32 bits (first value in the low half)
+  static __device__ __forceinline__ uint32_t from2(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+  static __device__ __forceinline__ float2 to2(uint32_t u) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&u));
+  }
 };
 template <>
 struct Elem<__nv_bfloat16> {
   static __device__ __forceinline__ uint16_t from(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
   static __device__ __forceinline__ float to(uint16_t u) { return __bfloat162float(__ushort_as_bfloat16(u)); }
+  static __device__ __forceinline__ uint32_t from2(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+  static __device__ __forceinline__ float2 to2(uint32_t u) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+  }
 };
 
 // ================================================================ tc_shrink
@@ -795,14 +810,16 @@ __global__ void __launch_bounds__(kExpandTcThreads, 1) tc_expand_kernel(const __
               if (h < nch) {
                 uint8_t* py = ytile + ((h ^ (m & 7)) << 4);   // swizzled 16-byte chunk
                 uint4 yv = *reinterpret_cast<const uint4*>(py);
-                uint16_t e[8];
-                memcpy(e, &yv, 16);
+                uint32_t w[4];
+                memcpy(w, &yv, 16);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  const uint32_t bits = h < 4 ? r0[8 * h + i] : r1[8 * (h - 4) + i];
-                  e[i] = Elem<E>::from(Elem<E>::to(e[i]) + d.s * __uint_as_float(bits));
+                for (int i = 0; i < 4; ++i) {   // pairs of columns: one unpack, two FMAs, one packing rounding
+                  const uint32_t b0 = h < 4 ? r0[8 * h + 2 * i] : r1[8 * (h - 4) + 2 * i];
+                  const uint32_t b1 = h < 4 ? r0[8 * h + 2 * i + 1] : r1[8 * (h - 4) + 2 * i + 1];
+                  const float2 yy = Elem<E>::to2(w[i]);
+                  w[i] = Elem<E>::from2(yy.x + d.s * __uint_as_float(b0), yy.y + d.s * __uint_as_float(b1));
                 }
-                memcpy(&yv, e, 16);
+                memcpy(&yv, w, 16);
                 if (tma_out) *reinterpret_cast<uint4*>(py) = yv;
                 else *reinterpret_cast<uint4*>(yrow + 64 * at + 8 * h) = yv;
               }
