@@ -59,6 +59,7 @@ extern "C" {
 #define SLORA_ERR_CUDA (-6)         /* a CUDA runtime call failed (see error string) */
 #define SLORA_ERR_DEVICE (-7)       /* a kernel reported bad input (see slora_device_status) */
 #define SLORA_ERR_TIMEOUT (-8)      /* a kernel's bounded wait gave up (device status only) */
+#define SLORA_ERR_DEVICE_ASSERT (-9) /* a bounds check of the SLORA_DEBUG build failed (device status only) */
 
 /* ---- element types and apply modes -------------------------------------- */
 #define SLORA_F16 0
@@ -347,6 +348,26 @@ int slora_set_tc_min_batch(slora_pool* pool, int32_t min_tokens);
 #define SLORA_FAULT_PAGE_ALLOC 1
 #define SLORA_FAULT_COPY 2
 int slora_debug_set_fault(slora_pool* pool, int32_t kind, int64_t nth);
+
+/*
+ * The SLORA_DEBUG build (libslora_debug.so, compiled with -DSLORA_DEBUG;
+ * the Python binding loads it when the environment has SLORA_DEBUG=1)
+ * checks, in every kernel, each page index it reads from a page table
+ * against the pool's page count and each token index it reads from the
+ * token order against the batch size.  A violation is reported by
+ * slora_device_status as SLORA_ERR_DEVICE_ASSERT (the index is replaced by
+ * 0, so no access leaves its buffer and no kernel waits for a copy that
+ * never comes); results of that call are then meaningless.  Other builds
+ * compile no checks.
+ *
+ * slora_debug_poke_page_table writes `value` into entry `entry` of the
+ * pool's device page table (entries of adapter a start at a * stride) and
+ * returns the previous value in *old: a test plants a bad page index and
+ * puts the old one back.  The host copy of the table is not changed.  Only
+ * in the SLORA_DEBUG build; other builds return SLORA_ERR_INVALID.  Not for
+ * serving: the next apply reads the planted value.
+ */
+int slora_debug_poke_page_table(slora_pool* pool, int64_t entry, int32_t value, int32_t* old);
 
 /*
  * Polls that each of the CUDA-core apply kernel's waits on other warps

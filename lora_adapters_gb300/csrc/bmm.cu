@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(kBmmThreads) bmm_map_kernel(const __grid_const
       if (d.seg_start[mid] <= j) lo = mid;
       else hi = mid - 1;
     }
-    d.tok_seg[d.perm[j]] = lo;
+    d.tok_seg[dbg_index(d.perm[j], d.T, d.error)] = lo;
   }
 }
 
@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(kBmmThreads) bmm_gather_kernel(const __grid_co
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
       if (k < r) {
         const int e = c8 * 8, chunk = e / d.H;
-        const int page = pt[(int64_t)r * d.rows_before + (int64_t)k * d.ppi + chunk];
+        const int page = dbg_index(pt[(int64_t)r * d.rows_before + (int64_t)k * d.ppi + chunk], d.num_pages, d.error);
         v = *reinterpret_cast<const uint4*>(d.pool + (int64_t)page * d.H + (e - chunk * d.H));
       }
       *reinterpret_cast<uint4*>(arow + c8 * 8) = v;
@@ -75,7 +75,8 @@ __global__ void __launch_bounds__(kBmmThreads) bmm_gather_kernel(const __grid_co
       float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
       if (k < r) {
         const int e = c8 * 8, chunk = e / d.H;
-        const int page = pt[(int64_t)r * (d.rows_before + d.ppi) + (int64_t)k * d.ppo + chunk];
+        const int page =
+            dbg_index(pt[(int64_t)r * (d.rows_before + d.ppi) + (int64_t)k * d.ppo + chunk], d.num_pages, d.error);
         const uint4 v = *reinterpret_cast<const uint4*>(d.pool + (int64_t)page * d.H + (e - chunk * d.H));
         const uint16_t* h = reinterpret_cast<const uint16_t*>(&v);
 #pragma unroll

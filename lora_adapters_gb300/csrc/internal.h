@@ -123,8 +123,32 @@ struct ApplyDev {
   // barrier opens).  Zero-initialised with the pool.
   int32_t* grid_sync;
   uint32_t wait_limit;           // polls of a wait on other warps before it gives up (0: kWaitLimit)
+  int64_t num_pages;             // pages of the pool (0: unknown, page indices not checked)
+  int32_t T;                     // tokens of the batch
 };
 enum : int { kSyncCount = 0, kSyncGen = 1, kGridSyncInts = 2 };
+
+// Bounds checks of the SLORA_DEBUG build (no code in other builds): an index
+// read from a page table or a token order and used to address memory is
+// checked against its range (bound <= 0: no range known); one outside it is
+// reported in the device error word as SLORA_ERR_DEVICE_ASSERT and replaced
+// by 0, so that the access stays in bounds and every copy a barrier expects
+// still arrives.  No trap.
+constexpr int32_t kErrDeviceAssert = -9;   // == SLORA_ERR_DEVICE_ASSERT
+#ifdef __CUDACC__
+__device__ __forceinline__ int dbg_index(int v, int64_t bound, int32_t* err) {
+#ifdef SLORA_DEBUG
+  if (bound > 0 && (v < 0 || (int64_t)v >= bound)) {
+    if (err) atomicCAS(err, 0, kErrDeviceAssert);
+    return 0;
+  }
+#else
+  (void)bound;
+  (void)err;
+#endif
+  return v;
+}
+#endif
 
 // Column tiles of a row of h_out elements over pages of H: tiles of at most
 // kExpandCols columns that never cross a page boundary.
@@ -202,6 +226,8 @@ struct BmmDev {
   void* y;
   int64_t ldy;
   float s;
+  int64_t num_pages;             // pages of the pool (bounds checks of the SLORA_DEBUG build)
+  int32_t* error;                // device error word
 };
 cudaError_t launch_bmm_gather(const BmmDev& d, int dtype, int grid, cudaStream_t st);
 cudaError_t launch_bmm_epilogue(const BmmDev& d, int dtype, int grid, cudaStream_t st);

@@ -1031,7 +1031,7 @@ __device__ __forceinline__ void load_b_pages(const ApplyDev& d, int a, int r, in
 #pragma unroll
   for (int m = 0; m < kPagesPerLane; ++m) {
     const int row = lane + 32 * m;
-    pg[m] = row < r ? __ldg(ptB + (int64_t)row * P.ppo) : 0;
+    pg[m] = row < r ? dbg_index(__ldg(ptB + (int64_t)row * P.ppo), d.num_pages, d.error) : 0;
   }
 }
 
@@ -1228,10 +1228,10 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
                             (int64_t)m_k0 * P.ppi;
 #pragma unroll
         for (int i = 0; i < kShrinkRows; ++i)
-          if (i < m_nrows) pg[i] = __ldg(pt + (int64_t)i * P.ppi);
+          if (i < m_nrows) pg[i] = dbg_index(__ldg(pt + (int64_t)i * P.ppi), d.num_pages, d.error);
 #pragma unroll
         for (int t = 0; t < kTT; ++t)
-          if (t < m_ntok) xt[t] = __ldg(d.perm + m_j0 + t);
+          if (t < m_ntok) xt[t] = dbg_index(__ldg(d.perm + m_j0 + t), d.T, d.error);
       }
       for (int l = 0; l < nb && ok; ++l) {
         const int p = __shfl_sync(0xffffffffu, m_p, l);
@@ -1262,7 +1262,7 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
         for (int c = 0; c < P.ppi && ok; ++c) {
           const int lenc = min(d.H, P.h_in - c * d.H);
           // the next page of this lane's row, fetched while this one streams
-          const int next = (has_row && c + 1 < P.ppi) ? __ldg(pt_row + c + 1) : 0;
+          const int next = (has_row && c + 1 < P.ppi) ? dbg_index(__ldg(pt_row + c + 1), d.num_pages, d.error) : 0;
           for (int o = 0; o < lenc; o += kShrinkK) {
             const int len = min(kShrinkK, lenc - o);
             const int last = (c == P.ppi - 1) && (o + len >= lenc);
@@ -1320,7 +1320,7 @@ __global__ void __launch_bounds__(kCcThreads, 1) apply_cc_kernel(const __grid_co
         col_tile(ct, d.proj[m_p].h_out, d.H, m_c, m_o, m_len);
 #pragma unroll
         for (int t = 0; t < kTT; ++t)
-          if (t < m_ntok) rws[t] = __ldg(d.perm + m_j0 + t);
+          if (t < m_ntok) rws[t] = dbg_index(__ldg(d.perm + m_j0 + t), d.T, d.error);
       }
       int pg[kPagesPerLane];
       load_b_pages(d, __shfl_sync(0xffffffffu, m_a, 0), __shfl_sync(0xffffffffu, m_r, 0),

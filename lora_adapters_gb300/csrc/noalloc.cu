@@ -211,6 +211,8 @@ extern "C" int slora_lora_apply_noalloc(const void* d_pool, int32_t page_elems, 
   d.v_ld = kMaxRank;
   d.s = s;
   d.error = err;
+  d.num_pages = 0;   // the caller's pool size is not known here: page indices are not checked
+  d.T = T;
   ProjDev& P = d.proj[0];
   P.x = d_x;
   P.ldx = ldx;

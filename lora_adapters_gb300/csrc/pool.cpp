@@ -917,6 +917,8 @@ int slora_lora_apply_multi(slora_pool* p, const slora_segments* seg, int32_t n, 
   d.off_n = std::min<int32_t>(kSegSmem, std::max(1, std::min(p->seg_T, p->max_adapters)) + 1);
   d.s = s;
   d.wait_limit = p->wait_limit;
+  d.num_pages = p->num_pages;
+  d.T = p->seg_T;
   for (int i = 0; i < n; ++i) {
     const int q = projs[i];
     if (q < 0 || q >= p->num_proj) return fail(SLORA_ERR_INVALID, "projection %d out of range", q);
@@ -1072,6 +1074,8 @@ int slora_lora_apply_bmm(slora_pool* p, const slora_segments* seg, int32_t proj,
   d.scale = p->d_scale;
   d.T = T;
   d.r_pad = r_pad;
+  d.num_pages = p->num_pages;
+  d.error = p->d_error;
   d.h_in = h_in;
   d.h_out = h_out;
   d.ppi = p->ppi[proj];
@@ -1208,6 +1212,25 @@ int slora_debug_set_fault(slora_pool* p, int32_t kind, int64_t nth) {
   for (int64_t& f : p->fault_left) f = 0;
   if (kind != SLORA_FAULT_NONE) p->fault_left[kind] = nth;
   return SLORA_OK;
+}
+
+int slora_debug_poke_page_table(slora_pool* p, int64_t entry, int32_t value, int32_t* old) {
+  SLORA_RANGE("slora_debug_poke_page_table");
+  if (int rc = check_device_pool(p)) return rc;
+#ifdef SLORA_DEBUG
+  if (!old) return fail(SLORA_ERR_INVALID, "old is NULL");
+  if (entry < 0 || entry >= (int64_t)p->max_adapters * p->pt_stride)
+    return fail(SLORA_ERR_INVALID, "entry %lld outside the page table", (long long)entry);
+  CUDA_TRY(cudaStreamSynchronize(p->compute));
+  CUDA_TRY(cudaMemcpy(old, p->d_pt + entry, sizeof(int32_t), cudaMemcpyDeviceToHost));
+  CUDA_TRY(cudaMemcpy(p->d_pt + entry, &value, sizeof(int32_t), cudaMemcpyHostToDevice));
+  return SLORA_OK;
+#else
+  (void)entry;
+  (void)value;
+  (void)old;
+  return fail(SLORA_ERR_INVALID, "slora_debug_poke_page_table exists only in the SLORA_DEBUG build");
+#endif
 }
 
 int slora_debug_set_wait_limit(slora_pool* p, uint32_t polls) {

@@ -290,7 +290,8 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
 #pragma unroll
       for (int j = 0; j < kShMaxRows; ++j)
         xrow[j] = j < nxr ? static_cast<const uint16_t*>(P.x) +
-                                (int64_t)__ldg(d.perm + su.j0 + row0 + kLoaderRowStep * j) * P.ldx
+                                (int64_t)dbg_index(__ldg(d.perm + su.j0 + row0 + kLoaderRowStep * j), d.T, d.error) *
+                                    P.ldx
                           : nullptr;
       int chunk = -1;
       int pg[kShMaxRows];
@@ -300,7 +301,8 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
           chunk = c;
 #pragma unroll
           for (int j = 0; j < kShMaxRows; ++j)
-            pg[j] = j < nrow ? __ldg(pt + (int64_t)(row0 + kLoaderRowStep * j) * P.ppi + c) : 0;
+            pg[j] = j < nrow ? dbg_index(__ldg(pt + (int64_t)(row0 + kLoaderRowStep * j) * P.ppi + c), d.num_pages, d.error)
+                             : 0;
         }
         if (!mbar_wait(&sm.empty[stage], phase ^ 1)) {
           ok = false;
@@ -627,7 +629,7 @@ __global__ void __launch_bounds__(kExpandTcThreads, 1) tc_expand_kernel(const __
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int row = 4 * k4 + i;
-          pg[i] = __ldg(ptB + (int64_t)(row < u.r ? row : 0) * P.ppo);
+          pg[i] = dbg_index(__ldg(ptB + (int64_t)(row < u.r ? row : 0) * P.ppo), d.num_pages, d.error);
         }
         const int kb = kb0 + (4 * k4) / kTcK, kr = (4 * k4) % kTcK;
         for (int nb = 0; nb < natoms; ++nb)
@@ -641,10 +643,10 @@ __global__ void __launch_bounds__(kExpandTcThreads, 1) tc_expand_kernel(const __
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int m = 4 * lane + i;
-          tok[i] = __ldg(d.perm + j0 + (m < len ? m : 0));
+          tok[i] = dbg_index(__ldg(d.perm + j0 + (m < len ? m : 0)), d.T, d.error);
         }
         const int t_first = __shfl_sync(0xffffffffu, tok[0], 0);
-        const bool run = __ldg(d.perm + j0 + len - 1) - t_first == len - 1;
+        const bool run = dbg_index(__ldg(d.perm + j0 + len - 1), d.T, d.error) - t_first == len - 1;
         const int n16 = (len + 15) >> 4, nx4 = (len + 3) >> 2;
         // y tile
         const int yb = (int)(ny % kEBufs);
@@ -777,10 +779,10 @@ __global__ void __launch_bounds__(kExpandTcThreads, 1) tc_expand_kernel(const __
       for (int mt = 0; mt < u.ntm && ok; ++mt) {
         const int j0 = u.start + mt * kTcM;
         const int len = min(kTcM, u.start + u.len - j0);
-        const int token = m < len ? __ldg(d.perm + j0 + m) : 0;
-        const int t_first = __ldg(d.perm + j0);
-        const bool tma_out =
-            len == kTcM && u.ncols == kTcNe && __ldg(d.perm + j0 + kTcM - 1) - t_first == kTcM - 1;
+        const int token = m < len ? dbg_index(__ldg(d.perm + j0 + m), d.T, d.error) : 0;
+        const int t_first = dbg_index(__ldg(d.perm + j0), d.T, d.error);
+        const bool tma_out = len == kTcM && u.ncols == kTcNe &&
+                             dbg_index(__ldg(d.perm + j0 + kTcM - 1), d.T, d.error) - t_first == kTcM - 1;
         const int ab = (int)(nt % kEBufs);
         const uint32_t ph = (nt / kEBufs) & 1;
         if (!wait_lane0(&sm.tfull[ab], ph) || !wait_lane0(&sm.y_full[ab], ph)) {

@@ -17,7 +17,10 @@ from typing import List, Optional, Sequence
 import numpy as np
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libslora.so")
+# SLORA_DEBUG=1 in the environment selects the build with bounds checks in
+# every kernel (libslora_debug.so); either way the library must exist.
+DEBUG = os.environ.get("SLORA_DEBUG", "") == "1"
+LIB_PATH = os.path.join(HERE, "libslora_debug.so" if DEBUG else "libslora.so")
 
 OK = 0
 ERR_INVALID = -1
@@ -28,6 +31,7 @@ ERR_BUSY = -5
 ERR_CUDA = -6
 ERR_DEVICE = -7
 ERR_TIMEOUT = -8
+ERR_DEVICE_ASSERT = -9
 F16, BF16 = 0, 1
 MODE_AUTO, MODE_DECODE, MODE_PREFILL = 0, 1, 2
 
@@ -39,6 +43,7 @@ EXPORTED = (
     "slora_last_error_string", "slora_lora_apply_noalloc", "slora_adapter_set_scale",
     "slora_lora_apply_bmm", "slora_bmm_scratch_bytes", "slora_set_tc_min_batch", "slora_debug_set_fault",
     "slora_debug_set_wait_limit", "slora_adapter_ready", "slora_build_segments_for",
+    "slora_debug_poke_page_table",
 )
 FAULT_NONE, FAULT_PAGE_ALLOC, FAULT_COPY = 0, 1, 2
 
@@ -84,6 +89,7 @@ _SIGS = {
     "slora_set_tc_min_batch": [P, I32],
     "slora_debug_set_fault": [P, I32, I64],
     "slora_debug_set_wait_limit": [P, ctypes.c_uint32],
+    "slora_debug_poke_page_table": [P, I64, I32, P],
     "slora_lora_apply_noalloc": [P, I32, I32, P, I64, P, I32, I32, P, P, I32, P, I32, P, I64, P, I64,
                                  ctypes.c_float, P, P],
 }
@@ -94,7 +100,8 @@ def lib() -> ctypes.CDLL:
     global _lib
     if _lib is None:
         if not os.path.exists(LIB_PATH):
-            raise ImportError(f"libslora.so not built at {LIB_PATH}: run lora_adapters_gb300.build.build()")
+            raise ImportError(f"{os.path.basename(LIB_PATH)} not built at {LIB_PATH}: "
+                              "run lora_adapters_gb300.build.build()")
         L = ctypes.CDLL(LIB_PATH)
         for name, args in _SIGS.items():
             f = getattr(L, name)
@@ -284,6 +291,13 @@ def slora_debug_set_fault(pool: int, kind: int, nth: int) -> None:
 
 def slora_debug_set_wait_limit(pool: int, polls: int) -> None:
     _check(lib().slora_debug_set_wait_limit(pool, polls), "slora_debug_set_wait_limit")
+
+
+def slora_debug_poke_page_table(pool: int, entry: int, value: int) -> int:
+    """Writes one device page-table entry (SLORA_DEBUG build only); returns the old value."""
+    old = ctypes.c_int32(0)
+    _check(lib().slora_debug_poke_page_table(pool, entry, value, ctypes.byref(old)), "slora_debug_poke_page_table")
+    return old.value
 
 
 NOALLOC_MAX_TOKENS = 2048

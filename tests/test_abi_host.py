@@ -42,6 +42,20 @@ def test_library_exports_every_declared_symbol(S):
     assert declared <= set(S.EXPORTED) | {n for n in declared if hasattr(lib, n)}
 
 
+def test_debug_library_builds_and_exports_every_declared_symbol():
+    """The SLORA_DEBUG build (bounds checks in every kernel) compiles and
+    exports the same calls; it is loaded here without any GPU work."""
+    import ctypes
+
+    from lora_adapters_gb300 import build
+
+    path = build.build(debug=True)
+    assert path.endswith("libslora_debug.so")
+    lib = ctypes.CDLL(path)
+    for name in sorted(_declared_symbols()):
+        assert hasattr(lib, name), name
+
+
 def _planning_pool(S, wl, max_adapters=None, max_rank=None):
     sp = wl.spec
     return S.Pool(wl.pool_pages, wl.H, sp.dtype, [(p.h_in, p.h_out) for p in sp.projections],
