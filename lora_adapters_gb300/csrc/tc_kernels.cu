@@ -486,8 +486,8 @@ constexpr int kTcNe = 128;                        // expand column tile
 constexpr int kEAtoms = kTcNe / 64;               // 64-column swizzle atoms per tile
 constexpr int kEKBlocks = kMaxRank / kTcK;        // B row blocks of 64 ranks
 constexpr int kEBufs = 3;                         // y tiles and TMEM accumulators in flight
-// warps: 0 y tiles and B rows, 1 MMAs, 2-5 epilogue, 6 v halves
-constexpr int kExpandTcThreads = kTcThreads + 32;
+// warps: 0 y tiles and B rows, 1 MMAs, 2-5 epilogue, 6 v halves, 7 y stores
+constexpr int kExpandTcThreads = kTcThreads + 64;
 constexpr int kETmemCols = 512;                   // power of two >= kEBufs * kTcNe
 static_assert(kEBufs * kTcNe <= kETmemCols, "accumulators must fit the TMEM allocation");
 struct TcExpandSmem {
@@ -759,7 +759,7 @@ __global__ void __launch_bounds__(kExpandTcThreads, 1) tc_expand_kernel(const __
       }
       __syncwarp();
     }
-  } else {  // ------------------------------------------------- epilogue (warps 2-5)
+  } else if (warp < 6) {  // --------------------------------------- epilogue (warps 2-5)
     // Per token tile: 64 accumulator columns per TMEM round trip; the TMEM
     // buffer is released as soon as it has been read.  A tile of 128
     // consecutive tokens and 128 columns (the common prefill case) is written
@@ -807,11 +807,17 @@ __global__ void __launch_bounds__(kExpandTcThreads, 1) tc_expand_kernel(const __
           if (m < len) {
             uint8_t* ytile = sm.Y[ab][at] + m * kRowBytes;
             const int nch = min(8, (u.ncols - 64 * at) >> 3);   // 8-column chunks in this atom
+            // every chunk of the row first: the stores below could otherwise
+            // hold each load back (the compiler cannot tell the chunks apart)
+            uint4 yin[8];
+#pragma unroll
+            for (int h = 0; h < 8; ++h)
+              if (h < nch) yin[h] = *reinterpret_cast<const uint4*>(ytile + ((h ^ (m & 7)) << 4));
 #pragma unroll
             for (int h = 0; h < 8; ++h) {
               if (h < nch) {
                 uint8_t* py = ytile + ((h ^ (m & 7)) << 4);   // swizzled 16-byte chunk
-                uint4 yv = *reinterpret_cast<const uint4*>(py);
+                uint4 yv = yin[h];
                 uint32_t w[4];
                 memcpy(w, &yv, 16);
 #pragma unroll
@@ -831,26 +837,48 @@ __global__ void __launch_bounds__(kExpandTcThreads, 1) tc_expand_kernel(const __
         if (tma_out) fence_async_shared();   // the tile's new values, for the TMA engine
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.epi_done[ab]);
-        if (warp == 2 && lane == 0) {
-          // once the four warps are done with the y tile: store it (TMA) or
-          // just hand it back to the producer
-          if (!mbar_wait(&sm.epi_done[ab], ph)) {
-            ok = false;
-          } else {
-            if (tma_out) {
-#pragma unroll
-              for (int at = 0; at < kEAtoms; ++at)
-                tma_store_2d(&t.y128_map[u.p], col0 + 64 * at, t_first, sm.Y[ab][at]);
-              bulk_commit();
-              bulk_wait_read();   // the y tile may be refilled once the stores have read it
-            }
-            mbar_arrive(&sm.y_empty[ab]);
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       }
     }
-    if (warp == 2 && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");   // stores complete
+  } else {  // ------------------------------------------------------------ y stores
+    // Once the four epilogue warps are done with a y tile: store it (TMA,
+    // whole 128-byte rows) and, when the stores have read it, hand the
+    // buffer back to the producer; a tile stored piecewise by the epilogue
+    // goes back at once.  Apart from the epilogue warps, so that they start
+    // the next tile while the stores read this one.
+    uint32_t nt = 0;
+    TcERaw rw = tc_eunit_raw(t, blockIdx.x, per_seg, G);   // one unit ahead
+    for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x) {
+      const TcEUnit u = tc_eunit_done(rw);
+      rw = tc_eunit_raw(t, g + gridDim.x, per_seg, G);
+      if (u.ntm == 0) continue;
+      const int col0 = u.c * d.H + u.o;
+      for (int mt = 0; mt < u.ntm && ok; ++mt) {
+        const int j0 = u.start + mt * kTcM;
+        const int len = min(kTcM, u.start + u.len - j0);
+        const int t_first = dbg_index(__ldg(d.perm + j0), d.T, d.error);
+        const bool tma_out = len == kTcM && u.ncols == kTcNe &&
+                             dbg_index(__ldg(d.perm + j0 + kTcM - 1), d.T, d.error) - t_first == kTcM - 1;
+        const int ab = (int)(nt % kEBufs);
+        const uint32_t ph = (nt / kEBufs) & 1;
+        ++nt;
+        if (!wait_lane0(&sm.epi_done[ab], ph)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          if (tma_out) {
+#pragma unroll
+            for (int at = 0; at < kEAtoms; ++at)
+              tma_store_2d(&t.y128_map[u.p], col0 + 64 * at, t_first, sm.Y[ab][at]);
+            bulk_commit();
+            bulk_wait_read();   // the y tile may be refilled once the stores have read it
+          }
+          mbar_arrive(&sm.y_empty[ab]);
+        }
+        __syncwarp();
+      }
+    }
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");   // stores complete
   }
   if (!ok && lane == 0) report_err(d.error, kErrTimeout);
   tc_fence_before();
