@@ -56,17 +56,17 @@ DEFAULT_MODE = {"llama13b_mlp_decode": "decode", "llama7b_decode": "decode", "ll
 # changed.  The 13B MLP batch was captured in a compact pool holding only the
 # batch's adapters (--compact-pool: the same kernel work on the same rows).
 NCU_TRAFFIC = {
-    # apply_cc, 13B MLP decode (compact pool, same work): 793.68 MB read + 25.41 MB written (mean of 2 launches)
-    ("apply_cc", "llama13b_mlp_decode"): (819089664, "dcd9c9a6a1bb21ae"),
-    # apply_cc, 7B decode: 277.72 MB read + 0.89 MB written (mean of 2 launches)
-    ("apply_cc", "llama7b_decode"): (278612992, "dcd9c9a6a1bb21ae"),
-    # tc_expand, 7B prefill: 360.34 MB read + 217.87 MB written (mean of 2 launches)
-    ("expand_tc", "llama7b_prefill"): (578214400, "dcd9c9a6a1bb21ae"),
+    # apply_cc, 13B MLP decode (compact pool, same work): 793.62 MB read + 25.28 MB written (mean of 2 launches)
+    ("apply_cc", "llama13b_mlp_decode"): (818902528, "ee5a74a732d62f15"),
+    # apply_cc, 7B decode: 277.73 MB read + 0.94 MB written (mean of 2 launches)
+    ("apply_cc", "llama7b_decode"): (278662912, "ee5a74a732d62f15"),
+    # tc_expand, 7B prefill: 360.35 MB read + 218.00 MB written (mean of 2 launches)
+    ("expand_tc", "llama7b_prefill"): (578352640, "ee5a74a732d62f15"),
 }
 # ncu sm__pipe_tensor_cycles_active (% of active cycles) of the tensor-core
 # kernels on the prefill batch, with the kernel-source hash.
 NCU_TENSOR_PIPE = {
-    "llama7b_prefill": ({"expand_tc": 10.32, "shrink_tc": 18.79}, "dcd9c9a6a1bb21ae"),
+    "llama7b_prefill": ({"expand_tc": 10.88, "shrink_tc": 18.81}, "ee5a74a732d62f15"),
 }
 
 
