@@ -98,9 +98,11 @@ struct Elem<__nv_bfloat16> {
 // Warps: 1 issues the MMAs, 2-5 drain TMEM, 6-13 copy each stage's token
 // rows (x) and adapter rows (A); warp 0 has no role.  Rows go through the
 // load/store unit: each loader thread copies one 16-byte chunk column of every
-// 32nd row with cp.async, straight to its 128-byte-swizzled place, and (once
-// its copies have landed) fences them for the tensor cores' async proxy and
-// arrives on the stage.
+// 32nd row with cp.async, straight to its 128-byte-swizzled place, and has the
+// copies themselves arrive on the stage's barrier when they land
+// (cp.async.mbarrier.arrive), so a loader runs up to the whole ring ahead
+// without waiting for its own copies; the MMA warp fences the async proxy
+// after its wait, before the tensor cores read the stage.
 //
 // The K range of (tile, projection) is split into up to kShParts parts (units
 // of their own, so that a short list of tiles still spreads over the CTAs).
@@ -248,6 +250,9 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
           break;
         }
         tc_fence_after();
+        // the loaders' cp.async writes (generic proxy), ordered before this
+        // point by the barrier, become visible to the MMAs' async-proxy reads
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         if (lane == 0) {
           const uint32_t xa = smem_addr(sm.st[stage]), aa = xa + (uint32_t)su.tok * kRowBytes;
 #pragma unroll
@@ -273,10 +278,6 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
     const int ch = lt & 7;                  // 16-byte chunk column of the 128-byte row
     const int row0 = lt >> 3;               // rows row0, row0 + kLoaderRowStep, ...
     uint32_t stage = 0, phase = 0;
-    // Stages whose copies are committed but not yet announced: the last
-    // npend stages before `stage`.  Up to kLoaderLag of them stay in flight.
-    constexpr int kLoaderLag = kShrinkTcStages - 1;
-    int npend = 0;
     for (int64_t g = blockIdx.x; g < G && ok; g += gridDim.x) {
       const ShUnit su = sh_unit(t, sm.uoff, wide_ok, S, g);
       if (su.skip) continue;
@@ -326,17 +327,9 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
             cp16_shared_zfill(xbase + m * kRowBytes + ((ch ^ (m & 7)) << 4), xrow[j] + (xbytes ? e : 0), xbytes);
           }
         }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-        if (npend == kLoaderLag) {
-          // the oldest pending stage's copies have landed (no more than
-          // kLoaderLag newer groups are outstanding): make them visible to
-          // the tensor cores' async proxy, then announce them
-          asm volatile("cp.async.wait_group %0;" ::"n"(kLoaderLag) : "memory");
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          mbar_arrive(&sm.full[(stage + kShrinkTcStages - kLoaderLag) % kShrinkTcStages]);
-          --npend;
-        }
-        ++npend;
+        // one of the stage's kShrinkLoaders arrivals, made when all of this
+        // thread's copies so far have landed
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(&sm.full[stage])) : "memory");
         if (++stage == kShrinkTcStages) {
           stage = 0;
           phase ^= 1;
@@ -344,10 +337,6 @@ __global__ void __launch_bounds__(kShrinkTcThreads, 1) tc_shrink_kernel(const __
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
-    if (ok) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      for (int i = npend; i > 0; --i) mbar_arrive(&sm.full[(stage + kShrinkTcStages - i) % kShrinkTcStages]);
-    }
   } else {  // ------------------------------------------------- epilogue (warps 2-5)
     // Warp w owns TMEM lanes 32 (w % 4) .. +31: rank rows k (and k + 128 in
     // the second M block); accumulator columns are the tile's tokens.  For
