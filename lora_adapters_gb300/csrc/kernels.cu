@@ -247,8 +247,23 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
     hist[a] = 0;
     if (rank_smem) rank_s[a] = args.rank[a];
   }
-  if (keys_smem)
-    for (int i = tid; i < T; i += nthr) skeys[i] = args.token_adapter[i];
+  if (keys_smem) {
+    // kKeyBatch independent loads in flight per thread, then their stores
+    constexpr int kKeyBatch = 8;
+    for (int base = 0; base < T; base += kKeyBatch * nthr) {
+      int kv[kKeyBatch];
+#pragma unroll
+      for (int u = 0; u < kKeyBatch; ++u) {
+        const int i = base + u * nthr + tid;
+        kv[u] = i < T ? args.token_adapter[i] : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < kKeyBatch; ++u) {
+        const int i = base + u * nthr + tid;
+        if (i < T) skeys[i] = kv[u];
+      }
+    }
+  }
   for (int r = tid; r <= kMaxRank; r += nthr) rcount[r] = 0;
   if (tid == 0) {
     s_bad = 0;
@@ -355,30 +370,40 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
   }
   __syncthreads();
 
-  // (3a) stable scatter by runs: thread t owns tokens [lo, hi); a run starts
-  // wherever the key changes (runs of invalid tokens are listed too and
-  // placed nowhere)
+  // (3a) stable scatter by runs: warp w owns tokens [wlo, whi), its lanes
+  // taking consecutive tokens (so the stores of a warp are consecutive
+  // positions of a run); a run starts wherever the key changes (runs of
+  // invalid tokens are listed too and placed nowhere)
   bool scattered = false;
   if (keys_smem && T > nthr) {
-    const int m = (T + nthr - 1) / nthr;
-    const int lo = min(T, tid * m), hi = min(T, lo + m);
+    const int nwarps = nthr >> 5;
+    const int per_warp = ((T + nwarps - 1) / nwarps + 31) & ~31;
+    const int wlo = min(T, warp * per_warp), whi = min(T, wlo + per_warp);
+    const unsigned below = (1u << lane) - 1u;
     auto starts_run = [&](int i) -> bool { return i == 0 || skeys[i - 1] != skeys[i]; };
-    int v[1] = {0}, tot[1];
-    for (int i = lo; i < hi; ++i) v[0] += starts_run(i) ? 1 : 0;
+    int cnt = 0;
+    for (int i = wlo + lane; i < whi; i += 32) cnt += starts_run(i) ? 1 : 0;
+    cnt = __reduce_add_sync(0xffffffffu, cnt);
+    int v[1] = {lane == 0 ? cnt : 0}, tot[1];
     block_scan_excl<1>(v, tot, scan_sh);
+    const int wbase = __shfl_sync(0xffffffffu, v[0], 0);   // runs starting before wlo
     const int R = tot[0];
     // worth it only for few, long runs; the run list lives in the group arrays
     if (R < 32 * 32 && 8 * R <= T) {
       int* run_start = &grp_cnt[0][0];   // [R + 1]
       int* run_key = &grp_key[0][0];     // [R]
       int* run_base = &grp_base[0][0];   // [R]
-      int q = v[0];
-      for (int i = lo; i < hi; ++i)
-        if (starts_run(i)) {
-          run_start[q] = i;
-          run_key[q] = skeys[i];
-          ++q;
+      int q = wbase;
+      for (int i0 = wlo; i0 < whi; i0 += 32) {
+        const int i = i0 + lane;
+        const bool st = i < whi && starts_run(i);
+        const unsigned b = __ballot_sync(0xffffffffu, st);
+        if (st) {
+          run_start[q + __popc(b & below)] = i;
+          run_key[q + __popc(b & below)] = skeys[i];
         }
+        q += __popc(b);
+      }
       if (tid == 0) run_start[R] = T;
       __syncthreads();
       if (warp == 0) {
@@ -409,9 +434,11 @@ __global__ void __launch_bounds__(kSegThreads) build_segments_kernel(const SegBu
         }
       }
       __syncthreads();
-      int cur = v[0] - 1;   // the run holding token lo (token 0 always starts one)
-      for (int i = lo; i < hi; ++i) {
-        if (starts_run(i)) ++cur;
+      // the run holding token wlo (token 0 always starts one), then each
+      // lane moves forward to the run holding its own token
+      int cur = wbase - 1 + (wlo < whi && starts_run(wlo) ? 1 : 0);
+      for (int i = wlo + lane; i < whi; i += 32) {
+        while (run_start[cur + 1] <= i) ++cur;
         if (skeys[i] >= 0) sd.perm[run_base[cur] + (i - run_start[cur])] = i;
       }
       scattered = true;
