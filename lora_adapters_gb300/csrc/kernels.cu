@@ -696,9 +696,12 @@ __device__ __forceinline__ void small_block_scan(int (&v)[K], int (&excl)[K], in
 // blockDim of them; absent keys = INT_MAX): each warp sorts its 32 keys with
 // a bitonic network in registers and lays them out as a sorted run in
 // `runs`; a thread's rank is the sum over the runs of the keys below its own,
-// found by binary search.  Ends with the block synchronised.
-__device__ __forceinline__ int block_rank(int key, int* runs) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+// found by binary search, four runs' searches at a time.  Only the first
+// `live` warps may hold present keys (the other runs are all INT_MAX and
+// count nothing), so only their runs are searched.  Ends with the block
+// synchronised.
+__device__ __forceinline__ int block_rank(int key, int* runs, int live) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int v = key;
 #pragma unroll
   for (int k = 2; k <= 32; k <<= 1)
@@ -711,7 +714,8 @@ __device__ __forceinline__ int block_rank(int key, int* runs) {
   runs[warp * 32 + lane] = v;
   __syncthreads();
   int rank = 0;
-  for (int w = 0; w < nw; ++w) {
+#pragma unroll 4
+  for (int w = 0; w < live; ++w) {
     const int* r = runs + w * 32;
     int c = 0;   // keys of run w below `key`
 #pragma unroll
@@ -762,7 +766,7 @@ __global__ void __launch_bounds__(kSmallSegMax) build_segments_small_kernel(cons
   const int n_sorted = __syncthreads_count(valid);
 
   // (2) sorted position = keys below this one
-  const int pos = block_rank(ckey, s_key);
+  const int pos = block_rank(ckey, s_key, nthr >> 5);
   if (valid) {
     s_kr[pos] = key | (r << 16);
     sd.perm[pos] = tid;
@@ -798,7 +802,7 @@ __global__ void __launch_bounds__(kSmallSegMax) build_segments_small_kernel(cons
 
   // (4) work order: (256 - rank, segment) keys, ranked like (2)
   const int wkey = tid < S ? ((kMaxRank - s_rnk[tid]) << 10) | tid : 0x7fffffff;
-  const int q = block_rank(wkey, s_key);
+  const int q = block_rank(wkey, s_key, (S + 31) >> 5);
   if (tid < S) s_order[q] = tid;
   __syncthreads();
 
