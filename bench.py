@@ -56,17 +56,17 @@ DEFAULT_MODE = {"llama13b_mlp_decode": "decode", "llama7b_decode": "decode", "ll
 # changed.  The 13B MLP batch was captured in a compact pool holding only the
 # batch's adapters (--compact-pool: the same kernel work on the same rows).
 NCU_TRAFFIC = {
-    # apply_cc, 13B MLP decode (compact pool, same work): 793.62 MB read + 25.28 MB written (mean of 2 launches)
-    ("apply_cc", "llama13b_mlp_decode"): (818902528, "ee5a74a732d62f15"),
-    # apply_cc, 7B decode: 277.73 MB read + 0.94 MB written (mean of 2 launches)
-    ("apply_cc", "llama7b_decode"): (278662912, "ee5a74a732d62f15"),
-    # tc_expand, 7B prefill: 360.35 MB read + 218.00 MB written (mean of 2 launches)
-    ("expand_tc", "llama7b_prefill"): (578352640, "ee5a74a732d62f15"),
+    # apply_cc, 13B MLP decode (compact pool, same work): 793.70 MB read + 25.25 MB written (mean of 2 launches)
+    ("apply_cc", "llama13b_mlp_decode"): (818947584, "79ef4a8af322f883"),
+    # apply_cc, 7B decode: 277.73 MB read + 1.05 MB written (mean of 2 launches)
+    ("apply_cc", "llama7b_decode"): (278776192, "79ef4a8af322f883"),
+    # tc_expand, 7B prefill: 360.35 MB read + 217.89 MB written (mean of 2 launches)
+    ("expand_tc", "llama7b_prefill"): (578235392, "79ef4a8af322f883"),
 }
 # ncu sm__pipe_tensor_cycles_active (% of active cycles) of the tensor-core
 # kernels on the prefill batch, with the kernel-source hash.
 NCU_TENSOR_PIPE = {
-    "llama7b_prefill": ({"expand_tc": 10.88, "shrink_tc": 18.81}, "ee5a74a732d62f15"),
+    "llama7b_prefill": ({"expand_tc": 10.91, "shrink_tc": 23.79}, "79ef4a8af322f883"),
 }
 
 
