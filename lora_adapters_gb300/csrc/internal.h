@@ -173,9 +173,9 @@ struct TcDev {
   uint16_t* vhi[kMaxProj];
   uint16_t* vlo[kMaxProj];
   int32_t v16_ld;                    // multiple of kTcK
-  // tc_shrink splits each (tile, projection) in two K halves: their partial
-  // sums (fp32, rows like v) and, per (tile, projection, 32-row quarter), a
-  // count of halves done (zero between calls)
+  // tc_shrink splits each (tile, projection)'s K range into up to
+  // kTcShrinkParts parts; their partial sums (fp32, rows like v) wait here
+  // for tc_combine
   float* vpart;                      // tc_shrink's partial sums, [kTcShrinkParts][kMaxProj][rows][v_ld] (by call position)
   int64_t vpart_part, vpart_proj;    // strides in floats
   int32_t tc_ncol[kMaxProj];         // expand column tiles per projection (tc_col_tiles)

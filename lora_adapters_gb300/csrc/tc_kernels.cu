@@ -8,7 +8,7 @@
 // operands from shared memory, fp32 accumulators in TMEM:
 //
 //   tc_shrink:  V^T[r x 256] = A[r x H_in] . X^T   (A rows = pages; rank on M, tokens on N)
-//   tc_combine: V = s_a (part 0 + part 1), written as V_hi and V_lo
+//   tc_combine: V = s_a (sum of tc_shrink's K parts), written as V_hi and V_lo
 //   tc_expand:  Y[128 x 128] += s * (V_hi + V_lo)[128 x r] . B[r x 128]
 //
 // tc_shrink copies token rows of x and adapter rows of A with cp.async into
