@@ -565,7 +565,11 @@ def measure(name, mode_name, args, rep, device, rank, world):
         if pipe and pipe[1] == src_hash:
             tensor["ncu_tensor_pipe_active_pct"] = pipe[0]
         roofline["tensor"] = tensor
-    launches = int(round(sum(c for k, (_, c) in kern.items() if k != "load_wait") / hook_steps)) * args.steps
+    # kernels behind each timing hook: the shrink_tc hook covers tc_shrink and
+    # the tc_combine launch that adds its K parts
+    per_hook = {"shrink_tc": 2}
+    launches = int(round(sum(c * per_hook.get(k, 1) for k, (_, c) in kern.items() if k != "load_wait")
+                         / hook_steps)) * args.steps
 
     # ---- end to end through the C ABI with host buffers.  Every step copies
     # its token ids, x and y in from pinned host memory and its y back out, as
