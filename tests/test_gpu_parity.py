@@ -4,6 +4,8 @@ Integer / index work (device page contents, perm, seg_start, seg_adapter,
 counts) must be bit-exact; y must satisfy |gpu - oracle| <= 5e-3 + 1e-2 |oracle|
 elementwise (fp16/bf16 storage, fp32 accumulation, one rounding).
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -120,6 +122,69 @@ def test_small_cases_all_modes(name):
         slora.slora_set_tc_threshold(case.pool.handle, thr)
         seg, _ = _run_and_check(case, slora.MODE_AUTO, want)
         _check_segments(case, seg)
+    case.pool.close()
+
+
+# Segment lengths on both sides of every tile size of both kernel families
+# (the CUDA-core kernel's 4-token tiles; the tensor-core kernels' 32-token
+# combine groups and 128- and 256-token tiles), each on an adapter of its own
+# so that each run is exactly one segment, over ranks from 1 to 256 (one and
+# two M blocks), with base-only runs between some of them.  The projections
+# have ragged K (320 = one page and a quarter) and ragged N (320 columns).
+EDGE_LENS = (1, 3, 4, 5, 31, 32, 33, 127, 128, 129, 255, 256, 257, 300)
+EDGE_RANKS = (1, 4, 9, 16, 64, 128, 129, 256, 8, 33, 100, 200, 2, 64)
+
+
+def _edge_workload(dtype: str, seed: int, token_adapter: np.ndarray) -> workloads.Workload:
+    sp = workloads.WorkloadSpec(
+        name="tile_edges", H=256, dtype=dtype,
+        projections=(workloads.Projection("a", 256, 320), workloads.Projection("b", 320, 256)),
+        num_adapters=len(EDGE_RANKS), rank_set=(1,), fixed_ranks=EDGE_RANKS, kind="decode", tokens=1,
+        pool_factor=1.3, s=0.7, seed=seed)
+    wl = workloads.make(sp)
+    return dataclasses.replace(wl, token_adapter=np.ascontiguousarray(token_adapter, dtype=np.int32),
+                               request_lens=None)
+
+
+def _edge_tokens() -> np.ndarray:
+    runs = []
+    for i, n in enumerate(EDGE_LENS):
+        runs.append(np.full(n, i, np.int32))
+        if i % 4 == 1:
+            runs.append(np.full(5, -1, np.int32))
+    return np.concatenate(runs)
+
+
+@pytest.mark.parametrize("dtype,seed", [("f16", 31), ("bf16", 32)])
+def test_tile_edges_all_modes(dtype, seed):
+    """Every row, in every mode and at AUTO splits on both sides of the tile
+    sizes, for segments whose lengths sit on every tile edge."""
+    wl = _edge_workload(dtype, seed, _edge_tokens())
+    case = G.build_case(wl)
+    want = None
+    for mode in MODES:
+        seg, want = _run_and_check(case, mode, want)
+        _check_segments(case, seg)
+    slora.slora_set_tc_min_batch(case.pool.handle, 0)
+    for thr in (0, 4, 33, 129, 257):
+        slora.slora_set_tc_threshold(case.pool.handle, thr)
+        _run_and_check(case, slora.MODE_AUTO, want)
+    case.pool.close()
+
+
+@pytest.mark.parametrize("adapter", [0, 7])
+def test_one_token_batch_all_modes(adapter):
+    """A batch of a single token (rank 1, or rank 256 with two M blocks):
+    every kernel path with one partial tile of one row."""
+    wl = _edge_workload("f16", 33, np.array([adapter], np.int32))
+    case = G.build_case(wl)
+    want = None
+    for mode in MODES:
+        seg, want = _run_and_check(case, mode, want)
+        _check_segments(case, seg)
+    slora.slora_set_tc_min_batch(case.pool.handle, 0)
+    slora.slora_set_tc_threshold(case.pool.handle, 1)
+    _run_and_check(case, slora.MODE_AUTO, want)
     case.pool.close()
 
 
