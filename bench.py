@@ -9,9 +9,9 @@ workloads, each a line of its own inside one printed JSON object:
   MLP decode batch -- H = 5120, gate/up 5120 -> 13824 and down 13824 -> 5120,
   512 tokens (one per request), 2000 adapters of ranks {16, 32, 64} resident
   in a 120 GB pool filled up with KV slots, token -> adapter Zipf(1.2), bf16;
-* ``configs[0]``: the Llama-7B-shaped decode batch -- q/k/v/o 4096 -> 4096,
+* the first entry of the line's ``configs`` list: the Llama-7B-shaped decode batch -- q/k/v/o 4096 -> 4096,
   256 tokens, 1000 adapters of ranks {8, 16, 32, 64}, Zipf(1), fp16;
-* ``configs[1]``: the Llama-7B-shaped prefill batch -- 32 requests of
+* the second entry: the Llama-7B-shaped prefill batch -- 32 requests of
   U{8..512} tokens, 200 adapters of ranks {8..128}, fp16, long segments on
   the tensor cores.
 
