@@ -383,7 +383,7 @@ const char* slora_last_error_string(void);
 
 /*
  * slora_lora_apply_noalloc -- y += s * (x A_a) B_a for one projection,
- * allocating nothing.  The paper has no counterpart of this entry point.
+ * allocating nothing.  The pages describe no counterpart of this entry point.
  *
  * For callers that cannot call cudaMalloc where they compute the delta: a
  * serving runtime that has handed all GPU memory to its own arena (page pool,
