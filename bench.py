@@ -583,11 +583,13 @@ def measure(name, mode_name, args, rep, device, rank, world):
     # adapter rows a step reads exceed L2 on the decode batches.
     # A step's inputs are staged in one contiguous pinned buffer -- the token
     # ids, every projection's x, then every y, each piece 256-byte aligned --
-    # and the device buffer of a set has the same layout.  A step that moves
-    # at most 64 MB goes in with one copy and comes out with one (issuing a
-    # copy costs the host about 10 us, which bounded the 7B decode step:
-    # 104 vs 135 us); larger steps copy piece by piece, which measured faster
-    # on the 13B batch (371 vs 385-391 us on three boxes out of four).
+    # and the device buffer of a set has the same layout.  Copies move up to
+    # kCopyChunk bytes each: few enough that issuing them (about 10 us of host
+    # time a copy) does not bound a small step, large enough that the two
+    # directions, sharing the link, interleave.  Measured: the 7B decode step
+    # (one copy each way) 104 us against 135 us with a copy per tensor; the
+    # 13B step (two each way) 340 us against 373 us with a copy per tensor
+    # and 339-391 us, depending on the box, with one each way.
     pieces = [ta] + list(xs) + list(y0)
     nbytes = [t.numel() * t.element_size() for t in pieces]
     offs, total = [], 0
@@ -611,8 +613,12 @@ def measure(name, mode_name, args, rep, device, rank, world):
     out_y = [torch.zeros(y_hi - y_lo, dtype=torch.uint8).pin_memory() for _ in sets]   # padding stays 0
     h2d = total
     d2h = y_hi - y_lo
-    whole_copies = h2d + d2h <= (64 << 20)
-    y_pieces = [(offs[i], nbytes[i]) for i in range(1 + len(xs), len(pieces))]
+    kCopyChunk = 32 << 20
+
+    def copy_chunks(dst, dst_off, src, src_off, n):
+        for c in range(0, n, kCopyChunk):
+            m = min(kCopyChunk, n - c)
+            dst[dst_off + c:dst_off + c + m].copy_(src[src_off + c:src_off + c + m], non_blocking=True)
     s_in = torch.cuda.Stream(device=device)
     s_out = torch.cuda.Stream(device=device)
     ev_in = [torch.cuda.Event() for _ in sets]
@@ -626,11 +632,7 @@ def measure(name, mode_name, args, rep, device, rank, world):
         buf, d_ta, d_xs, d_ys = sets[b]
         s_in.wait_event(ev_out[b])          # the result of the set's previous step has left it
         with torch.cuda.stream(s_in):
-            if whole_copies:
-                buf.copy_(pin_in, non_blocking=True)
-            else:
-                for o, n in zip(offs, nbytes):
-                    buf[o:o + n].copy_(pin_in[o:o + n], non_blocking=True)
+            copy_chunks(buf, 0, pin_in, 0, total)
             ev_in[b].record(s_in)
         stream.wait_event(ev_in[b])
         with torch.cuda.stream(stream):
@@ -639,11 +641,7 @@ def measure(name, mode_name, args, rep, device, rank, world):
             ev_comp[b].record(stream)
         s_out.wait_event(ev_comp[b])
         with torch.cuda.stream(s_out):
-            if whole_copies:
-                out_y[b].copy_(buf[y_lo:y_hi], non_blocking=True)
-            else:
-                for o, n in y_pieces:
-                    out_y[b][o - y_lo:o - y_lo + n].copy_(buf[o:o + n], non_blocking=True)
+            copy_chunks(out_y[b], 0, buf, y_lo, y_hi - y_lo)
             ev_out[b].record(s_out)
 
     for k in range(args.warmup):
@@ -673,8 +671,7 @@ def measure(name, mode_name, args, rep, device, rank, world):
     e2e = {"value": rep.rate(wl.T, e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
            "d2h_bytes_per_step": int(d2h), "ms_per_step": e_ms,
            "pipelining": f"{n_sets} buffer sets: later steps' inputs in and earlier steps' y out while a step "
-                         "computes; contiguous pinned staging, "
-                         + ("one copy in and one out per step" if whole_copies else "one copy per tensor"),
+                         f"computes; contiguous pinned staging, copies of at most {kCopyChunk >> 20} MB",
            "l2": "not flushed",
            "link": dict(link, note="one plain pinned copy of the step's input bytes (h2d) and of its output "
                                    "bytes (d2h), each alone: the end-to-end step cannot beat the larger "
