@@ -398,6 +398,21 @@ class Replicas:
 
 
 # ---------------------------------------------------------------- GPU arm
+def staging_layout(nbytes, align: int = 256):
+    """Offsets of pieces of the given sizes laid end to end, each starting on
+    an `align`-byte boundary, and the total size."""
+    offs, total = [], 0
+    for n in nbytes:
+        offs.append(total)
+        total += (n + align - 1) // align * align
+    return offs, total
+
+
+def copy_spans(n: int, chunk: int):
+    """(start, length) of the copies that move n bytes, at most `chunk` each."""
+    return [(c, min(chunk, n - c)) for c in range(0, n, chunk)]
+
+
 def _link_gbs(torch, device, h2d: int, d2h: int):
     """A plain pinned-memory copy of one step's bytes each way, alone: the
     link-bound floor of the end-to-end step."""
@@ -592,10 +607,7 @@ def measure(name, mode_name, args, rep, device, rank, world):
     # and 339-391 us, depending on the box, with one each way.
     pieces = [ta] + list(xs) + list(y0)
     nbytes = [t.numel() * t.element_size() for t in pieces]
-    offs, total = [], 0
-    for n in nbytes:
-        offs.append(total)
-        total += (n + 255) // 256 * 256
+    offs, total = staging_layout(nbytes)
     y_lo, y_hi = offs[1 + len(xs)], offs[-1] + nbytes[-1]
     pin_in = torch.zeros(total, dtype=torch.uint8).pin_memory()
     for t, o, n in zip(pieces, offs, nbytes):
@@ -616,8 +628,7 @@ def measure(name, mode_name, args, rep, device, rank, world):
     kCopyChunk = 32 << 20
 
     def copy_chunks(dst, dst_off, src, src_off, n):
-        for c in range(0, n, kCopyChunk):
-            m = min(kCopyChunk, n - c)
+        for c, m in copy_spans(n, kCopyChunk):
             dst[dst_off + c:dst_off + c + m].copy_(src[src_off + c:src_off + c + m], non_blocking=True)
     s_in = torch.cuda.Stream(device=device)
     s_out = torch.cuda.Stream(device=device)

@@ -77,3 +77,21 @@ def test_kernel_source_hash_ignores_comments(tmp_path, monkeypatch):
     assert bench._kernel_source_hash() == h0
     (d / "kernels.cu").write_text("int a = 2;\nint b;\n")
     assert bench._kernel_source_hash() != h0
+
+
+def test_staging_layout_aligns_and_separates_the_pieces():
+    sizes = [4 * 301, 2 * 256 * 5120, 2 * 512 * 13824, 2, 0, 2 * 7 * 33]
+    offs, total = bench.staging_layout(sizes)
+    assert offs[0] == 0 and all(o % 256 == 0 for o in offs)
+    ends = [o + n for o, n in zip(offs, sizes)]
+    assert all(e <= o2 for e, o2 in zip(ends, offs[1:]))        # no overlap, in order
+    assert total >= ends[-1] and total - ends[-1] < 256 and total % 256 == 0
+
+
+@pytest.mark.parametrize("n,chunk", [(0, 32), (1, 32), (32, 32), (33, 32), (58198016, 32 << 20), (100, 7)])
+def test_copy_spans_cover_every_byte_once(n, chunk):
+    spans = bench.copy_spans(n, chunk)
+    assert all(0 < m <= chunk for _, m in spans)
+    assert [c for c, _ in spans] == list(range(0, n, chunk))
+    assert sum(m for _, m in spans) == n
+    assert len(spans) == -(-n // chunk)
