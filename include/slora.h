@@ -226,6 +226,14 @@ int slora_adapter_pages(const slora_pool* pool, int32_t adapter_id, int32_t* out
  * stream).  d_token_adapter: device int32[T], ids in [-1, max_adapters);
  * 0 <= T <= max_tokens.  Fills *out with pool-owned device arrays (see
  * slora_segments) plus the internal work lists of the apply kernels.
+ *
+ * CUDA graphs: this call and the apply calls only enqueue work on the
+ * compute stream, so a step (segments, then one apply per layer) can be
+ * captured in a graph and replayed, as long as the compute stream is not
+ * the legacy default stream and no load of an adapter the batch uses is
+ * still copying when the capture is made (its wait would refer to a copy
+ * outside the graph).  A replay rebuilds the segments from the token ids
+ * then in the captured buffer.
  */
 int slora_build_segments(slora_pool* pool, const int32_t* d_token_adapter, int32_t T,
                          slora_segments* out);

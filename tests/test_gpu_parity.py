@@ -188,6 +188,57 @@ def test_one_token_batch_all_modes(adapter):
     case.pool.close()
 
 
+@pytest.mark.parametrize("mode,split", [(slora.MODE_DECODE, None), (slora.MODE_PREFILL, None),
+                                        (slora.MODE_AUTO, 33)])
+def test_cuda_graph_capture_replays_the_step(mode, split):
+    """The segment build and the multi-projection apply, captured in a CUDA
+    graph on the pool's compute stream (not the legacy default stream) and
+    replayed: every replay equals the eager call bit for bit and the oracle
+    within tolerance, in every mode (AUTO split between both kernel
+    families)."""
+    wl = _edge_workload("f16", 34, _edge_tokens())
+    sp = wl.spec
+    dims = [(p.h_in, p.h_out) for p in sp.projections]
+    cs = torch.cuda.Stream()
+    pool = slora.Pool(wl.pool_pages, wl.H, sp.dtype, dims, sp.num_adapters, max(EDGE_RANKS), wl.T,
+                      device="cuda", compute_stream=cs)
+    pool.replay(wl.pool_ops, wl.ranks, wl.adapter)
+    if split is not None:
+        slora.slora_set_tc_min_batch(pool.handle, 0)
+        slora.slora_set_tc_threshold(pool.handle, split)
+    torch.cuda.synchronize()
+    ta = torch.from_numpy(wl.token_adapter.copy()).cuda()
+    xs = [G.to_dev(wl.x(p), sp.dtype) for p in range(len(dims))]
+    y0 = [G.to_dev(wl.y_in(p), sp.dtype) for p in range(len(dims))]
+    ys = [y.clone() for y in y0]
+    projs = list(range(len(dims)))
+    with torch.cuda.stream(cs):
+        seg = pool.build_segments(ta)
+        pool.apply_multi(seg, projs, xs, ys, sp.s, mode)
+    torch.cuda.synchronize()
+    eager = [G.to_bits(y) for y in ys]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cs):
+        seg = pool.build_segments(ta)
+        pool.apply_multi(seg, projs, xs, ys, sp.s, mode)
+    opool_ = H.oracle_pool_for(wl, max_adapters=sp.num_adapters, max_rank=max(EDGE_RANKS))
+    case = G.GpuCase(wl, pool, ta, xs, ys, opool_, H.touched(wl.token_adapter))
+    want = G.oracle_outputs(case)
+    for _ in range(3):
+        for y, y_ in zip(ys, y0):
+            y.copy_(y_)
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        for p in projs:
+            got = G.to_bits(ys[p])
+            assert np.array_equal(got, eager[p]), f"projection {p}: replay differs from the eager call"
+            ok, err, bad = G.compare(got, want[p], sp.dtype)
+            assert ok, f"projection {p}: {bad} elements out of tolerance, max |err| {err}"
+    assert pool.status() == slora.OK
+    pool.close()
+
+
 def test_full_size_llama7b_decode():
     """The benchmark workload: H=4096, q/k/v/o, 256 tokens, 1000 adapters, Zipf 1."""
     wl = workloads.make("llama7b_decode")
